@@ -1,0 +1,405 @@
+/*
+ * Plain CPU oracle of the W4A16 Mixture-of-Experts expert layer.
+ *
+ * TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py load this library. It shares no
+ * code, header, table or helper with the CUDA path.
+ *
+ * Pages followed (all four restate one announcement):
+ *   [P3] "Perplexity Open Sources Lily: A Rust + Metal Inference Engine for
+ *        Qwen3.6-35B-A3B on Apple Silicon" (insight.aitobox.com), sections
+ *        "Three Workload Shapes", "Prefill: Keep Weights Packed, Keep Routing
+ *        on the GPU", "Decode: Minimize Bytes Moved Per Token".
+ *   [P1] "Perplexity Open Sources Lily : un moteur d'inference Rust + Metal
+ *        pour Qwen3.6-35B-A3B sur Apple Silicon" (cmedia.click), paragraphs
+ *        on the model, on quantisation and on routing.
+ *
+ * What the pages fix: a router scores 256 experts and picks eight, plus one
+ * shared expert that sees every token [P3 "Three Workload Shapes"]; weights
+ * are groupwise-affine 4-bit, 64 weights per group sharing a bf16 scale and
+ * bias, rebuilt to bf16 one tile at a time and accumulated in FP32 [P3
+ * "Prefill"]; routing keeps a histogram, a prefix scan, a scatter and a
+ * block map on the GPU [P3 "Prefill"]. Everything else (fp32 logit order,
+ * tie-break, softmax renormalisation over the selected experts, SwiGLU,
+ * weight-1 shared expert, gate/up row split, nibble order, block-map
+ * format, rounding points) is the layer's workload definition or a stated
+ * reading; each function below names the one it follows.
+ *
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fopenmp -shared -fPIC.
+ * -ffp-contract=off matters: the router's adds must not fuse into FMAs.
+ *
+ * Arithmetic: fp64 everywhere except the router logit, whose fp32 order is
+ * itself the definition (see orc_router_logit).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+/* bf16 bits -> value: the bf16 pattern is the high half of an IEEE binary32. */
+double orc_bf16_value(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* value -> bf16 bits, one rounding to nearest, ties to even, from the fp64
+ * value (not via fp32, which would round twice). bf16 keeps 8 significant
+ * bits; below 2^-126 the spacing is fixed at 2^-133 (subnormals). */
+uint16_t orc_bf16_rne(double v) {
+  if (isnan(v)) return 0x7FC0;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80;
+  int e;
+  frexp(a, &e);               /* a = m * 2^e, m in [0.5, 1) */
+  int ue = e - 8;             /* spacing of 8-significant-bit values here */
+  if (ue < -133) ue = -133;
+  double q = nearbyint(ldexp(a, -ue)); /* exact scaling; RNE to an integer */
+  double r = ldexp(q, ue);
+  if (r >= 0x1p128) return sign | 0x7F80;
+  float f = (float)r;         /* exact: r has at most 9 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return sign | (uint16_t)(u >> 16);
+}
+
+static float bf16_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* -------------------------------------------------------------- router -- */
+
+/* Router logit of one token against one expert row, fp32, in a fixed order.
+ *
+ * The pages say only that a router scores the experts [P3 "Three Workload
+ * Shapes"]; they fix no precision or summation order. Reading used: fp32
+ * products accumulated with correctly rounded fmaf into 32 partial sums,
+ * where partial L takes elements k = 8*(32*j + L) + i for j = 0..H/256-1,
+ * i = 0..7 in that order, starting from +0; the 32 partials are then
+ * combined pairwise across index distance 16, 8, 4, 2, 1 (partial L
+ * becomes a_L + a_{L xor d}), and the logit is partial 0. Requires
+ * H % 256 == 0. */
+float orc_router_logit(const uint16_t* x, const uint16_t* w, int H) {
+  float a[32], b[32];
+  for (int L = 0; L < 32; ++L) {
+    float acc = 0.0f;
+    for (int j = 0; j < H / 256; ++j)
+      for (int i = 0; i < 8; ++i) {
+        int k = 8 * (32 * j + L) + i;
+        acc = fmaf(bf16_f32(x[k]), bf16_f32(w[k]), acc);
+      }
+    a[L] = acc;
+  }
+  for (int d = 16; d >= 1; d >>= 1) {
+    for (int L = 0; L < 32; ++L) b[L] = a[L] + a[L ^ d];
+    memcpy(a, b, sizeof a);
+  }
+  return a[0];
+}
+
+/* logits[t][e] = router logit (+ bias[e] as one fp32 add when bias != NULL). */
+void orc_router_logits(const uint16_t* x, const uint16_t* w_r, const float* bias,
+                       int T, int H, int E, float* logits) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      float l = orc_router_logit(x + (size_t)t * H, w_r + (size_t)e * H, H);
+      if (bias) l = l + bias[e];
+      logits[(size_t)t * E + e] = l;
+    }
+}
+
+/* Top-K selection and renormalised softmax weights, per token.
+ *
+ * "a router scores 256 experts and picks eight" [P3 "Three Workload
+ * Shapes"]; softmax renormalised over the selected experts is the layer's
+ * workload definition. Readings: experts are ordered by logit descending,
+ * ties to the lower expert id, compared by value (so -0 == +0); slot k
+ * holds the k-th expert of that order. Selection is made on the logits
+ * (softmax is monotone, so the set is the same in exact arithmetic).
+ * w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), in fp64. */
+void orc_topk(const float* logits, int T, int E, int K, int32_t* ids,
+              float* w32, double* w64) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (size_t)t * E;
+    int sel[1024];
+    for (int k = 0; k < K; ++k) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        int taken = 0;
+        for (int j = 0; j < k; ++j) taken |= (sel[j] == e);
+        if (taken) continue;
+        if (best < 0 || l[e] > l[best]) best = e; /* strict: lower id keeps ties */
+      }
+      sel[k] = best;
+    }
+    double z = 0.0, ex[1024];
+    for (int k = 0; k < K; ++k) {
+      ex[k] = exp((double)l[sel[k]] - (double)l[sel[0]]);
+      z += ex[k];
+    }
+    for (int k = 0; k < K; ++k) {
+      ids[(size_t)t * K + k] = sel[k];
+      if (w32) w32[(size_t)t * K + k] = (float)(ex[k] / z);
+      if (w64) w64[(size_t)t * K + k] = ex[k] / z;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- plan -- */
+
+/* Histogram, exclusive scan, stable scatter and block map [P3 "Prefill":
+ * routing histogram, prefix scan, scatter and block map].
+ *
+ * Items are f = t*K + k (routed slot rows), R = T*K of them.
+ *   counts[e]      = #{f : ids[f] == e}
+ *   offsets[e]     = sum_{e' < e} counts[e'],  offsets[E] = R
+ *   sorted_rows[p] = f, scattered in ascending f (stable), row_pos[f] = p
+ *   block map      = for e ascending, rows [offsets[e] + r0, + min(BM, counts[e]-r0))
+ *                    as triples (e, offsets[e] + r0, nrows), r0 = 0, BM, ...;
+ *                    then, when n_shared == 1, triples (E, R + r0, nrows) over
+ *                    the T shared rows (token order).
+ * Returns the number of blocks, or -1 if an id is out of [0, E) or the map
+ * would exceed max_blocks. */
+int orc_plan(const int32_t* ids, int T, int E, int K, int n_shared, int BM,
+             int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
+             int32_t* row_pos, int32_t* block_map, int max_blocks) {
+  int R = T * K;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (int f = 0; f < R; ++f) {
+    if (ids[f] < 0 || ids[f] >= E) return -1;
+    counts[ids[f]]++;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int32_t* cur = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+  for (int e = 0; e < E; ++e) cur[e] = offsets[e];
+  for (int f = 0; f < R; ++f) {
+    int p = cur[ids[f]]++;
+    sorted_rows[p] = f;
+    row_pos[f] = p;
+  }
+  free(cur);
+  int nb = 0;
+  for (int e = 0; e < E; ++e)
+    for (int r0 = 0; r0 < counts[e]; r0 += BM) {
+      if (nb >= max_blocks) return -1;
+      int n = counts[e] - r0 < BM ? counts[e] - r0 : BM;
+      block_map[3 * nb + 0] = e;
+      block_map[3 * nb + 1] = offsets[e] + r0;
+      block_map[3 * nb + 2] = n;
+      nb++;
+    }
+  if (n_shared)
+    for (int r0 = 0; r0 < T; r0 += BM) {
+      if (nb >= max_blocks) return -1;
+      int n = T - r0 < BM ? T - r0 : BM;
+      block_map[3 * nb + 0] = E;
+      block_map[3 * nb + 1] = R + r0;
+      block_map[3 * nb + 2] = n;
+      nb++;
+    }
+  return nb;
+}
+
+/* ------------------------------------------------------------- dequant -- */
+
+/* Groupwise-affine 4-bit dequantisation [P3 "Prefill"; P1 paragraph on
+ * quantisation: 64 weights per group share a bf16 scale and bias].
+ * Matrix [N][Kd]: q[n][k] is nibble k%8 (bits 4*(k%8)..+3, low nibble first)
+ * of word qw[n][k/8]; group g = k/64 has scale s[n][g] and bias b[n][g].
+ * w = RNE_bf16(s*q + b). The fp64 sum s*q + b is exact whenever the two
+ * terms' exponents differ by less than 40; otherwise the small term is far
+ * below half a bf16 step of the large one and cannot move the rounding, so
+ * the result equals rounding the exact value once. */
+uint16_t orc_dequant_one(const uint32_t* qw, const uint16_t* s, const uint16_t* b,
+                         int Kd, int n, int k) {
+  uint32_t word = qw[(size_t)n * (Kd / 8) + k / 8];
+  int q = (int)((word >> (4 * (k % 8))) & 15u);
+  double sv = orc_bf16_value(s[(size_t)n * (Kd / 64) + k / 64]);
+  double bv = orc_bf16_value(b[(size_t)n * (Kd / 64) + k / 64]);
+  return orc_bf16_rne(sv * (double)q + bv);
+}
+
+void orc_dequant(const uint32_t* qw, const uint16_t* s, const uint16_t* b, int N,
+                 int Kd, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < Kd; ++k)
+      out[(size_t)n * Kd + k] = orc_dequant_one(qw, s, b, Kd, n, k);
+}
+
+/* ----------------------------------------------------------------- FFN -- */
+
+/* One expert's SwiGLU FFN on one bf16 input row, fp64 accumulation.
+ * Weights are the dequantised bf16 values (as doubles) of
+ *   gate_up [2I][H]: rows 0..I-1 gate, rows I..2I-1 up (concatenated),
+ *   down    [H][I].
+ * g_j = sum_k x_k*Wg[j][k], u_j = sum_k x_k*Wu[j][k] (k ascending),
+ * h_j = RNE_bf16(silu(g_j)*u_j), silu(g) = g/(1+exp(-g)),
+ * d_n = sum_j h_j*Wd[n][j] (j ascending).
+ * FP32-or-better accumulation and bf16 weights/activations into the
+ * contraction follow [P3 "Prefill"]; SwiGLU and the gate/up split are the
+ * layer's workload definition; h is rounded to bf16 because the second
+ * contraction takes bf16 operands, as the first does. */
+static void ffn_row(const double* wgu, const double* wd, const double* x, int H,
+                    int I, uint16_t* h_out, double* d_out) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  for (int j = 0; j < I; ++j) {
+    const double* rg = wgu + (size_t)j * H;
+    const double* ru = wgu + (size_t)(I + j) * H;
+    double g = 0.0, u = 0.0;
+    for (int k = 0; k < H; ++k) {
+      g += x[k] * rg[k];
+      u += x[k] * ru[k];
+    }
+    double a = g / (1.0 + exp(-g)) * u;
+    uint16_t hb = orc_bf16_rne(a);
+    if (h_out) h_out[j] = hb;
+    h[j] = orc_bf16_value(hb);
+  }
+  for (int n = 0; n < H; ++n) {
+    const double* r = wd + (size_t)n * I;
+    double acc = 0.0;
+    for (int j = 0; j < I; ++j) acc += h[j] * r[j];
+    d_out[n] = acc;
+  }
+  free(h);
+}
+
+static double* expand(const uint32_t* qw, const uint16_t* s, const uint16_t* b,
+                      int N, int Kd) {
+  double* w = (double*)malloc(sizeof(double) * (size_t)N * Kd);
+  for (int n = 0; n < N; ++n)
+    for (int k = 0; k < Kd; ++k)
+      w[(size_t)n * Kd + k] = orc_bf16_value(orc_dequant_one(qw, s, b, Kd, n, k));
+  return w;
+}
+
+/* Expert FFN for `nrows` input rows of one expert.
+ * x_rows: bf16 [nrows][H]; h_out: bf16 [nrows][I] or NULL; d_out: fp64 [nrows][H]. */
+void orc_expert_ffn(const uint32_t* q_gu, const uint16_t* s_gu, const uint16_t* b_gu,
+                    const uint32_t* q_d, const uint16_t* s_d, const uint16_t* b_d,
+                    int H, int I, const uint16_t* x_rows, int nrows,
+                    uint16_t* h_out, double* d_out) {
+  double* wgu = expand(q_gu, s_gu, b_gu, 2 * I, H);
+  double* wd = expand(q_d, s_d, b_d, H, I);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int r = 0; r < nrows; ++r) {
+    double* x = (double*)malloc(sizeof(double) * (size_t)H);
+    for (int k = 0; k < H; ++k) x[k] = orc_bf16_value(x_rows[(size_t)r * H + k]);
+    ffn_row(wgu, wd, x, H, I, h_out ? h_out + (size_t)r * I : NULL,
+            d_out + (size_t)r * H);
+    free(x);
+  }
+  free(wgu);
+  free(wd);
+}
+
+/* --------------------------------------------------------------- layer -- */
+
+/* Whole layer output for a subset of tokens.
+ *
+ * y[t][n] = RNE_bf16( sum_{k=0..K-1} w[t][k] * FFN_{ids[t][k]}(x_t)[n]
+ *                     + FFN_shared(x_t)[n] )
+ * summed in fp64 in slot order then the shared term (weight 1, no gate;
+ * "one shared expert that sees every token" [P3 "Three Workload Shapes"]).
+ * ids/w64 come from orc_topk (w in fp64). Experts with no selected token in
+ * the subset are never expanded. Expert e's weights start at
+ * q_gu + e*2I*H/8 etc.; the shared expert's arrays are separate (NULL when
+ * n_shared == 0).
+ * tok: token indices [ntok] into x; y_out: bf16 [ntok][H];
+ * d_slots (optional): fp64 [ntok][K+1][H] slot outputs (shared last). */
+void orc_layer_tokens(const uint16_t* x, int H, int E, int K, int I,
+                      const int32_t* ids, const double* w64,
+                      const uint32_t* q_gu, const uint16_t* s_gu, const uint16_t* b_gu,
+                      const uint32_t* q_d, const uint16_t* s_d, const uint16_t* b_d,
+                      const uint32_t* sq_gu, const uint16_t* ss_gu, const uint16_t* sb_gu,
+                      const uint32_t* sq_d, const uint16_t* ss_d, const uint16_t* sb_d,
+                      const int32_t* tok, int ntok, uint16_t* y_out, double* d_slots) {
+  size_t gu_w = (size_t)2 * I * (H / 8), gu_g = (size_t)2 * I * (H / 64);
+  size_t d_w = (size_t)H * (I / 8), d_g = (size_t)H * (I / 64);
+  int S = K + 1;
+  double* dsl = d_slots ? d_slots : (double*)calloc((size_t)ntok * S * H, sizeof(double));
+  int has_shared = sq_gu != NULL;
+  /* per expert (shared = E): gather the (token, slot) rows routed to it */
+  int* nrow = (int*)calloc((size_t)E + 1, sizeof(int));
+  for (int i = 0; i < ntok; ++i)
+    for (int k = 0; k < K; ++k) nrow[ids[(size_t)tok[i] * K + k]]++;
+  nrow[E] = has_shared ? ntok : 0;
+  for (int e = 0; e <= E; ++e) {
+    if (nrow[e] == 0) continue;
+    int* which = (int*)malloc(sizeof(int) * (size_t)nrow[e]); /* i*S + slot */
+    int m = 0;
+    for (int i = 0; i < ntok; ++i) {
+      if (e == E) { which[m++] = i * S + K; continue; }
+      for (int k = 0; k < K; ++k)
+        if (ids[(size_t)tok[i] * K + k] == e) which[m++] = i * S + k;
+    }
+    uint16_t* xr = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)m * H);
+    for (int r = 0; r < m; ++r)
+      memcpy(xr + (size_t)r * H, x + (size_t)tok[which[r] / S] * H, sizeof(uint16_t) * H);
+    double* d = (double*)malloc(sizeof(double) * (size_t)m * H);
+    if (e < E)
+      orc_expert_ffn(q_gu + e * gu_w, s_gu + e * gu_g, b_gu + e * gu_g, q_d + e * d_w,
+                     s_d + e * d_g, b_d + e * d_g, H, I, xr, m, NULL, d);
+    else
+      orc_expert_ffn(sq_gu, ss_gu, sb_gu, sq_d, ss_d, sb_d, H, I, xr, m, NULL, d);
+    for (int r = 0; r < m; ++r)
+      memcpy(dsl + (size_t)which[r] * H, d + (size_t)r * H, sizeof(double) * H);
+    free(d);
+    free(xr);
+    free(which);
+  }
+  free(nrow);
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < ntok; ++i)
+    for (int n = 0; n < H; ++n) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k)
+        acc += w64[(size_t)tok[i] * K + k] * dsl[((size_t)i * S + k) * H + n];
+      if (has_shared) acc += dsl[((size_t)i * S + K) * H + n];
+      y_out[(size_t)i * H + n] = orc_bf16_rne(acc);
+    }
+  if (!d_slots) free(dsl);
+}
+
+/* Unit-gain RMS normalisation between stacked layers:
+ * x'[n] = RNE_bf16( y[n] / sqrt(mean_n(y[n]^2) + 1e-6) ), y the bf16 layer
+ * output, fp64 arithmetic. The layer's workload stacks layers with each
+ * output feeding the next; without a normalisation the activations leave
+ * the bf16 range within a few layers, so the plainest normalisation (no
+ * learned gain) is the reading used. */
+void orc_rmsnorm_rows(const uint16_t* y, int T, int H, uint16_t* out) {
+  for (int t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int n = 0; n < H; ++n) {
+      double v = orc_bf16_value(y[(size_t)t * H + n]);
+      ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / H + 1e-6);
+    for (int n = 0; n < H; ++n)
+      out[(size_t)t * H + n] = orc_bf16_rne(orc_bf16_value(y[(size_t)t * H + n]) * inv);
+  }
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

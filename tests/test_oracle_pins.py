@@ -1,0 +1,301 @@
+"""Pins of the CPU oracle to facts other than itself: closed forms, library
+routines (torch's fp32->bf16 rounding, numpy's stable argsort, scipy's
+softmax), a standard floating-point error bound, the hand-worked one-token
+example under tests/golden/, invariants, and the independent brute-force
+dense reference (oracle/dense.py)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax
+
+import oracle
+import synth
+from oracle import dense
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32_bits(v):
+    return int(np.float32(v).view(np.uint32))
+
+
+def torch_bf16_bits(v32):
+    t = torch.tensor(np.asarray(v32, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().astype(np.uint16)
+
+
+# ------------------------------------------------------------------ bf16 --
+def test_bf16_rne_matches_torch_on_fp32_values():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(5000) * 10.0 ** rng.integers(-30, 30, 5000),
+                        np.float32([0.0, -0.0, 1.0, -1.0, 3.0e38, 1.0e-40, -2.5e-39])])
+    v = v.astype(np.float32)
+    want = torch_bf16_bits(v)
+    got = np.array([oracle.bf16_rne(float(a)) for a in v], np.uint16)
+    assert (got == want).all()
+
+
+def test_bf16_rne_ties_to_even_and_single_rounding():
+    one = 0x3F80
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8) == one              # tie -> even (1.0)
+    assert oracle.bf16_rne(1.0 + 3 * 2.0 ** -8) == one + 2      # tie -> even (up)
+    # just above a tie, below fp32 resolution: rounding via fp32 would tie to even
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8 + 2.0 ** -40) == one + 1
+    assert oracle.bf16_rne(-(1.0 + 2.0 ** -8 + 2.0 ** -40)) == 0x8000 | (one + 1)
+    assert oracle.bf16_rne(float("inf")) == 0x7F80
+    assert oracle.bf16_rne(3.5e38) == 0x7F80                    # overflow
+    for b in (0x0001, 0x3F80, 0x7F7F, 0xBF80, 0x0080):
+        assert oracle.bf16_rne(oracle.bf16_value(b)) == b
+
+
+# ---------------------------------------------------------------- router --
+def _bits(vals):
+    return synth.bf16_bits(np.asarray(vals, np.float64))
+
+
+def test_router_logit_error_bound_vs_exact():
+    """|L - exact| <= (H/32 + 5) * 2^-24 * sum|x w| (Higham, Accuracy and
+    Stability of Numerical Algorithms, sec. 3.1: recursive summation of n
+    terms errs by at most (n-1)u sum|x_i|; here each partial sums H/32
+    exact products, then 5 pairwise levels)."""
+    rng = np.random.default_rng(2)
+    for H in (256, 2048):
+        x = _bits(rng.standard_normal((8, H)))
+        w = _bits(rng.standard_normal((32, H)) / math.sqrt(H))
+        lg = oracle.router_logits(x, w)
+        xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+        wf = synth.bf16_bits_to_f32(w).astype(np.float64)
+        exact = xf @ wf.T
+        bound = (H / 32 + 5) * 2.0 ** -24 * (np.abs(xf) @ np.abs(wf).T)
+        assert (np.abs(lg - exact) <= bound).all()
+
+
+def test_router_logit_tree_order():
+    """The fixed fp32 order is observable: big values cancel or absorb
+    depending on which partial holds them."""
+    H = 256
+    B = 2.0 ** 24
+    w = np.zeros(H)
+    x = np.ones(H)
+    # partial 0 holds +B (k=0), partial 1 holds +1 (k=8), partial 16 holds -B (k=128)
+    w[0], w[8], w[128] = B, 1.0, -B
+    assert oracle.router_logits(_bits(x)[None], _bits(w)[None])[0, 0] == 1.0
+    # partial 0 holds +B, partial 1 holds -B, partial 16 holds +1: the +1 is
+    # absorbed at the distance-16 step (B + 1 rounds to B in fp32), result 0
+    w[:] = 0
+    w[0], w[8], w[128] = B, -B, 1.0
+    assert oracle.router_logits(_bits(x)[None], _bits(w)[None])[0, 0] == 0.0
+    # plain left-to-right summation would give 1 here: the order is not sequential
+    assert (np.float32(B) + np.float32(-B)) + np.float32(1.0) == 1.0
+
+
+def test_router_single_term_and_bias_exact():
+    H, E = 256, 4
+    x = np.zeros((1, H)); x[0, 77] = 1.5
+    w = np.zeros((E, H)); w[:, 77] = [0.25, -2.0, 3.0, 0.0]
+    bias = np.float32([0.5, 0.25, -1.0, 7.0])
+    lg = oracle.router_logits(_bits(x), _bits(w), bias)
+    assert lg.tolist() == [[0.375 + 0.5, -3.0 + 0.25, 4.5 - 1.0, 7.0]]
+
+
+# ------------------------------------------------------------------ top-k --
+def test_topk_ties_lower_id_and_uniform_weights():
+    g = json.load(open(os.path.join(GOLD, "tie_router.json")))
+    lg = np.zeros((1, 16), np.float32)
+    ids, w32, w64 = oracle.topk(lg, 2)
+    assert ids[0].tolist() == g["expected"]["ids"]
+    assert np.allclose(w64[0], g["expected"]["weights"], atol=0, rtol=1e-15)
+    lg = np.full((3, 256), -0.0, np.float32); lg[:, ::2] = 0.0   # -0 == +0
+    ids, _, w64 = oracle.topk(lg, 8)
+    assert (ids == np.arange(8)).all() and np.allclose(w64, 1 / 8)
+
+
+def test_topk_matches_lexsort_and_scipy_softmax():
+    rng = np.random.default_rng(3)
+    lg = rng.integers(-6, 6, size=(200, 64)).astype(np.float32) * 0.5   # many ties
+    K = 8
+    ids, w32, w64 = oracle.topk(lg, K)
+    E = lg.shape[1]
+    for t in range(lg.shape[0]):
+        order = np.lexsort((np.arange(E), -lg[t]))
+        assert ids[t].tolist() == order[:K].tolist()
+        assert np.allclose(w64[t], softmax(lg[t, order[:K]].astype(np.float64)), rtol=1e-13)
+    assert np.allclose(w64.sum(1), 1.0, atol=1e-14)
+    assert np.abs(w32 - w64).max() < 1e-7
+
+
+# ------------------------------------------------------------------- plan --
+@pytest.mark.parametrize("T,E,K,BM,skew", [(16, 16, 2, 128, 0), (513, 256, 8, 128, 0),
+                                           (300, 256, 8, 32, 1), (1, 256, 8, 16, 0),
+                                           (7, 4, 4, 1, 0)])
+def test_plan_invariants_and_stable_sort(T, E, K, BM, skew):
+    rng = np.random.default_rng(T + E)
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        ids = np.stack([rng.choice(E, K, replace=False, p=p / p.sum()) for _ in range(T)])
+    else:
+        ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)])
+    ids = ids.astype(np.int32)
+    P = oracle.plan(ids, E, 1, BM)
+    R = T * K
+    flat = ids.ravel()
+    assert (P["counts"] == np.bincount(flat, minlength=E)).all()
+    assert P["counts"].sum() == R
+    assert P["offsets"][0] == 0 and P["offsets"][-1] == R
+    assert (np.diff(P["offsets"]) == P["counts"]).all()
+    assert (P["sorted_rows"] == np.argsort(flat, kind="stable")).all()
+    assert (np.sort(P["sorted_rows"]) == np.arange(R)).all()
+    assert (P["row_pos"][P["sorted_rows"]] == np.arange(R)).all()
+    bm = P["block_map"]
+    assert P["num_blocks"] == sum(-(-int(c) // BM) for c in P["counts"]) + -(-T // BM)
+    assert ((bm[:, 2] >= 1) & (bm[:, 2] <= BM)).all()
+    assert bm[:, 2].sum() == R + T
+    for e, r0, n in bm:
+        if e < E:
+            assert (flat[P["sorted_rows"][r0:r0 + n]] == e).all()
+        else:
+            assert r0 >= R and r0 + n <= R + T
+    assert (np.diff(bm[:, 0]) >= 0).all()
+
+
+def test_plan_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        oracle.plan(np.array([[0, 16]], np.int32), 16, 1, 8)
+
+
+# ---------------------------------------------------------------- dequant --
+def test_dequant_nibble_order():
+    q = np.array([[0x76543210, 0xFEDCBA98] * 4], np.uint32)     # K = 64
+    s = _bits([[1.0]])
+    b = _bits([[0.0]])
+    got = synth.bf16_bits_to_f32(oracle.dequant(q, s, b))[0]
+    assert got.tolist() == list(range(16)) * 4
+
+
+def test_dequant_closed_form_all_q():
+    """b = -8s makes s*q + b = s*(q-8), exact in fp32; rounding that fp32
+    value to bf16 is torch's fp32->bf16 conversion. q-8 in {+-1,2,4,8,0}
+    must come out exactly s*(q-8)."""
+    rng = np.random.default_rng(4)
+    n = 2000
+    s = _bits(rng.uniform(0.002, 0.02, n) * 10.0 ** rng.integers(-3, 4, n))
+    sv = synth.bf16_bits_to_f32(s).astype(np.float64)
+    b = _bits(-8 * sv)
+    for qv in range(16):
+        word = sum(qv << (4 * i) for i in range(8))
+        q = np.full((n, 8), word, np.uint32)
+        got = oracle.dequant(q, s[:, None], b[:, None])
+        want = torch_bf16_bits((sv * (qv - 8)).astype(np.float32))
+        assert (got == want[:, None]).all(), qv
+        if qv - 8 in (0, 1, -1, 2, -2, 4, -4, -8):
+            assert (synth.bf16_bits_to_f32(got[:, 0]) == sv * (qv - 8)).all()
+
+
+def test_dequant_general_bias_matches_dense():
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 1 << 32, (64, 32), dtype=np.uint64).astype(np.uint32)
+    s = _bits(rng.uniform(-1, 1, (64, 4)))
+    b = _bits(rng.uniform(-3, 3, (64, 4)))
+    got = synth.bf16_bits_to_f32(oracle.dequant(q, s, b)).astype(np.float64)
+    assert (got == dense.dequant(q, s, b)).all()
+
+
+# -------------------------------------------------------------- hand case --
+def _hand_layer():
+    g = json.load(open(os.path.join(GOLD, "hand_worked_1token.json")))
+    sh = g["shape"]
+    H, E, I = sh["H"], sh["E"], sh["I"]
+    def word(n):
+        return sum(n << (4 * i) for i in range(8))
+    s = synth.bf16_bits(np.full(1, 2.0 ** -8))[0]
+    b = synth.bf16_bits(np.full(1, -8 * 2.0 ** -8))[0]
+    qgu = np.full((E, 2 * I, H // 8), word(9), np.uint32)
+    qd = np.full((E, H, I // 8), word(8), np.uint32)
+    qd[15] = word(10)
+    qd[14] = word(7)
+    L = synth.LayerInputs(
+        x=synth.bf16_bits(np.ones((1, H))),
+        w_router=synth.bf16_bits(np.repeat(np.arange(E)[:, None] / 1024.0, H, 1)),
+        router_bias=None,
+        q_gate_up=qgu, s_gate_up=np.full((E, 2 * I, H // 64), s, np.uint16),
+        b_gate_up=np.full((E, 2 * I, H // 64), b, np.uint16),
+        q_down=qd, s_down=np.full((E, H, I // 64), s, np.uint16),
+        b_down=np.full((E, H, I // 64), b, np.uint16),
+        sh_q_gate_up=qgu[:1].copy(), sh_s_gate_up=np.full((1, 2 * I, H // 64), s, np.uint16),
+        sh_b_gate_up=np.full((1, 2 * I, H // 64), b, np.uint16),
+        sh_q_down=np.full((1, H, I // 8), word(9), np.uint32),
+        sh_s_down=np.full((1, H, I // 64), s, np.uint16),
+        sh_b_down=np.full((1, H, I // 64), b, np.uint16))
+    return g, L
+
+
+def test_hand_worked_one_token():
+    g, L = _hand_layer()
+    ex = g["expected"]
+    ids, w32, w64 = oracle.route(L, g["shape"]["K"])
+    assert ids[0].tolist() == ex["ids"]
+    assert np.allclose(w64[0], ex["weights"], rtol=1e-15)
+    h, d = oracle.expert_ffn(L.q_gate_up[15], L.s_gate_up[15], L.b_gate_up[15],
+                             L.q_down[15], L.s_down[15], L.b_down[15], L.x)
+    assert (synth.bf16_bits_to_f32(h) == ex["h"]).all()
+    assert (d == ex["d"][0]).all()
+    y, dsl = oracle.layer_tokens(L, ids, w64, want_slots=True)
+    assert (dsl[0, 0] == ex["d"][0]).all() and (dsl[0, 1] == ex["d"][1]).all()
+    assert (dsl[0, 2] == ex["d"][2]).all()
+    assert (y == ex["y_bf16_bits"]).all()
+    assert synth.bf16_bits_to_f32(y[0, 0]) == ex["y_bf16"]
+
+
+# ------------------------------------------------------- dense brute force --
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_oracle_layer_vs_dense_brute_force(seed):
+    shape = synth.CONFIGS["tiny"].shape
+    L = synth.gen_layer(16, shape, seed=seed, zipf_s=1.1 if seed == 3 else 0.0)
+    ids, w32, w64 = oracle.route(L, shape.K)
+    y = oracle.layer_tokens(L, ids, w64)
+    yd, idd, wd, lg = dense.layer(L, shape.K)
+    # ids agree wherever the K-th / K+1-th exact gap exceeds the fp32 bound
+    srt = -np.sort(-lg, axis=1)
+    gap = srt[:, shape.K - 1] - srt[:, shape.K]
+    clear = gap > 1e-4
+    assert clear.sum() >= 12
+    assert (ids[clear] == idd[clear]).all()
+    assert np.abs(w64[clear] - wd[clear]).max() < 1e-5
+    yo = synth.bf16_bits_to_f32(y).astype(np.float64)[clear]
+    yr = yd[clear]
+    # the final bf16 rounding and h's bf16 rounding are the only gaps
+    assert np.abs(yo - yr).max() <= 1e-2 * np.abs(yr).max() + 1e-3
+    assert np.abs(yo - yr).sum() / np.abs(yr).sum() <= 2e-3
+
+
+def test_oracle_detects_planted_mistakes():
+    """A dropped shared term or a transposed down operand must break the
+    dense comparison (the pin has teeth)."""
+    shape = synth.CONFIGS["tiny"].shape
+    L = synth.gen_layer(16, shape, seed=7)
+    ids, w32, w64 = oracle.route(L, shape.K)
+    yd, *_ = dense.layer(L, shape.K)
+    y_ok = synth.bf16_bits_to_f32(oracle.layer_tokens(L, ids, w64)).astype(np.float64)
+    L2 = synth.gen_layer(16, shape, seed=7)
+    L2.sh_q_down = L2.sh_q_down * 0 + np.uint32(0x88888888)   # shared output -> 0
+    y_bad = synth.bf16_bits_to_f32(oracle.layer_tokens(L2, ids, w64)).astype(np.float64)
+    tol = 1e-2 * np.abs(yd).max() + 1e-3
+    assert np.abs(y_ok - yd).max() <= tol
+    assert np.abs(y_bad - yd).max() > tol
+    # swapped slot weights
+    y_sw = synth.bf16_bits_to_f32(oracle.layer_tokens(L, ids, w64[:, ::-1].copy())).astype(np.float64)
+    assert np.abs(y_sw - yd).max() > tol
+
+
+def test_rmsnorm_closed_form():
+    H = 256
+    y = np.zeros((2, H)); y[0, :] = 2.0; y[1, 0] = 3.0; y[1, 1] = 4.0
+    out = synth.bf16_bits_to_f32(oracle.rmsnorm_rows(synth.bf16_bits(y))).astype(np.float64)
+    assert np.allclose(out[0], 2.0 / math.sqrt(4.0 + 1e-6), rtol=2 ** -8)
+    r = math.sqrt(25.0 / H + 1e-6)
+    assert abs(out[1, 0] - 3 / r) <= 2 ** -8 * 3 / r and abs(out[1, 1] - 4 / r) <= 2 ** -8 * 4 / r
+    assert (out[1, 2:] == 0).all()
