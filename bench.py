@@ -1,0 +1,477 @@
+"""Throughput of the W4A16 MoE expert layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path (router logits + top-K, plan,
+gate_up+SwiGLU and down grouped GEMMs, combine) over one batch of seeded
+synthetic tokens with all weights resident in HBM. Workloads (synth.CONFIGS):
+  prefill  T=512, H=2048, 256 experts top-8 + 1 shared, I=512, 1 layer (default)
+  skewed   T=2048, same layer, Zipf(1.1)-shifted router logits
+  decode   T=1 through 40 stacked layers (one token of a decode step)
+  chunked  T=16384 as 8 chunks of 2048 through 40 stacked layers
+  tiny     T=16, H=256, 16 experts top-2 + 1 shared, I=128
+Weights of every layer (455.8 MB for the full shape) exceed the 129 MB L2,
+so no L2 flush is needed between steps; config says so.
+
+Prints one JSON line (rank 0). value = tokens/s of the whole job; e2e =
+the same through moe_layer_w4 with the step's hidden states copied from
+pinned host memory and the output copied back inside the timed region;
+roofline = the expert-FFN call (both grouped GEMMs) against the measured
+HBM copy bandwidth; cpu_baseline = the CPU oracle on a bounded sample.
+--impl reference times the CPU oracle itself on the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_PATH))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+def expert_bytes(H, I):
+    gu = 2 * I * (H // 8) * 4 + 2 * (2 * I * (H // 64) * 2)
+    dn = H * (I // 8) * 4 + 2 * (H * (I // 64) * 2)
+    return gu + dn
+
+
+def layer_algo(T, shape, counts):
+    """Algorithmic bytes and FLOPs of one layer call (realised histogram)."""
+    H, E, K, I = shape.H, shape.E, shape.K, shape.I
+    touched = int((np.asarray(counts) > 0).sum()) + shape.n_shared
+    wbytes = touched * expert_bytes(H, I)
+    io = T * H * 2 * 2 + E * H * 2 + T * K * 8
+    rows = T * K + T * shape.n_shared
+    flops = 2 * (2 * I * H + H * I) * rows + 2 * E * H * T
+    ffn_bytes = wbytes + T * H * 2 * 2
+    return wbytes + io, flops, ffn_bytes
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = os.path.join("/tmp", "moe_clocks_%d.csv" % os.getpid())
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.bus_id:
+            cmd += ["--id=" + self.bus_id]
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------- CPU oracle arm --
+def oracle_sample(wl, budget_s=12.0):
+    """The oracle as it stands on a bounded sample of the workload; returns
+    (tokens/s, seconds, sample text, threads)."""
+    import oracle
+    S = wl.shape
+    t_start = time.time()
+    tokens = 0
+    T = wl.T
+    L = synth.gen_layer(T, S, seed=wl.seed, zipf_s=wl.zipf_s)
+    n = min(T, 256 if T > 512 else T)
+    tok = np.arange(n, dtype=np.int32)
+    spent = 0.0
+    reps = 0
+    while reps == 0 or (spent < budget_s and reps < 3):
+        t0 = time.time()
+        lg = oracle.router_logits(L.x[:n], L.w_router, L.router_bias)
+        ids, _, w64 = oracle.topk(lg, S.K)
+        oracle.plan(ids, S.E, S.n_shared, 128)
+        oracle.layer_tokens(L, ids, w64, tokens=tok, x=L.x[:n])
+        spent += time.time() - t0
+        reps += 1
+        tokens += n
+    layers_per_token = wl.layers if wl.layers > 1 else 1
+    tps = tokens / spent / layers_per_token
+    return tps, spent, "%d token(s) of one %s layer x %d run(s)%s" % (
+        n, wl.name, reps, ", scaled by 1/%d layers" % layers_per_token if layers_per_token > 1
+        else ""), oracle.num_threads()
+
+
+def decode_oracle(wl, budget_s=12.0):
+    import oracle
+    S = wl.shape
+    x = synth.gen_tokens(1, S.H, 10 ** 6)
+    spent, layers = 0.0, 0
+    while layers < wl.layers and (layers == 0 or spent < budget_s):
+        L = synth.gen_layer(1, S, seed=layers)
+        t0 = time.time()
+        ids, _, w64 = oracle.topk(oracle.router_logits(x, L.w_router, None), S.K)
+        oracle.plan(ids, S.E, S.n_shared, 128)
+        y = oracle.layer_tokens(L, ids, w64, x=x)
+        x = oracle.rmsnorm_rows(y)
+        spent += time.time() - t0
+        layers += 1
+    per_token = spent / layers * wl.layers
+    return 1.0 / per_token, spent, "%d of %d layers of one decode token, scaled to %d" % (
+        layers, wl.layers, wl.layers), oracle.num_threads()
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    if wl.name == "decode":
+        v, spent, sample, thr = decode_oracle(wl, budget_s)
+    else:
+        v, spent, sample, thr = oracle_sample(wl, budget_s)
+    return {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": sample, "seconds": round(spent, 3)}
+
+
+def run_reference(args, wl):
+    """The CPU oracle as the reference arm: each step one bounded sample of
+    the workload (16 tokens through one layer; one layer of the token for
+    decode), the whole run capped at about 150 s."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    S = wl.shape
+    L = synth.gen_layer(wl.T if wl.name != "decode" else 1, S, seed=wl.seed, zipf_s=wl.zipf_s)
+    n = 1 if wl.name == "decode" else min(16, wl.T)
+    x = L.x[:n] if wl.name != "decode" else synth.gen_tokens(1, S.H, 10 ** 6)
+    tok = np.arange(n, dtype=np.int32)
+    per_token_layers = wl.layers
+    times = []
+    t_start = time.time()
+    for i in range(args.warmup + args.steps):
+        t0 = time.time()
+        ids, _, w64 = oracle.topk(oracle.router_logits(x, L.w_router, L.router_bias), S.K)
+        oracle.plan(ids, S.E, S.n_shared, 128)
+        oracle.layer_tokens(L, ids, w64, tokens=tok, x=x)
+        dt = time.time() - t0
+        if i >= args.warmup:
+            times.append(dt)
+        if times and time.time() - t_start > 150.0:
+            break
+    v = n * len(times) / sum(times) / per_token_layers
+    sample = "%d token(s) through one layer per step%s" % (
+        n, ", tokens/s divided by %d layers" % per_token_layers if per_token_layers > 1 else "")
+    cb = {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": sample}
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "layers": wl.layers},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "W4 MoE layer tokens/s at T=1/512/2048; % of HBM or tensor roofline"
+
+
+# ---------------------------------------------------------- GPU arm --
+class GpuWorkload:
+    def __init__(self, wl, dev, m, tile_rows=128):
+        import torch
+        self.wl, self.dev, self.m, self.torch = wl, dev, m, torch
+        S = wl.shape
+        self.S = S
+        self.layers = []
+        nl = wl.layers
+        T = wl.T
+        self.T = T
+        self.shape = m.make_shape(T, S.H, S.E, S.K, S.I, S.n_shared, tile_rows)
+        for l in range(nl):
+            L = synth.gen_layer(T if l == 0 else 1, S, seed=(wl.seed if nl == 1 else l),
+                                zipf_s=wl.zipf_s)
+            d = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa
+            ex = m.ExpertWeights.from_numpy(L.q_gate_up, L.s_gate_up, L.b_gate_up, L.q_down,
+                                            L.s_down, L.b_down, dev)
+            sh = m.ExpertWeights.from_numpy(L.sh_q_gate_up, L.sh_s_gate_up, L.sh_b_gate_up,
+                                            L.sh_q_down, L.sh_s_down, L.sh_b_down, dev) \
+                if S.n_shared else None
+            bias = None if L.router_bias is None else torch.from_numpy(L.router_bias).to(dev)
+            self.layers.append((d(L.w_router), bias, ex, sh))
+            if l == 0:
+                x0 = L.x
+            del L
+        if wl.chunk:
+            self.n_chunks = wl.total_tokens // wl.chunk
+            xs = [synth.gen_tokens(T, S.H, 10 ** 6 + c) for c in range(self.n_chunks)]
+            self.x_host = np.concatenate(xs)
+        elif wl.name == "decode":
+            self.n_chunks = 1
+            self.x_host = synth.gen_tokens(1, S.H, 10 ** 6)
+        else:
+            self.n_chunks = 1
+            self.x_host = x0
+        self.tokens_per_step = T * self.n_chunks
+        self.x_all = torch.from_numpy(self.x_host.view(np.int16)).to(dev)
+        self.ws = m.alloc_workspace(self.shape, dev)
+        self.ids = torch.empty((T, S.K), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, S.K), dtype=torch.float32, device=dev)
+        self.plan = m.PlanBuffers(self.shape, dev)
+        R = T * S.K
+        self.y_slots = torch.empty((R + T * S.n_shared, S.H), dtype=torch.int16, device=dev)
+        self.y = torch.empty((T, S.H), dtype=torch.int16, device=dev)
+        self.xa = torch.empty((T, S.H), dtype=torch.int16, device=dev)
+        self.xb = torch.empty((T, S.H), dtype=torch.int16, device=dev)
+        self.y_out = torch.empty((T * self.n_chunks, S.H), dtype=torch.int16, device=dev)
+
+    def calls_per_layer(self):
+        return 7  # route: 2 kernels, plan: 2, ffn: 2, combine: 1
+
+    def step(self, ev_pairs=None):
+        """One pass of the hot path over the step's tokens (device-resident)."""
+        m, S, T = self.m, self.S, self.T
+        nl = len(self.layers)
+        for c in range(self.n_chunks):
+            x = self.x_all[c * T:(c + 1) * T]
+            for l, (wr, bias, ex, sh) in enumerate(self.layers):
+                last = l == nl - 1
+                m.moe_route(self.shape, x, wr, bias, self.ids, self.w, self.ws)
+                m.moe_plan(self.shape, self.ids, self.plan, self.ws)
+                if ev_pairs is not None:
+                    ev_pairs[0].record()
+                m.moe_expert_ffn_w4(self.shape, x, ex, sh, self.plan, self.y_slots, self.ws)
+                if ev_pairs is not None:
+                    ev_pairs[1].record()
+                    ev_pairs = None
+                y = self.y_out[c * T:(c + 1) * T] if last else self.y
+                xn = None if last else (self.xa if l % 2 == 0 else self.xb)
+                m.moe_combine(self.shape, self.y_slots, self.plan.row_pos, self.w, y, xn)
+                x = xn
+
+    def step_e2e(self, x_pin, y_pin):
+        """The same through moe_layer_w4 with host buffers copied in and out."""
+        m, T = self.m, self.T
+        nl = len(self.layers)
+        for c in range(self.n_chunks):
+            self.xa.copy_(x_pin[c * T:(c + 1) * T], non_blocking=True)
+            x = self.xa
+            for l, (wr, bias, ex, sh) in enumerate(self.layers):
+                last = l == nl - 1
+                xn = None if last else (self.xb if x is self.xa else self.xa)
+                m.moe_layer_w4(self.shape, x, wr, bias, ex, sh, self.y, self.ws, x_next=xn)
+                x = xn
+            y_pin[c * T:(c + 1) * T].copy_(self.y, non_blocking=True)
+
+    def realised_counts(self):
+        """Histogram of the step's first layer call (for algorithmic bytes)."""
+        self.m.moe_route(self.shape, self.x_all[:self.T], self.layers[0][0], self.layers[0][1],
+                         self.ids, self.w, self.ws)
+        self.m.moe_plan(self.shape, self.ids, self.plan, self.ws)
+        self.torch.cuda.synchronize()
+        return self.plan.counts.cpu().numpy()
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_moe_expert_histogram_gb300 as m
+    m.load()
+
+    G = GpuWorkload(wl, dev, m)
+    counts = G.realised_counts()
+    algo_bytes, flops, ffn_bytes = layer_algo(G.T, wl.shape, counts)
+    calls = G.n_chunks * len(G.layers)
+    step_bytes = algo_bytes * calls
+    step_flops = flops * calls
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        G.step()
+    st = m.moe_query_device_status(G.ws)
+    if st != 0:
+        raise RuntimeError("device status %d after warm-up" % st)
+    torch.cuda.synchronize()
+
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus) if rank == 0 else None
+    ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    for i in range(args.steps):
+        G.step(ffn_ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        clocks = sampler.stop()
+    else:
+        clocks = None
+    if world > 1:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    st = m.moe_query_device_status(G.ws)
+    if st != 0:
+        raise RuntimeError("device status %d after timed region" % st)
+
+    # e2e: host buffers in and out through moe_layer_w4
+    x_pin = torch.from_numpy(G.x_host.view(np.int16)).pin_memory()
+    y_pin = torch.empty((G.tokens_per_step, wl.shape.H), dtype=torch.int16).pin_memory()
+    e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        G.step_e2e(x_pin, y_pin)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        G.step_e2e(x_pin, y_pin)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+
+    hbm, bf16, bf16s, src = peaks()
+    ms_step = ms / args.steps
+    value = G.tokens_per_step * world / (ms_step / 1e3)
+    ffn_gbs = ffn_bytes / (ffn_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 x u4 -> fp32 accumulate",
+        "data": "synthetic (seeded numpy: hidden N(0,1), router N(0,1/H), nibbles U{0..15}, "
+                "scales U[0.002,0.02], bias -8*scale)",
+        "config": {"workload": wl.name, "T": wl.T, "layers": wl.layers,
+                   "chunks": G.n_chunks, "H": wl.shape.H, "E": wl.shape.E, "K": wl.shape.K,
+                   "I": wl.shape.I, "n_shared": wl.shape.n_shared, "tile_rows": 128,
+                   "l2": "no flush: weights %.1f MB per layer > 129 MB L2" %
+                         (len(G.layers) and (wl.shape.E + wl.shape.n_shared) *
+                          expert_bytes(wl.shape.H, wl.shape.I) / 1e6),
+                   "parallelism": "token-sharded replicas x%d" % world},
+        "step": {"algorithmic_bytes": step_bytes, "flops": step_flops,
+                 "gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+                 "tflops": round(step_flops / (ms_step / 1e3) / 1e12, 2),
+                 "hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
+                 "tensor_frac": round(step_flops / (ms_step / 1e3) / 1e12 / bf16s, 4),
+                 "touched_experts": int((counts > 0).sum()), "max_group": int(counts.max())},
+        "roofline": {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)",
+                     "bound": "hbm", "achieved": round(ffn_gbs, 1), "peak": hbm,
+                     "peak_source": src, "unit": "GB/s", "frac": round(ffn_gbs / hbm, 4),
+                     "traffic": None, "ms_per_launch": round(ffn_ms, 5),
+                     "algorithmic_bytes_per_launch": ffn_bytes},
+        "e2e": {"value": round(G.tokens_per_step * world / (e_ms / 1e3), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
+                "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
+                "steps": e_steps, "ms_per_step": round(e_ms, 5)},
+        "gpu_launches": G.calls_per_layer() * calls * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="prefill", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = synth.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,231 @@
+"""W4A16 Mixture-of-Experts expert layer for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in include/moe_w4.h. Every function here
+only marshals arguments (device pointers from torch tensors, the current
+CUDA stream) and raises MoeError on a non-zero status; all arithmetic runs
+in the CUDA kernels of libmoe_w4.so. There is no CPU fallback: if the
+library has not been built, load() raises.
+
+Names follow the C ABI: moe_route, moe_plan, moe_expert_ffn_w4,
+moe_combine, moe_layer_w4, moe_workspace_bytes, moe_max_blocks,
+moe_workspace_init, moe_query_device_status, moe_debug_dequant_w4.
+"""
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe_w4.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_BAD_INPUT = 5
+MOE_ERR_TIMEOUT = 6
+
+EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_route",
+           "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
+           "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
+           "moe_last_error")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        lib = _lib
+        text = lib.moe_status_string(status).decode() if lib else str(status)
+        detail = lib.moe_last_error().decode() if lib else ""
+        super().__init__("%s: %s (%d)%s" % (where, text, status, (" - " + detail) if detail else ""))
+
+
+class Shape(C.Structure):
+    _fields_ = [("T", C.c_int32), ("H", C.c_int32), ("E", C.c_int32), ("K", C.c_int32),
+                ("I", C.c_int32), ("n_shared", C.c_int32), ("tile_rows", C.c_int32)]
+
+    def __repr__(self):
+        return "Shape(T=%d, H=%d, E=%d, K=%d, I=%d, n_shared=%d, tile_rows=%d)" % (
+            self.T, self.H, self.E, self.K, self.I, self.n_shared, self.tile_rows)
+
+
+class W4Weights(C.Structure):
+    _fields_ = [("q_gate_up", C.c_void_p), ("s_gate_up", C.c_void_p), ("b_gate_up", C.c_void_p),
+                ("q_down", C.c_void_p), ("s_down", C.c_void_p), ("b_down", C.c_void_p)]
+
+
+class PlanPtrs(C.Structure):
+    _fields_ = [("counts", C.c_void_p), ("offsets", C.c_void_p), ("sorted_rows", C.c_void_p),
+                ("row_pos", C.c_void_p), ("block_map", C.c_void_p), ("num_blocks", C.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load():
+    """Load libmoe_w4.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise FileNotFoundError(
+                    "libmoe_w4.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+            L = C.CDLL(LIB_PATH)
+            P, I32, SZ = C.c_void_p, C.c_int32, C.c_size_t
+            pS, pW, pP = C.POINTER(Shape), C.POINTER(W4Weights), C.POINTER(PlanPtrs)
+            L.moe_workspace_bytes.restype = SZ
+            L.moe_workspace_bytes.argtypes = [pS]
+            L.moe_max_blocks.restype = I32
+            L.moe_max_blocks.argtypes = [pS]
+            for name, args in (
+                    ("moe_workspace_init", [P, SZ, P]),
+                    ("moe_route", [pS, P, P, P, P, P, P, SZ, P]),
+                    ("moe_plan", [pS, P, pP, P, SZ, P]),
+                    ("moe_expert_ffn_w4", [pS, P, pW, pW, pP, P, P, SZ, P]),
+                    ("moe_combine", [pS, P, P, P, P, P, P]),
+                    ("moe_layer_w4", [pS, P, P, P, pW, pW, P, P, P, P, P, SZ, P]),
+                    ("moe_query_device_status", [P, SZ, P]),
+                    ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P])):
+                f = getattr(L, name)
+                f.restype = C.c_int
+                f.argtypes = args
+            L.moe_status_string.restype = C.c_char_p
+            L.moe_status_string.argtypes = [C.c_int]
+            L.moe_last_error.restype = C.c_char_p
+            L.moe_last_error.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _check(status, where):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _p(t):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def make_shape(T, H, E, K, I, n_shared=1, tile_rows=128):
+    return Shape(T, H, E, K, I, n_shared, tile_rows)
+
+
+def moe_workspace_bytes(shape):
+    return load().moe_workspace_bytes(C.byref(shape))
+
+
+def moe_max_blocks(shape):
+    return load().moe_max_blocks(C.byref(shape))
+
+
+def moe_workspace_init(ws, stream=None):
+    _check(load().moe_workspace_init(_p(ws), ws.numel() * ws.element_size(), _s(stream)),
+           "moe_workspace_init")
+
+
+def moe_route(shape, x, w_router, router_bias, topk_ids, topk_w, ws, stream=None):
+    _check(load().moe_route(C.byref(shape), _p(x), _p(w_router), _p(router_bias), _p(topk_ids),
+                            _p(topk_w), _p(ws), ws.numel(), _s(stream)), "moe_route")
+
+
+def moe_plan(shape, topk_ids, plan, ws, stream=None):
+    _check(load().moe_plan(C.byref(shape), _p(topk_ids), C.byref(plan.ptrs), _p(ws), ws.numel(),
+                           _s(stream)), "moe_plan")
+
+
+def moe_expert_ffn_w4(shape, x, experts, shared, plan, y_slots, ws, stream=None):
+    _check(load().moe_expert_ffn_w4(C.byref(shape), _p(x), C.byref(experts.ptrs),
+                                    C.byref(shared.ptrs) if shared is not None else None,
+                                    C.byref(plan.ptrs), _p(y_slots), _p(ws), ws.numel(),
+                                    _s(stream)), "moe_expert_ffn_w4")
+
+
+def moe_combine(shape, y_slots, row_pos, topk_w, y, x_next=None, stream=None):
+    _check(load().moe_combine(C.byref(shape), _p(y_slots), _p(row_pos), _p(topk_w), _p(y),
+                              _p(x_next), _s(stream)), "moe_combine")
+
+
+def moe_layer_w4(shape, x, w_router, router_bias, experts, shared, y, ws, x_next=None,
+                 topk_ids=None, topk_w=None, stream=None):
+    _check(load().moe_layer_w4(C.byref(shape), _p(x), _p(w_router), _p(router_bias),
+                               C.byref(experts.ptrs),
+                               C.byref(shared.ptrs) if shared is not None else None,
+                               _p(y), _p(x_next), _p(topk_ids), _p(topk_w), _p(ws), ws.numel(),
+                               _s(stream)), "moe_layer_w4")
+
+
+def moe_query_device_status(ws, stream=None):
+    """Synchronises the stream; returns the device status code (and clears it)."""
+    return load().moe_query_device_status(_p(ws), ws.numel(), _s(stream))
+
+
+def moe_debug_dequant_w4(q, s, b, out, stream=None):
+    N, K8 = q.shape
+    _check(load().moe_debug_dequant_w4(_p(q), _p(s), _p(b), _p(out), N, K8 * 8, _s(stream)),
+           "moe_debug_dequant_w4")
+
+
+# ----------------------------------------------------- device-side holders --
+class ExpertWeights:
+    """Packed 4-bit weights of n experts resident on the device (layouts of
+    moe_w4_weights_t); bf16 arrays are kept as int16 storage."""
+
+    def __init__(self, q_gate_up, s_gate_up, b_gate_up, q_down, s_down, b_down):
+        self.tensors = (q_gate_up, s_gate_up, b_gate_up, q_down, s_down, b_down)
+        for t in self.tensors:
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("expert weights must be contiguous CUDA tensors")
+        self.ptrs = W4Weights(*[t.data_ptr() for t in self.tensors])
+
+    @classmethod
+    def from_numpy(cls, q_gate_up, s_gate_up, b_gate_up, q_down, s_down, b_down, device="cuda"):
+        def dev(a):
+            a = a.view("int32") if a.dtype.itemsize == 4 else a.view("int16")
+            return torch.from_numpy(a.copy()).to(device)
+        return cls(*[dev(a) for a in (q_gate_up, s_gate_up, b_gate_up, q_down, s_down, b_down)])
+
+    @property
+    def nbytes(self):
+        return sum(t.numel() * t.element_size() for t in self.tensors)
+
+
+class PlanBuffers:
+    """Caller-owned plan buffers (moe_plan_t) for one shape."""
+
+    def __init__(self, shape, device="cuda"):
+        R = shape.T * shape.K
+        mb = moe_max_blocks(shape)
+        z = lambda n: torch.zeros(n, dtype=torch.int32, device=device)  # noqa: E731
+        self.counts = z(shape.E)
+        self.offsets = z(shape.E + 1)
+        self.sorted_rows = z(R)
+        self.row_pos = z(R)
+        self.block_map = z(mb * 3)
+        self.num_blocks = z(1)
+        self.ptrs = PlanPtrs(*[t.data_ptr() for t in (self.counts, self.offsets, self.sorted_rows,
+                                                      self.row_pos, self.block_map,
+                                                      self.num_blocks)])
+
+
+def alloc_workspace(shape, device="cuda", stream=None):
+    n = moe_workspace_bytes(shape)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "alloc_workspace")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws

@@ -1,0 +1,387 @@
+// C ABI of the W4A16 MoE expert layer (declared in include/moe_w4.h):
+// host-side validation, workspace layout, TMA descriptors and launches.
+// Nothing here allocates device memory or synchronises a stream, except
+// moe_query_device_status, whose job is to synchronise.
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t cuda_fail(cudaError_t e, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return MOE_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_ok(const moe_shape_t* s) {
+  if (!s) return false;
+  if (s->T < 1 || s->H < 256 || s->H % 256 != 0 || s->H > 8192) return false;
+  if (s->I < 128 || s->I % 128 != 0 || s->I > 8192) return false;
+  if (s->K < 1 || s->K > 32 || s->E < s->K || s->E > 1024) return false;
+  if (s->n_shared != 0 && s->n_shared != 1) return false;
+  if (s->tile_rows < 1 || s->tile_rows > ffn_max_tile_n()) return false;
+  const int64_t R = (int64_t)s->T * s->K;
+  const int64_t S = R + (int64_t)s->T * s->n_shared;
+  if (S * s->H >= INT32_MAX || S * s->I >= INT32_MAX) return false;
+  if ((int64_t)s->T * s->E >= INT32_MAX) return false;
+  if ((int64_t)s->E * 2 * s->I * (s->H / 8) >= INT32_MAX) return false;
+  if ((int64_t)s->E * s->H * (s->I / 8) >= INT32_MAX) return false;
+  return true;
+}
+
+int64_t max_blocks_of(const moe_shape_t* s) {
+  const int64_t R = (int64_t)s->T * s->K, BM = s->tile_rows;
+  const int64_t shared_blocks = s->n_shared ? (s->T + BM - 1) / BM : 0;
+  return (R + BM - 1) / BM + (R < s->E ? R : s->E) + shared_blocks;
+}
+
+struct Layout {
+  size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, total;
+};
+
+Layout layout_of(const moe_shape_t* s) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  const size_t T = s->T, K = s->K, E = s->E, R = T * K, S = R + T * s->n_shared;
+  const size_t nchunks = (R + kPlanChunk - 1) / kPlanChunk;
+  L.ctrl = take(sizeof(Ctrl));
+  L.hist = take(nchunks * E * 4);
+  L.logits = take(T * E * 4);
+  L.h = take(S * (size_t)s->I * 2);
+  L.ids = take(R * 4);
+  L.w = take(R * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.sorted = take(R * 4);
+  L.rowpos = take(R * 4);
+  L.bmap = take((size_t)max_blocks_of(s) * 12);
+  L.nblk = take(4);
+  L.yslots = take(S * (size_t)s->H * 2);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------- device info --
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+moe_status_t sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) {
+    g_last_error = "device index out of range";
+    return MOE_ERR_CUDA;
+  }
+  int n = g_sm_count[dev].load();
+  if (n == 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_sm_count[dev].store(n);
+  }
+  *out = n;
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------- tensor maps --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major 2-D tensor [outer][inner] of elements of `esize` bytes.
+moe_status_t map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base,
+                    uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                    CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    g_last_error = "cuTensorMapEncodeTiled unavailable";
+    return MOE_ERR_CUDA;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_error = "cuTensorMapEncodeTiled failed: " + std::to_string((int)r);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+bool weights_ok(const moe_w4_weights_t* w) {
+  return w && w->q_gate_up_dev && w->s_gate_up_dev && w->b_gate_up_dev && w->q_down_dev &&
+         w->s_down_dev && w->b_down_dev && aligned16(w->q_gate_up_dev) &&
+         aligned16(w->s_gate_up_dev) && aligned16(w->b_gate_up_dev) &&
+         aligned16(w->q_down_dev) && aligned16(w->s_down_dev) && aligned16(w->b_down_dev);
+}
+
+bool plan_ok(const moe_plan_t* p) {
+  return p && p->counts_dev && p->offsets_dev && p->sorted_rows_dev && p->row_pos_dev &&
+         p->block_map_dev && p->num_blocks_dev;
+}
+
+moe_status_t check_ws(const moe_shape_t* s, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout_of(s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+#define MOE_TRY(x)                     \
+  do {                                 \
+    moe_status_t st_ = (x);            \
+    if (st_ != MOE_OK) return st_;     \
+  } while (0)
+
+moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t* ex,
+                     const moe_w4_weights_t* sh, const moe_plan_t* plan, void* y_slots,
+                     uint8_t* ws, cudaStream_t stream) {
+  const Layout L = layout_of(s);
+  const int T = s->T, H = s->H, E = s->E, K = s->K, I = s->I;
+  const int R = T * K, S = R + T * s->n_shared;
+  const int maxb = (int)max_blocks_of(s);
+  int nsm = 0;
+  MOE_TRY(sm_count(&nsm));
+  const moe_w4_weights_t* shw = s->n_shared ? sh : ex;
+  uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+
+  CUtensorMap tw, twsh, tx, th;
+  MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_gate_up_dev, H / 8,
+                 (uint64_t)E * 2 * I, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+  MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_gate_up_dev, H / 8,
+                 (uint64_t)(s->n_shared ? 1 : E) * 2 * I, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, 64, 1,
+                 CU_TENSOR_MAP_SWIZZLE_128B));
+  FfnArgs a{};
+  a.block_map = plan->block_map_dev;
+  a.num_blocks = plan->num_blocks_dev;
+  a.sorted_rows = plan->sorted_rows_dev;
+  a.K = K;
+  a.R = R;
+  a.E = E;
+  a.rows_per_expert = 2 * I;
+  a.half_rows = I;
+  a.mtiles = I / ffn_tile_m();
+  a.kstages = H / ffn_stage_k();
+  a.kgroups = H / 64;
+  a.s_exp = ex->s_gate_up_dev;
+  a.b_exp = ex->b_gate_up_dev;
+  a.s_sh = shw->s_gate_up_dev;
+  a.b_sh = shw->b_gate_up_dev;
+  a.out = h;
+  a.out_ld = I;
+  a.ctrl = ctrl;
+  a.max_units = maxb * a.mtiles;
+  cudaError_t e = launch_ffn_gate_up(tw, twsh, tx, a, a.max_units < nsm ? a.max_units : nsm, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "ffn gate_up launch");
+
+  MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_down_dev, I / 8, (uint64_t)E * H,
+                 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+  MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_down_dev, I / 8,
+                 (uint64_t)(s->n_shared ? 1 : E) * H, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+  MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, 1,
+                 CU_TENSOR_MAP_SWIZZLE_128B));
+  a.sorted_rows = nullptr;
+  a.rows_per_expert = H;
+  a.half_rows = 0;
+  a.mtiles = H / ffn_tile_m();
+  a.kstages = I / ffn_stage_k();
+  a.kgroups = I / 64;
+  a.s_exp = ex->s_down_dev;
+  a.b_exp = ex->b_down_dev;
+  a.s_sh = shw->s_down_dev;
+  a.b_sh = shw->b_down_dev;
+  a.out = reinterpret_cast<uint16_t*>(y_slots);
+  a.out_ld = H;
+  a.max_units = maxb * a.mtiles;
+  e = launch_ffn_down(tw, twsh, th, a, a.max_units < nsm ? a.max_units : nsm, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "ffn down launch");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_shape_t* shape) {
+  return shape_ok(shape) ? layout_of(shape).total : 0;
+}
+
+int32_t moe_max_blocks(const moe_shape_t* shape) {
+  return shape_ok(shape) ? (int32_t)max_blocks_of(shape) : 0;
+}
+
+moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws_dev || ws_bytes < sizeof(Ctrl)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(ws_dev, 0, sizeof(Ctrl), (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
+}
+
+moe_status_t moe_route(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
+                       const float* router_bias_dev, int32_t* topk_ids_dev, float* topk_w_dev,
+                       void* ws_dev, size_t ws_bytes, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x_dev || !w_router_dev || !topk_ids_dev || !topk_w_dev) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_dev) || !aligned16(w_router_dev)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  const Layout L = layout_of(shape);
+  cudaError_t e = launch_route(static_cast<const uint16_t*>(x_dev),
+                               static_cast<const uint16_t*>(w_router_dev), router_bias_dev,
+                               shape->T, shape->H, shape->E, shape->K,
+                               reinterpret_cast<float*>(ws + L.logits), topk_ids_dev, topk_w_dev,
+                               (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
+}
+
+moe_status_t moe_plan(const moe_shape_t* shape, const int32_t* topk_ids_dev,
+                      const moe_plan_t* plan, void* ws_dev, size_t ws_bytes,
+                      moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!topk_ids_dev || !plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  const Layout L = layout_of(shape);
+  cudaError_t e = launch_plan(topk_ids_dev, shape->T, shape->K, shape->E, shape->n_shared,
+                              shape->tile_rows, *plan, reinterpret_cast<int32_t*>(ws + L.hist),
+                              reinterpret_cast<Ctrl*>(ws + L.ctrl), (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_plan launch");
+}
+
+moe_status_t moe_expert_ffn_w4(const moe_shape_t* shape, const void* x_dev,
+                               const moe_w4_weights_t* experts, const moe_w4_weights_t* shared,
+                               const moe_plan_t* plan, void* y_slots_dev, void* ws_dev,
+                               size_t ws_bytes, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x_dev || !aligned16(x_dev) || !weights_ok(experts) || !plan_ok(plan) || !y_slots_dev)
+    return MOE_ERR_INVALID_ARG;
+  if (shape->n_shared && !weights_ok(shared)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  return run_ffn(shape, x_dev, experts, shared, plan, y_slots_dev,
+                 static_cast<uint8_t*>(ws_dev), (cudaStream_t)stream);
+}
+
+moe_status_t moe_combine(const moe_shape_t* shape, const void* y_slots_dev,
+                         const int32_t* row_pos_dev, const float* topk_w_dev, void* y_dev,
+                         void* x_next_dev, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!y_slots_dev || !row_pos_dev || !topk_w_dev || !y_dev) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_slots_dev) || !aligned16(y_dev) || (x_next_dev && !aligned16(x_next_dev)))
+    return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_combine(static_cast<const uint16_t*>(y_slots_dev), row_pos_dev,
+                                 topk_w_dev, shape->T, shape->H, shape->K, shape->n_shared,
+                                 static_cast<uint16_t*>(y_dev),
+                                 static_cast<uint16_t*>(x_next_dev), (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
+}
+
+moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
+                          const float* router_bias_dev, const moe_w4_weights_t* experts,
+                          const moe_w4_weights_t* shared, void* y_dev, void* x_next_dev,
+                          int32_t* topk_ids_dev, float* topk_w_dev, void* ws_dev,
+                          size_t ws_bytes, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x_dev || !w_router_dev || !y_dev || !aligned16(x_dev) || !aligned16(w_router_dev) ||
+      !aligned16(y_dev) || !weights_ok(experts))
+    return MOE_ERR_INVALID_ARG;
+  if (x_next_dev && !aligned16(x_next_dev)) return MOE_ERR_INVALID_ARG;
+  if (shape->n_shared && !weights_ok(shared)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  const Layout L = layout_of(shape);
+  int32_t* ids = topk_ids_dev ? topk_ids_dev : reinterpret_cast<int32_t*>(ws + L.ids);
+  float* w = topk_w_dev ? topk_w_dev : reinterpret_cast<float*>(ws + L.w);
+  moe_plan_t plan;
+  plan.counts_dev = reinterpret_cast<int32_t*>(ws + L.counts);
+  plan.offsets_dev = reinterpret_cast<int32_t*>(ws + L.offsets);
+  plan.sorted_rows_dev = reinterpret_cast<int32_t*>(ws + L.sorted);
+  plan.row_pos_dev = reinterpret_cast<int32_t*>(ws + L.rowpos);
+  plan.block_map_dev = reinterpret_cast<int32_t*>(ws + L.bmap);
+  plan.num_blocks_dev = reinterpret_cast<int32_t*>(ws + L.nblk);
+  void* y_slots = ws + L.yslots;
+  cudaStream_t st = (cudaStream_t)stream;
+  MOE_TRY(moe_route(shape, x_dev, w_router_dev, router_bias_dev, ids, w, ws_dev, ws_bytes, stream));
+  MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
+  MOE_TRY(run_ffn(shape, x_dev, experts, shared, &plan, y_slots, ws, st));
+  return moe_combine(shape, y_slots, plan.row_pos_dev, w, y_dev, x_next_dev, stream);
+}
+
+moe_status_t moe_query_device_status(void* ws_dev, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws_dev || ws_bytes < sizeof(Ctrl)) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int word[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(word, ws_dev, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word[0] != 0) {
+    g_last_error = "device error " + std::to_string(word[0]) + " in kernel " +
+                   std::to_string(word[1]) + " block " + std::to_string(word[2]) + " detail " +
+                   std::to_string(word[3]);
+    e = cudaMemset(ws_dev, 0, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return (moe_status_t)word[0];
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_dequant_w4(const uint32_t* q_dev, const uint16_t* s_dev,
+                                  const uint16_t* b_dev, uint16_t* out_dev, int32_t N,
+                                  int32_t Kd, moe_stream_t stream) {
+  if (!q_dev || !s_dev || !b_dev || !out_dev || N < 1 || Kd < 64 || Kd % 64 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(out_dev) || (int64_t)N * Kd >= INT32_MAX) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_dequant(q_dev, s_dev, b_dev, out_dev, N, Kd, (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_debug_dequant_w4 launch");
+}
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_INPUT: return "bad input on device (expert id out of range)";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

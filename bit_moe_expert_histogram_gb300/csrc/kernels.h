@@ -1,0 +1,57 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_w4.h"
+
+namespace moe {
+
+struct Ctrl;
+
+constexpr int kPlanChunk = 2048;  // routed rows per plan block
+
+// Arguments of one grouped W4A16 GEMM launch (gate_up or down).
+struct FfnArgs {
+  const int32_t* block_map;    // [max_blocks][3] (expert, row_start, nrows)
+  const int32_t* num_blocks;   // device count of block-map entries
+  const int32_t* sorted_rows;  // gate_up: routed row -> f = t*K + k
+  int K;                       // experts per token
+  int R;                       // routed rows (T*K)
+  int E;                       // routed experts; entry expert E = shared
+  int rows_per_expert;         // weight rows per expert (2I or H)
+  int half_rows;               // gate_up: I (first up row); down: 0
+  int mtiles;                  // 128-row weight tiles per entry
+  int kstages;                 // reduction stages (Kdim / 128)
+  int kgroups;                 // 64-wide groups per weight row (Kdim / 64)
+  const uint16_t* s_exp;       // [E][rows][kgroups] bf16 scales
+  const uint16_t* b_exp;       // [E][rows][kgroups] bf16 biases
+  const uint16_t* s_sh;        // shared expert [rows][kgroups]
+  const uint16_t* b_sh;
+  uint16_t* out;               // bf16 [S][out_ld]
+  int out_ld;
+  Ctrl* ctrl;
+  int max_units;               // host bound on units
+};
+
+cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
+                         int E, int K, float* logits, int32_t* ids, float* w,
+                         cudaStream_t stream);
+cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, int BM,
+                        const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, cudaStream_t stream);
+cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
+                               const CUtensorMap& tx, const FfnArgs& a, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, const CUtensorMap& th,
+                            const FfnArgs& a, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, const float* w, int T,
+                           int H, int K, int n_shared, uint16_t* y, uint16_t* x_next,
+                           cudaStream_t stream);
+cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
+                           int N, int Kd, cudaStream_t stream);
+int ffn_tile_m();
+int ffn_max_tile_n();
+int ffn_stage_k();
+
+}  // namespace moe

@@ -1,0 +1,205 @@
+/*
+ * moe_w4.h - C ABI of the W4A16 Mixture-of-Experts expert layer for GB300
+ * (sm_103a): GPU-resident routing and grouped 4-bit-weight GEMMs.
+ *
+ * The operations follow the announcement "Perplexity Open Sources Lily: A
+ * Rust + Metal Inference Engine for Qwen3.6-35B-A3B on Apple Silicon"
+ * (abbreviated [Lily] below), sections "Three Workload Shapes" (a router
+ * scores 256 experts and picks eight, plus one shared expert that sees every
+ * token), "Prefill: Keep Weights Packed, Keep Routing on the GPU" (groupwise
+ * affine 4-bit weights, 64 per group with a bf16 scale and bias, rebuilt to
+ * bf16 one tile at a time inside the grouped GEMM with FP32 accumulation;
+ * routing histogram, prefix scan, scatter and block map kept on the GPU with
+ * no CPU synchronisation inside the layer) and "Decode: Minimize Bytes Moved
+ * Per Token" (batch-1 decode is bandwidth bound).
+ *
+ * Conventions for every call:
+ *  - Pointers named *_dev are device pointers owned by the caller; the
+ *    library never allocates, frees or keeps them. Host pointers are only
+ *    read during the call. bf16 tensors are passed as raw 16-bit patterns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and never synchronise it, so they can be captured in a
+ *    CUDA graph. The device that is current when a call is made must own all
+ *    device pointers of that call.
+ *  - Argument and shape errors are returned before anything is enqueued.
+ *    A failed launch returns MOE_ERR_CUDA (text in moe_last_error()).
+ *    Errors found on the device (an expert id out of range, a bounded wait
+ *    that ran out) are recorded in the workspace's status word and the
+ *    kernel returns early; they surface through moe_query_device_status().
+ *  - The workspace is caller-owned device memory of at least
+ *    moe_workspace_bytes() bytes, 256-byte aligned, zero-filled once before
+ *    first use (moe_workspace_init). Calls that share a workspace must be
+ *    ordered (same stream, or events); separate workspaces make calls
+ *    independent.
+ *  - Supported shapes: 1 <= T, H % 256 == 0, I % 128 == 0, 1 <= K <= E <= 1024,
+ *    K <= 32, n_shared in {0, 1}, 1 <= tile_rows <= 128, and every row /
+ *    element count fits in int32.
+ */
+#ifndef MOE_W4_H
+#define MOE_W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,       /* null pointer, misaligned pointer, bad flag */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside the supported set above */
+  MOE_ERR_WORKSPACE = 3,         /* workspace smaller than moe_workspace_bytes() */
+  MOE_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  MOE_ERR_BAD_INPUT = 5,         /* device: an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 6            /* device: a bounded wait ran out */
+} moe_status_t;
+
+/* Layer shape. T tokens of hidden size H; E routed experts, K selected per
+ * token; expert intermediate size I (routed and shared experts alike);
+ * n_shared always-on shared experts (0 or 1); tile_rows = the most rows one
+ * block-map entry (one GEMM tile of tokens) may hold. */
+typedef struct moe_shape {
+  int32_t T, H, E, K, I, n_shared, tile_rows;
+} moe_shape_t;
+
+/* Packed 4-bit weights of n experts ([Lily] "Prefill": groupwise affine,
+ * 64 weights per group along the reduction dimension, bf16 scale and bias;
+ * the dequantised weight is w = bf16(scale * q + bias), q in 0..15).
+ *  q_gate_up_dev  uint32 [n][2I][H/8]   rows 0..I-1: gate, rows I..2I-1: up
+ *  s_gate_up_dev  bf16   [n][2I][H/64]  scale of group g = k/64
+ *  b_gate_up_dev  bf16   [n][2I][H/64]  bias  of group g
+ *  q_down_dev     uint32 [n][H][I/8]
+ *  s_down_dev     bf16   [n][H][I/64]
+ *  b_down_dev     bf16   [n][H][I/64]
+ * Word w of a row holds elements k = 8w..8w+7; element 8w+i is the nibble at
+ * bits 4i..4i+3 (low nibble first). All six pointers 16-byte aligned. */
+typedef struct moe_w4_weights {
+  const uint32_t* q_gate_up_dev;
+  const uint16_t* s_gate_up_dev;
+  const uint16_t* b_gate_up_dev;
+  const uint32_t* q_down_dev;
+  const uint16_t* s_down_dev;
+  const uint16_t* b_down_dev;
+} moe_w4_weights_t;
+
+/* Routing plan ([Lily] "Prefill": routing histogram, prefix scan, scatter,
+ * block map). All device int32 buffers, caller-owned. R = T*K routed rows
+ * f = t*K + k; the shared expert's rows are R..R+T-1 in token order.
+ *  counts_dev      [E]      rows routed to each expert
+ *  offsets_dev     [E+1]    exclusive prefix sum of counts; offsets[E] = R
+ *  sorted_rows_dev [R]      routed rows in expert-contiguous order, ascending
+ *                           f within an expert (stable)
+ *  row_pos_dev     [R]      inverse: sorted_rows[row_pos[f]] = f
+ *  block_map_dev   [moe_max_blocks() * 3]  entries (expert, row_start, nrows):
+ *                           for e ascending, tiles of at most tile_rows rows
+ *                           over [offsets[e], offsets[e+1]); then, with a
+ *                           shared expert, entries (E, R + r0, nrows) over the
+ *                           T shared rows. Entries past num_blocks are unused.
+ *  num_blocks_dev  [1]      entries written (device-side; never read back) */
+typedef struct moe_plan {
+  int32_t* counts_dev;
+  int32_t* offsets_dev;
+  int32_t* sorted_rows_dev;
+  int32_t* row_pos_dev;
+  int32_t* block_map_dev;
+  int32_t* num_blocks_dev;
+} moe_plan_t;
+
+/* Bytes of workspace every call below needs for `shape` (all calls of one
+ * shape can share one workspace). 0 if the shape is unsupported. */
+size_t moe_workspace_bytes(const moe_shape_t* shape);
+
+/* Upper bound on block-map entries: ceil(R/tile_rows) + min(E, R) +
+ * ceil(T/tile_rows) with a shared expert. Known on the host, so grids are
+ * sized without reading the device count back. 0 if unsupported. */
+int32_t moe_max_blocks(const moe_shape_t* shape);
+
+/* Zero-fill the workspace's status area (enqueued on stream). */
+moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Router: logits, top-K, renormalised softmax ([Lily] "Three Workload
+ * Shapes": a router scores the experts and picks the top K).
+ *  x_dev           bf16 [T][H] hidden states (16-byte aligned rows)
+ *  w_router_dev    bf16 [E][H] router weight
+ *  router_bias_dev fp32 [E] added to each logit, or NULL
+ *  topk_ids_dev    int32 [T][K] out: experts by logit descending, ties to the
+ *                  lower id
+ *  topk_w_dev      fp32 [T][K] out: exp(l_k - l_0) / sum_j exp(l_j - l_0)
+ * The logit is fp32 in one fixed order: 32 partial sums, partial L
+ * accumulating (fma, round to nearest) elements k = 8*(32j+L)+i for
+ * j = 0..H/256-1, i = 0..7 from +0; partials then added pairwise at index
+ * distance 16, 8, 4, 2, 1; then + bias. Bit-exact and deterministic. */
+moe_status_t moe_route(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
+                       const float* router_bias_dev, int32_t* topk_ids_dev, float* topk_w_dev,
+                       void* ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Plan: histogram, exclusive scan, stable scatter and block map of
+ * topk_ids_dev [T][K] into `plan` (layouts above). An id outside [0, E)
+ * sets MOE_ERR_BAD_INPUT on the device and that item is skipped.
+ * Integer work, bit-exact and deterministic. */
+moe_status_t moe_plan(const moe_shape_t* shape, const int32_t* topk_ids_dev,
+                      const moe_plan_t* plan, void* ws_dev, size_t ws_bytes,
+                      moe_stream_t stream);
+
+/* Expert FFNs over the plan's block map ([Lily] "Prefill": grouped GEMM that
+ * rebuilds 4-bit weights to bf16 one tile at a time on chip, FP32
+ * accumulation; the expanded weights never reach device memory).
+ * For every routed row r of expert e (sorted order) with token t =
+ * sorted_rows[r]/K, and every shared row R+t:
+ *   g = x_t Wg^T, u = x_t Wu^T (fp32 accumulate), h = bf16(silu(g) * u),
+ *   y_slots[row] = bf16(h Wd^T)
+ *  x_dev        bf16 [T][H]
+ *  experts      E routed experts' weights; shared: the shared expert's
+ *               weights (n = 1) or NULL when n_shared == 0
+ *  y_slots_dev  bf16 [R + T*n_shared][H] out, rows in plan order
+ * h lives in the workspace. */
+moe_status_t moe_expert_ffn_w4(const moe_shape_t* shape, const void* x_dev,
+                               const moe_w4_weights_t* experts, const moe_w4_weights_t* shared,
+                               const moe_plan_t* plan, void* y_slots_dev, void* ws_dev,
+                               size_t ws_bytes, moe_stream_t stream);
+
+/* Weighted combine back to token order:
+ *   y[t] = bf16( sum_{k asc} w[t][k] * y_slots[row_pos[t*K+k]] + y_slots[R+t] )
+ * in fp32, in that fixed order (shared term only with a shared expert).
+ *  y_dev      bf16 [T][H] out
+ *  x_next_dev bf16 [T][H] out or NULL: unit-gain RMS normalisation of the
+ *             bf16 y, y / sqrt(mean(y^2) + 1e-6), the input of a stacked
+ *             next layer. */
+moe_status_t moe_combine(const moe_shape_t* shape, const void* y_slots_dev,
+                         const int32_t* row_pos_dev, const float* topk_w_dev, void* y_dev,
+                         void* x_next_dev, moe_stream_t stream);
+
+/* The whole layer (route, plan, expert FFNs, combine) with every
+ * intermediate in the workspace. Small T takes fused decode kernels that
+ * stream only the selected experts' packed bytes ([Lily] "Decode").
+ * Results equal the four calls above within the FFN's fp32 tolerance;
+ * routing is bit-identical. topk_ids_dev / topk_w_dev may be NULL. */
+moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
+                          const float* router_bias_dev, const moe_w4_weights_t* experts,
+                          const moe_w4_weights_t* shared, void* y_dev, void* x_next_dev,
+                          int32_t* topk_ids_dev, float* topk_w_dev, void* ws_dev,
+                          size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, read and clear the workspace's device status word.
+ * Returns MOE_OK, the recorded device error, or MOE_ERR_CUDA. Test and
+ * debug use: it blocks the host. */
+moe_status_t moe_query_device_status(void* ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Dequantise a packed matrix [N][Kd] (layout as in moe_w4_weights_t) to
+ * bf16 [N][Kd] with the same device routine the GEMMs use. Test use. */
+moe_status_t moe_debug_dequant_w4(const uint32_t* q_dev, const uint16_t* s_dev,
+                                  const uint16_t* b_dev, uint16_t* out_dev, int32_t N,
+                                  int32_t Kd, moe_stream_t stream);
+
+/* Static text of a status code; text of the last CUDA error seen by this
+ * thread's calls ("" if none). */
+const char* moe_status_string(moe_status_t status);
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4_H */

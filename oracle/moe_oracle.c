@@ -280,12 +280,23 @@ static void ffn_row(const double* wgu, const double* wd, const double* x, int H,
   free(h);
 }
 
+/* Dequantised matrix as doubles. Every weight of group g of row n is one of
+ * the 16 values RNE_bf16(s*q + b), q = 0..15, so the group's 16 values are
+ * formed once (orc_dequant_one's arithmetic) and selected by the nibble. */
 static double* expand(const uint32_t* qw, const uint16_t* s, const uint16_t* b,
                       int N, int Kd) {
   double* w = (double*)malloc(sizeof(double) * (size_t)N * Kd);
   for (int n = 0; n < N; ++n)
-    for (int k = 0; k < Kd; ++k)
-      w[(size_t)n * Kd + k] = orc_bf16_value(orc_dequant_one(qw, s, b, Kd, n, k));
+    for (int g = 0; g < Kd / 64; ++g) {
+      double sv = orc_bf16_value(s[(size_t)n * (Kd / 64) + g]);
+      double bv = orc_bf16_value(b[(size_t)n * (Kd / 64) + g]);
+      double tab[16];
+      for (int q = 0; q < 16; ++q) tab[q] = orc_bf16_value(orc_bf16_rne(sv * (double)q + bv));
+      for (int k = 64 * g; k < 64 * g + 64; ++k) {
+        uint32_t word = qw[(size_t)n * (Kd / 8) + k / 8];
+        w[(size_t)n * Kd + k] = tab[(word >> (4 * (k % 8))) & 15u];
+      }
+    }
   return w;
 }
 
@@ -340,6 +351,7 @@ void orc_layer_tokens(const uint16_t* x, int H, int E, int K, int I,
   for (int i = 0; i < ntok; ++i)
     for (int k = 0; k < K; ++k) nrow[ids[(size_t)tok[i] * K + k]]++;
   nrow[E] = has_shared ? ntok : 0;
+#pragma omp parallel for schedule(dynamic, 1)
   for (int e = 0; e <= E; ++e) {
     if (nrow[e] == 0) continue;
     int* which = (int*)malloc(sizeof(int) * (size_t)nrow[e]); /* i*S + slot */
@@ -349,19 +361,25 @@ void orc_layer_tokens(const uint16_t* x, int H, int E, int K, int I,
       for (int k = 0; k < K; ++k)
         if (ids[(size_t)tok[i] * K + k] == e) which[m++] = i * S + k;
     }
-    uint16_t* xr = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)m * H);
-    for (int r = 0; r < m; ++r)
-      memcpy(xr + (size_t)r * H, x + (size_t)tok[which[r] / S] * H, sizeof(uint16_t) * H);
-    double* d = (double*)malloc(sizeof(double) * (size_t)m * H);
-    if (e < E)
-      orc_expert_ffn(q_gu + e * gu_w, s_gu + e * gu_g, b_gu + e * gu_g, q_d + e * d_w,
-                     s_d + e * d_g, b_d + e * d_g, H, I, xr, m, NULL, d);
-    else
-      orc_expert_ffn(sq_gu, ss_gu, sb_gu, sq_d, ss_d, sb_d, H, I, xr, m, NULL, d);
-    for (int r = 0; r < m; ++r)
-      memcpy(dsl + (size_t)which[r] * H, d + (size_t)r * H, sizeof(double) * H);
-    free(d);
+    const uint32_t *qg, *qd;
+    const uint16_t *sg, *bg, *sd, *bd;
+    if (e < E) {
+      qg = q_gu + e * gu_w; sg = s_gu + e * gu_g; bg = b_gu + e * gu_g;
+      qd = q_d + e * d_w; sd = s_d + e * d_g; bd = b_d + e * d_g;
+    } else {
+      qg = sq_gu; sg = ss_gu; bg = sb_gu; qd = sq_d; sd = ss_d; bd = sb_d;
+    }
+    double* wgu = expand(qg, sg, bg, 2 * I, H);
+    double* wd = expand(qd, sd, bd, H, I);
+    double* xr = (double*)malloc(sizeof(double) * (size_t)H);
+    for (int r = 0; r < m; ++r) {
+      const uint16_t* xs = x + (size_t)tok[which[r] / S] * H;
+      for (int k = 0; k < H; ++k) xr[k] = orc_bf16_value(xs[k]);
+      ffn_row(wgu, wd, xr, H, I, NULL, dsl + (size_t)which[r] * H);
+    }
     free(xr);
+    free(wgu);
+    free(wd);
     free(which);
   }
   free(nrow);

@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every symbol the header declares;
+host-side validation returns its errors before any device work (no GPU
+needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import bit_moe_expert_histogram_gb300 as m
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_w4.h")
+
+
+def declared():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", txt, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return m.load()
+
+
+def test_header_declares_the_calls():
+    names = declared()
+    for n in ("moe_route", "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
+              "moe_workspace_bytes", "moe_max_blocks", "moe_query_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = C.CDLL(m.LIB_PATH)
+    missing = [n for n in declared() if not hasattr(raw, n)]
+    assert not missing, missing
+    assert set(m.EXPORTS) <= set(declared())
+
+
+def test_workspace_and_block_bounds(lib):
+    s = m.make_shape(512, 2048, 256, 8, 512, 1, 128)
+    assert m.moe_max_blocks(s) == 4096 // 128 + 256 + 512 // 128
+    ws = m.moe_workspace_bytes(s)
+    R, S = 512 * 8, 512 * 9
+    assert ws >= S * 2048 * 2 + S * 512 * 2 + 512 * 256 * 4
+    assert ws % 256 == 0
+    s1 = m.make_shape(1, 2048, 256, 8, 512, 1, 128)
+    assert m.moe_max_blocks(s1) == 1 + 8 + 1
+
+
+@pytest.mark.parametrize("bad", [dict(H=200), dict(H=128), dict(I=64), dict(K=0), dict(K=17, E=16),
+                                 dict(E=2048), dict(n_shared=2), dict(tile_rows=0),
+                                 dict(tile_rows=129), dict(T=0), dict(K=33, E=64)])
+def test_unsupported_shapes(lib, bad):
+    kw = dict(T=16, H=256, E=16, K=2, I=128, n_shared=1, tile_rows=128)
+    kw.update(bad)
+    s = m.make_shape(**kw)
+    assert m.moe_workspace_bytes(s) == 0
+    assert m.moe_max_blocks(s) == 0
+    st = lib.moe_route(C.byref(s), C.c_void_p(16), C.c_void_p(16), None, C.c_void_p(16),
+                       C.c_void_p(16), C.c_void_p(256), 1 << 30, None)
+    assert st == m.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_argument_errors_before_any_launch(lib):
+    s = m.make_shape(16, 256, 16, 2, 128, 1, 128)
+    need = m.moe_workspace_bytes(s)
+    P = C.c_void_p
+    # null input
+    assert lib.moe_route(C.byref(s), None, P(16), None, P(16), P(16), P(256), need, None) == \
+        m.MOE_ERR_INVALID_ARG
+    # misaligned hidden states
+    assert lib.moe_route(C.byref(s), P(18), P(16), None, P(16), P(16), P(256), need, None) == \
+        m.MOE_ERR_INVALID_ARG
+    # workspace too small / misaligned
+    assert lib.moe_route(C.byref(s), P(16), P(16), None, P(16), P(16), P(256), need - 1, None) == \
+        m.MOE_ERR_WORKSPACE
+    assert lib.moe_route(C.byref(s), P(16), P(16), None, P(16), P(16), P(128), need, None) == \
+        m.MOE_ERR_INVALID_ARG
+    # plan with a null buffer
+    plan = m.PlanPtrs(16, 16, 16, 16, 16, 0)
+    assert lib.moe_plan(C.byref(s), P(16), C.byref(plan), P(256), need, None) == \
+        m.MOE_ERR_INVALID_ARG
+    # ffn: shared expert required when n_shared == 1
+    w = m.W4Weights(16, 16, 16, 16, 16, 16)
+    plan = m.PlanPtrs(16, 16, 16, 16, 16, 16)
+    assert lib.moe_expert_ffn_w4(C.byref(s), P(16), C.byref(w), None, C.byref(plan), P(16),
+                                 P(256), need, None) == m.MOE_ERR_INVALID_ARG
+    wbad = m.W4Weights(16, 16, 24, 16, 16, 16)
+    assert lib.moe_expert_ffn_w4(C.byref(s), P(16), C.byref(wbad), C.byref(w), C.byref(plan),
+                                 P(16), P(256), need, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(C.byref(s), P(16), None, P(16), P(16), None, None) == \
+        m.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_dequant_w4(P(16), P(16), P(16), P(16), 4, 100, None) == \
+        m.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.moe_status_string(code)
+    assert lib.moe_status_string(99) == b"unknown status"
