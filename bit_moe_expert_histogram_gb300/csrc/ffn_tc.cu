@@ -26,6 +26,7 @@
 // Pipelines: kNS shared-memory stages of kKS reduction elements, kNA TMEM
 // stages of the rebuilt A tile. Every wait is bounded; on a timeout the CTA
 // records MOE_ERR_TIMEOUT, drains what it started, frees TMEM and returns.
+// Before exit the MMA thread waits for the arrival of every commit it issued.
 #include <atomic>
 
 #include "common.cuh"
@@ -65,8 +66,7 @@ __host__ __device__ constexpr int b_afull(int a) { return 3 * kNS + a; }
 __host__ __device__ constexpr int b_aempty(int a) { return 3 * kNS + kNA + a; }
 constexpr int kBarAccFull = 3 * kNS + 2 * kNA;
 constexpr int kBarAccEmpty = kBarAccFull + 1;
-constexpr int kBarDrain = kBarAccFull + 2;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kNumBars = kBarAccEmpty + 1;
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarAccFull), 1);
     mbar_init(bar(kBarAccEmpty), 8);
-    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -198,8 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      uint32_t it = 0, ait = 0, uc = 0;
-      bool issued = false;
+      uint32_t it = 0, ait = 0, uc = 0, nacc = 0;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
         const int blk = u / a.mtiles;
         const int nrows = a.block_map[3 * blk + 2];
@@ -231,22 +229,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ts(tmem + m * kTileN, tmem + acol, bd, idesc, (st | kk) != 0 ? 1u : 0u);
             }
           }
-          issued = true;
           mma_commit(bar(b_bfree(s)));
           mma_commit(bar(b_aempty(ai)));
         }
         if (!ok) break;
         mma_commit(bar(kBarAccFull));
+        ++nacc;
       }
       if (!ok) {
         set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 2);
         *abort_flag = 1;
       }
-      if (issued) {  // all MMAs complete before TMEM is released
-        mma_commit(bar(kBarDrain));
-        volatile int never = 0;
-        mbar_wait(bar(kBarDrain), 0, &never);
-      }
+      // Tail: each tcgen05.commit above arrives on its barrier asynchronously
+      // once the MMAs finish. Wait for the latest phase of every barrier a
+      // commit targets, so no arrive can land after this CTA has exited (and
+      // all MMAs are complete before TMEM is released).
+      volatile int never = 0;
+      for (uint32_t i = it > (uint32_t)kNS ? it - kNS : 0u; i < it; ++i)
+        mbar_wait(bar(b_bfree(i % kNS)), (i / kNS) & 1u, &never);
+      for (uint32_t i = ait > (uint32_t)kNA ? ait - kNA : 0u; i < ait; ++i)
+        mbar_wait(bar(b_aempty(i % kNA)), (i / kNA) & 1u, &never);
+      if (nacc > 0) mbar_wait(bar(kBarAccFull), (nacc - 1) & 1u, &never);
     }
   } else {
     // ------------------------------------------- dequant, then epilogue --

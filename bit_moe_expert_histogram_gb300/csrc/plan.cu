@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     if (tid == 0) *plan.num_blocks_dev = nb_total + nsb;
   }
 
-  for (int i = tid; i < kPlanWarps * E; i += kPlanThreads) (&wcnt[0][0])[i] = 0;
+  for (int i = tid; i < kPlanWarps * E; i += kPlanThreads) wcnt[i / E][i % E] = 0;
   __syncthreads();
 
   const int f0 = blockIdx.x * kPlanChunk;

@@ -247,3 +247,43 @@ def test_determinism_two_runs():
     c.run_calls()
     assert np.array_equal(h16(c.y), a)
     assert np.array_equal(h16(c.y_slots), b_)
+
+
+@pytest.mark.parametrize("E", [16, 100, 256])
+def test_plan_after_ffn_dirtied_shared_memory(E):
+    """The plan's per-warp count table must be cleared for every expert,
+    whatever earlier kernels left in shared memory (the FFN fills it)."""
+    L = layer(512, FULL, 0)
+    c = Case(L, 512, FULL)
+    c.run_calls()                      # leaves FFN data in shared memory
+    T, K = 700, 4
+    rng = np.random.default_rng(E)
+    ids = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    s = m.make_shape(T, 256, E, K, 128, 1, 64)
+    dev = torch.device("cuda")
+    ws = m.alloc_workspace(s, dev)
+    plan = m.PlanBuffers(s, dev)
+    m.moe_plan(s, torch.from_numpy(ids).to(dev), plan, ws)
+    assert m.moe_query_device_status(ws) == 0
+    P = oracle.plan(ids, E, 1, 64)
+    assert np.array_equal(plan.sorted_rows.cpu().numpy(), P["sorted_rows"])
+    assert np.array_equal(plan.row_pos.cpu().numpy(), P["row_pos"])
+    nb = int(plan.num_blocks.item())
+    assert np.array_equal(plan.block_map.cpu().numpy().reshape(-1, 3)[:nb], P["block_map"])
+
+
+def test_back_to_back_steps_match_single_step():
+    """20 full layer steps queued without a host sync give the same bits as
+    one step, and the oracle's output within tolerance."""
+    L = layer(512, FULL, 0)
+    c = Case(L, 512, FULL)
+    c.run_calls()
+    y1 = h16(c.y).copy()
+    for _ in range(20):
+        m.moe_route(c.shape, c.x, c.wr, c.bias, c.ids, c.w, c.ws)
+        m.moe_plan(c.shape, c.ids, c.plan, c.ws)
+        m.moe_expert_ffn_w4(c.shape, c.x, c.ex, c.sh, c.plan, c.y_slots, c.ws)
+        m.moe_combine(c.shape, c.y_slots, c.plan.row_pos, c.w, c.y, None)
+    assert m.moe_query_device_status(c.ws) == 0
+    assert np.array_equal(h16(c.y), y1)
+    _ffn_check(c, L, np.arange(0, 512, 8))
