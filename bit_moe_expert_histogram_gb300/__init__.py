@@ -30,7 +30,7 @@ MOE_ERR_TIMEOUT = 6
 EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_route",
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
-           "moe_last_error")
+           "moe_last_error", "moe_plan_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -88,7 +88,8 @@ def load():
                     ("moe_combine", [pS, P, P, P, P, P, P]),
                     ("moe_layer_w4", [pS, P, P, P, pW, pW, P, P, P, P, P, SZ, P]),
                     ("moe_query_device_status", [P, SZ, P]),
-                    ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P])):
+                    ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P]),
+                    ("moe_plan_noalloc", [pS, P, pP, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -153,6 +154,12 @@ def moe_expert_ffn_w4(shape, x, experts, shared, plan, y_slots, ws, stream=None)
                                     C.byref(shared.ptrs) if shared is not None else None,
                                     C.byref(plan.ptrs), _p(y_slots), _p(ws), ws.numel(),
                                     _s(stream)), "moe_expert_ffn_w4")
+
+
+def moe_plan_noalloc(shape, topk_ids, plan, stream=None):
+    """moe_plan without a workspace (static device scratch; see moe_w4.h)."""
+    _check(load().moe_plan_noalloc(C.byref(shape), _p(topk_ids), C.byref(plan.ptrs), _s(stream)),
+           "moe_plan_noalloc")
 
 
 def moe_combine(shape, y_slots, row_pos, topk_w, y, x_next=None, stream=None):

@@ -236,6 +236,12 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
 
 }  // namespace
 
+namespace moe {
+bool shape_supported(const moe_shape_t* shape) { return shape_ok(shape); }
+void set_last_error(const char* text) { g_last_error = text; }
+void set_last_cuda_error(cudaError_t e, const char* where) { cuda_fail(e, where); }
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_shape_t* shape) {

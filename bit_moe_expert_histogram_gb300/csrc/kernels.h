@@ -50,6 +50,10 @@ cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, cons
                            cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
                            int N, int Kd, cudaStream_t stream);
+// Host helpers shared by the C-ABI translation units (api.cu keeps the state).
+bool shape_supported(const moe_shape_t* shape);
+void set_last_error(const char* text);
+void set_last_cuda_error(cudaError_t e, const char* where);
 int ffn_tile_m();
 int ffn_max_tile_n();
 int ffn_stage_k();

@@ -183,6 +183,25 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
                           int32_t* topk_ids_dev, float* topk_w_dev, void* ws_dev,
                           size_t ws_bytes, moe_stream_t stream);
 
+/* moe_plan without a workspace: same inputs, same outputs, bit-identical
+ * results. The pages have no counterpart; this entry point exists for
+ * callers that cannot allocate device memory where they build the plan (code
+ * running inside a memory-pool or allocator callback, where allocating would
+ * re-enter the allocator, or a runtime that forbids cudaMalloc after
+ * start-up) and have no spare buffer to pass. Its scratch (the per-chunk
+ * histograms and a status word, 256 KiB) is one static device array that
+ * every GPU loading the library holds until the process exits. Limit:
+ * ceil(T*K/2048) * E <= 65472, else MOE_ERR_UNSUPPORTED_SHAPE (text in
+ * moe_last_error()) before anything is enqueued. The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress, with the
+ * device current), so make it before any stream capture. It allocates and
+ * frees nothing. All calls share the one array: calls that can overlap on
+ * the GPU (other streams, other host threads) race and must be ordered by
+ * the caller. Expert ids outside [0, E) are skipped, as in moe_plan, but are
+ * not reported. */
+moe_status_t moe_plan_noalloc(const moe_shape_t* shape, const int32_t* topk_ids_dev,
+                              const moe_plan_t* plan, moe_stream_t stream);
+
 /* Synchronise `stream`, read and clear the workspace's device status word.
  * Returns MOE_OK, the recorded device error, or MOE_ERR_CUDA. Test and
  * debug use: it blocks the host. */
