@@ -181,10 +181,14 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
 
   CUtensorMap tw, twsh, tx, th;
+  // packed weights: boxes of 128 rows x 32 words (256 reduction elements);
+  // a reduction length that is not a multiple of 256 reads zero-filled
+  // columns past the row end in its last box
+  const uint32_t wbox = (uint32_t)ffn_stage_k() / 8;
   MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_gate_up_dev, H / 8,
-                 (uint64_t)E * 2 * I, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+                 (uint64_t)E * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_gate_up_dev, H / 8,
-                 (uint64_t)(s->n_shared ? 1 : E) * 2 * I, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+                 (uint64_t)(s->n_shared ? 1 : E) * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, 64, 1,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   FfnArgs a{};
@@ -197,7 +201,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   a.rows_per_expert = 2 * I;
   a.half_rows = I;
   a.mtiles = I / ffn_tile_m();
-  a.kstages = H / ffn_stage_k();
+  a.kdim = H;
   a.kgroups = H / 64;
   a.s_exp = ex->s_gate_up_dev;
   a.b_exp = ex->b_gate_up_dev;
@@ -211,16 +215,16 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   if (e != cudaSuccess) return cuda_fail(e, "ffn gate_up launch");
 
   MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_down_dev, I / 8, (uint64_t)E * H,
-                 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+                 wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_down_dev, I / 8,
-                 (uint64_t)(s->n_shared ? 1 : E) * H, 16, 128, CU_TENSOR_MAP_SWIZZLE_64B));
+                 (uint64_t)(s->n_shared ? 1 : E) * H, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, 1,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   a.sorted_rows = nullptr;
   a.rows_per_expert = H;
   a.half_rows = 0;
   a.mtiles = H / ffn_tile_m();
-  a.kstages = I / ffn_stage_k();
+  a.kdim = I;
   a.kgroups = I / 64;
   a.s_exp = ex->s_down_dev;
   a.b_exp = ex->b_down_dev;
