@@ -211,6 +211,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   a.out_ld = I;
   a.ctrl = ctrl;
   a.max_units = maxb * a.mtiles;
+  a.shared_blocks = s->n_shared ? (T + s->tile_rows - 1) / s->tile_rows : 0;
   cudaError_t e = launch_ffn_gate_up(tw, twsh, tx, a, a.max_units < nsm ? a.max_units : nsm, stream);
   if (e != cudaSuccess) return cuda_fail(e, "ffn gate_up launch");
 
@@ -222,8 +223,8 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
                  CU_TENSOR_MAP_SWIZZLE_128B));
   a.sorted_rows = nullptr;
   a.rows_per_expert = H;
-  a.half_rows = 0;
-  a.mtiles = H / ffn_tile_m();
+  a.half_rows = ffn_tile_m();            // two consecutive 128-row tiles per unit
+  a.mtiles = H / (2 * ffn_tile_m());
   a.kdim = I;
   a.kgroups = I / 64;
   a.s_exp = ex->s_down_dev;

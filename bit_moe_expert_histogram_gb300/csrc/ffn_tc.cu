@@ -14,22 +14,33 @@
 // multiple of 16) over the tokens of one block-map entry, so an expert with
 // 5 rows pads to 16, not to 128.
 //
-// One persistent CTA per SM walks units u = (block-map entry, 128-row weight
-// tile). Warp roles (16 warps):
-//   warp 0       W producer: TMA of packed nibble tiles, 128 rows x 128 B
-//                (256 reduction elements) per matrix, 128-byte swizzle
-//   warp 1       B producer: the entry's activation rows, 64 elements each,
-//                gathered four rows per TMA (tile::gather4, 128-byte swizzle)
-//   warp 2       TMEM allocator and MMA issuer (one thread)
-//   warps 4..7   epilogue: tcgen05.ld of the fp32 accumulators, released as
-//                soon as they are in registers, then SwiGLU (or plain) -> bf16
-//   warps 8..15  dequantisation of the nibble tiles into TMEM (tcgen05.st)
-// Rings: kNW shared-memory W stages (freed by the dequant warps once read),
-// kNB shared-memory B stages and kNA TMEM A sub-stages (freed by the MMAs'
-// commits), kNAcc accumulator buffers (freed by the epilogue). Every wait
-// is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains what it
-// started, frees TMEM and returns. Before exit the MMA thread waits for the
-// arrival of every commit it issued.
+// A unit is (block-map entry, 256 weight rows) = two 128-row matrices with
+// one accumulator each: for gate_up the matching gate and up rows (the
+// epilogue applies SwiGLU to the pair), for down two consecutive 128-row
+// tiles of the down matrix. One persistent CTA per SM takes units from a
+// device-wide counter, the shared expert's (widest) units first; the last
+// CTA to finish resets the counter for the next launch.
+// Warp roles (24 warps):
+//   warp 0        unit queue and W producer: takes units, publishes them to
+//                 the CTA through a small shared-memory queue, and loads the
+//                 packed nibble tiles by TMA, 128 rows x 128 B (256 reduction
+//                 elements) per matrix, 128-byte swizzle
+//   warp 1        B producer: the entry's activation rows, 64 elements each,
+//                 gathered four rows per TMA (tile::gather4, 128-byte swizzle)
+//   warp 2        TMEM allocator and MMA issuer (one thread)
+//   warps 4..7    epilogue: tcgen05.ld of the fp32 accumulators, released as
+//                 soon as they are in registers, then SwiGLU (or plain) -> bf16
+//   warps 8..23   dequantisation of the nibble tiles into TMEM (tcgen05.st);
+//                 each thread rebuilds half of one row's 64-element slice
+// Rings: kNW shared-memory W stages (freed by the dequant warps once read,
+// behind a proxy fence); kNS slots of kKS reduction elements, each a
+// shared-memory B stage plus a TMEM A stage, filled under one barrier (the
+// dequant warps' arrivals and the B gathers' bytes) and freed together by
+// one MMA commit, so the MMA thread synchronises once per 16 MMAs; one
+// accumulator pair (freed by the epilogue). Roles that mostly wait sleep in their barrier waits. Every
+// wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains what
+// it started, frees TMEM and returns. Before exit the MMA thread waits for
+// the arrival of every commit it issued.
 #include <atomic>
 
 #include "common.cuh"
@@ -38,47 +49,47 @@
 namespace moe {
 
 namespace {
-constexpr int kTileM = 128;                // weight rows per tile (MMA M)
+constexpr int kTileM = 128;                // weight rows per matrix (MMA M)
 constexpr int kTileN = 128;                // most tokens per tile (MMA N)
+constexpr int kMats = 2;                   // matrices (accumulators) per unit
 constexpr int kKW = 256;                   // reduction elements per W stage
-constexpr int kKA = 64;                    // reduction elements per A / B sub-stage
-constexpr int kSub = kKW / kKA;            // sub-stages per W stage
+constexpr int kKA = 64;                    // reduction elements per 128-byte swizzle atom
+constexpr int kKS = 128;                   // reduction elements per slot (MMA handshake)
+constexpr int kSlotsPerW = kKW / kKS;      // slots per W stage
 constexpr int kNW = 4;                     // W stages (shared memory)
-constexpr int kNB = 4;                     // B stages (shared memory)
-constexpr int kNA = 4;                     // A sub-stages (TMEM)
-constexpr int kThreads = 512;
-constexpr int kDequantWarps = 8;
+constexpr int kNS = 2;                     // slots: B (shared memory) + A (TMEM)
+constexpr int kNU = 4;                     // unit queue slots
+constexpr int kDequantWarps = 16;
 constexpr int kEpiWarps = 4;
-constexpr int kBStage = kTileN * 128;      // 128 rows x 64 bf16
+constexpr int kUnitReaders = 2 + kEpiWarps + kDequantWarps;  // B producer, MMA, epilogue, dequant
+constexpr int kThreads = (8 + kDequantWarps) * 32;
+constexpr int kBAtom = kTileN * 128;       // 128 rows x 64 bf16
+constexpr int kBStage = (kKS / kKA) * kBAtom;  // one slot of B: two atoms
 constexpr int kWMat = kTileM * (kKW / 2);  // 128 rows x 128 B of nibbles
-
-template <bool GATED>
-struct Cfg {
-  static constexpr int kMats = GATED ? 2 : 1;
-  static constexpr int kNAcc = GATED ? 1 : 2;
-  static constexpr int kWStage = kMats * kWMat;
-  static constexpr int kAccCols = kMats * kTileN;      // one accumulator buffer
-  static constexpr int kACols = kMats * (kKA / 2);     // 2 bf16 per 32-bit column
-  static constexpr int kABase = kNAcc * kAccCols;
-  static constexpr int kTmemCols = 512;
-  static constexpr int kSmemW = 0;
-  static constexpr int kSmemB = kNW * kWStage;
-  static constexpr int kSmemBar = kSmemB + kNB * kBStage;
-  static constexpr int kSmemBytes = kSmemBar + 512 + 1024;
-  static_assert(kABase + kNA * kACols <= kTmemCols, "TMEM budget");
-};
+constexpr int kWStage = kMats * kWMat;
+constexpr int kAccCols = kMats * kTileN;   // accumulator pair
+constexpr int kACols = kMats * (kKS / 2);  // A columns per slot (2 bf16 per column)
+constexpr int kABase = kAccCols;
+constexpr int kTmemCols = 512;
+constexpr int kSmemW = 0;
+constexpr int kSmemB = kNW * kWStage;
+constexpr int kSmemBar = kSmemB + kNS * kBStage;
+constexpr int kSmemBytes = kSmemBar + 512 + 1024;
+static_assert(kABase + kNS * kACols <= kTmemCols, "TMEM budget");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // barrier slots
 __host__ __device__ constexpr int b_wfull(int s) { return s; }
 __host__ __device__ constexpr int b_wfree(int s) { return kNW + s; }
-__host__ __device__ constexpr int b_bfull(int s) { return 2 * kNW + s; }
-__host__ __device__ constexpr int b_bfree(int s) { return 2 * kNW + kNB + s; }
-__host__ __device__ constexpr int b_afull(int a) { return 2 * kNW + 2 * kNB + a; }
-__host__ __device__ constexpr int b_aempty(int a) { return 2 * kNW + 2 * kNB + kNA + a; }
-__host__ __device__ constexpr int b_accfull(int i) { return 2 * kNW + 2 * kNB + 2 * kNA + i; }
-__host__ __device__ constexpr int b_accempty(int i) { return 2 * kNW + 2 * kNB + 2 * kNA + 2 + i; }
-constexpr int kNumBars = 2 * kNW + 2 * kNB + 2 * kNA + 4;
-static_assert(kNumBars * 8 + 8 <= 512, "barrier area");
+__host__ __device__ constexpr int b_sfull(int s) { return 2 * kNW + s; }
+__host__ __device__ constexpr int b_sfree(int s) { return 2 * kNW + kNS + s; }
+__host__ __device__ constexpr int b_ufull(int q) { return 2 * kNW + 2 * kNS + q; }
+__host__ __device__ constexpr int b_uempty(int q) { return 2 * kNW + 2 * kNS + kNU + q; }
+constexpr int kBarAccFull = 2 * kNW + 2 * kNS + 2 * kNU;
+constexpr int kBarAccEmpty = kBarAccFull + 1;
+constexpr int kNumBars = kBarAccEmpty + 1;
+constexpr int kRingOff = kNumBars * 8 + 8;  // unit queue (ints) after the barriers
+static_assert(kRingOff + 4 * kNU <= 512, "barrier area");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -104,18 +115,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm,
       "l"(tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -139,21 +138,38 @@ __device__ __forceinline__ Unit load_unit(const FfnArgs& a, int u) {
   t.nrows = a.block_map[3 * blk + 2];
   return t;
 }
+
+// Next unit from the CTA's queue (published by the W producer); -1 = no more.
+// Every lane of the calling warp waits; one arrival per warp frees the slot.
+__device__ __forceinline__ bool next_unit(uint32_t ufull, uint32_t uempty, const volatile int* ring,
+                                          uint32_t uc, volatile int* abort, int lane, int* u) {
+  const int q = uc % kNU;
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(ufull + 8u * q, (uc / kNU) & 1u, abort)))
+    return false;
+  *u = ring[q];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(uempty + 8u * q);
+  return true;
+}
 }  // namespace
 
+// GATED (gate_up): matrix 0 = gate rows mt*128.., matrix 1 = up rows
+// I + mt*128.. (a.half_rows = I); the epilogue writes bf16(silu(g) * u) to
+// column mt*128 + r. Otherwise (down): matrices are rows mt*256.. and
+// mt*256 + 128.. (a.half_rows = 128), written to columns mt*256 + 128*m + r.
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_w4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_wsh,
                   const __grid_constant__ CUtensorMap tm_b, const FfnArgs a) {
-  using C = Cfg<GATED>;
+  constexpr int kMtRows = GATED ? kTileM : 2 * kTileM;  // weight rows advanced per M tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (sbase - raw);
-  const uint32_t sW = sbase + C::kSmemW, sB = sbase + C::kSmemB, sBar = sbase + C::kSmemBar;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kSmemBar + kNumBars * 8);
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(gbase + C::kSmemBar + kNumBars * 8 + 4);
+  const uint32_t sW = sbase + kSmemW, sB = sbase + kSmemB, sBar = sbase + kSmemBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kSmemBar + kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kSmemBar + kNumBars * 8 + 4);
+  volatile int* ring = reinterpret_cast<volatile int*>(gbase + kSmemBar + kRingOff);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,18 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(b_wfull(s)), 1);
       mbar_init(bar(b_wfree(s)), kDequantWarps);
     }
-    for (int s = 0; s < kNB; ++s) {
-      mbar_init(bar(b_bfull(s)), 1);
-      mbar_init(bar(b_bfree(s)), 1);
+    for (int s = 0; s < kNS; ++s) {
+      // slot full: every dequant warp, plus the B producer's expect_tx arrival
+      mbar_init(bar(b_sfull(s)), kDequantWarps + 1);
+      mbar_init(bar(b_sfree(s)), 1);
     }
-    for (int i = 0; i < kNA; ++i) {
-      mbar_init(bar(b_afull(i)), kDequantWarps);
-      mbar_init(bar(b_aempty(i)), 1);
+    for (int q = 0; q < kNU; ++q) {
+      mbar_init(bar(b_ufull(q)), 1);
+      mbar_init(bar(b_uempty(q)), kUnitReaders);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(b_accfull(i)), 1);
-      mbar_init(bar(b_accempty(i)), kEpiWarps);
-    }
+    mbar_init(bar(kBarAccFull), 1);
+    mbar_init(bar(kBarAccEmpty), kEpiWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_b);
   if (warp == 2) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -193,30 +208,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int units = min(*a.num_blocks * a.mtiles, a.max_units);
   const int wstages = (a.kdim + kKW - 1) / kKW;  // W stages per unit (the last may be half)
-  const int bstages = a.kdim / kKA;              // B / A sub-stages per unit
+  const int bstages = a.kdim / kKS;              // slots per unit
+  const uint32_t ufull0 = bar(b_ufull(0)), uempty0 = bar(b_uempty(0));
   bool ok = true;
 
   if (warp == 0) {
-    // -------------------------------------------------------- W producer --
+    // ------------------------------------ unit queue + W producer (lane 0) --
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint32_t it = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      // shared-expert units (the last block-map entries, the widest) go first
+      const int shared_units = min(a.shared_blocks * a.mtiles, units);
+      const int routed_units = units - shared_units;
+      uint32_t it = 0, uc = 0;
+      for (;; ++uc) {
+        const int q = uc % kNU;
+        if (!mbar_wait_sleep(bar(b_uempty(q)), ((uc / kNU) & 1u) ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const unsigned v = atomicAdd(&a.ctrl->unit_next, 1u);
+        const int u = (v >= (unsigned)units) ? -1
+                      : ((int)v < shared_units ? routed_units + (int)v : (int)v - shared_units);
+        ring[q] = u;
+        mbar_arrive(bar(b_ufull(q)));
+        if (u < 0) break;
         const Unit t = load_unit(a, u);
         const CUtensorMap* tw = (t.e < a.E) ? &tm_w : &tm_wsh;
-        const int wrow = (t.e < a.E ? t.e : 0) * a.rows_per_expert + t.mt * kTileM;
+        const int wrow = (t.e < a.E ? t.e : 0) * a.rows_per_expert + t.mt * kMtRows;
         for (int st = 0; st < wstages; ++st, ++it) {
           const int s = it % kNW;
-          if (!mbar_wait(bar(b_wfree(s)), ((it / kNW) & 1u) ^ 1u, abort_flag)) {
+          if (!mbar_wait_sleep(bar(b_wfree(s)), ((it / kNW) & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(b_wfull(s)), (uint32_t)C::kWStage);
-          tma_load_2d(sW + s * C::kWStage, tw, st * (kKW / 8), wrow, bar(b_wfull(s)), pol);
-          if (GATED)
-            tma_load_2d(sW + s * C::kWStage + kWMat, tw, st * (kKW / 8), wrow + a.half_rows,
-                        bar(b_wfull(s)), pol);
+          mbar_arrive_expect_tx(bar(b_wfull(s)), (uint32_t)kWStage);
+          tma_load_2d(sW + s * kWStage, tw, st * (kKW / 8), wrow, bar(b_wfull(s)), pol);
+          tma_load_2d(sW + s * kWStage + kWMat, tw, st * (kKW / 8), wrow + a.half_rows,
+                      bar(b_wfull(s)), pol);
         }
+        if (!ok) break;
       }
       if (!ok) {
         set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 1);
@@ -225,11 +255,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t i = it > (uint32_t)kNW ? it - kNW : 0u; i < it; ++i)
           mbar_wait(bar(b_wfull(i % kNW)), (i / kNW) & 1u, &never);
       }
+      // this CTA takes no more units; the last CTA to get here resets the counter
+      __threadfence();
+      if (atomicAdd(&a.ctrl->unit_done, 1u) == gridDim.x - 1) {
+        atomicExch(&a.ctrl->unit_next, 0u);
+        atomicExch(&a.ctrl->unit_done, 0u);
+      }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- B producer --
-    uint32_t it = 0;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    uint32_t it = 0, uc = 0;
+    int u = -1;
+    while (ok) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+        ok = false;
+        break;
+      }
+      if (u < 0) break;
       const Unit t = load_unit(a, u);
       const int ngroups = (t.nrows + 3) >> 2;  // gather4 groups of rows
       int src[4];
@@ -239,71 +281,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = t.row0 + n;
         src[j] = GATED ? (r < a.R ? a.sorted_rows[r] / a.K : r - a.R) : r;
       }
-      const uint32_t bytes = (uint32_t)ngroups * 4 * 128;
+      const uint32_t bytes = (uint32_t)ngroups * 4 * 128 * (kKS / kKA);
       for (int st = 0; st < bstages; ++st, ++it) {
-        const int s = it % kNB;
+        const int s = it % kNS;
         bool good = true;
-        if (lane == 0) good = mbar_wait(bar(b_bfree(s)), ((it / kNB) & 1u) ^ 1u, abort_flag);
+        if (lane == 0) good = mbar_wait_sleep(bar(b_sfree(s)), ((it / kNS) & 1u) ^ 1u, abort_flag);
         if (!__shfl_sync(0xFFFFFFFFu, good ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(b_bfull(s)), bytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar(b_sfull(s)), bytes);
         __syncwarp();
-        if (lane < ngroups)
-          tma_gather4(sB + s * kBStage + lane * 512, &tm_b, st * kKA, src[0], src[1], src[2],
-                      src[3], bar(b_bfull(s)));
+        if (lane < ngroups) {
+#pragma unroll
+          for (int at = 0; at < kKS / kKA; ++at)
+            tma_gather4(sB + s * kBStage + at * kBAtom + lane * 512, &tm_b, st * kKS + at * kKA,
+                        src[0], src[1], src[2], src[3], bar(b_sfull(s)));
+        }
       }
     }
     if (!ok && lane == 0) {
       set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 2);
       *abort_flag = 1;
       volatile int never = 0;
-      for (uint32_t i = it > (uint32_t)kNB ? it - kNB : 0u; i < it; ++i)
-        mbar_wait(bar(b_bfull(i % kNB)), (i / kNB) & 1u, &never);
+      for (uint32_t i = it > (uint32_t)kNS ? it - kNS : 0u; i < it; ++i)
+        mbar_wait(bar(b_sfull(i % kNS)), (i / kNS) & 1u, &never);
     }
   } else if (warp == 2) {
     // -------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      uint32_t it = 0, uc = 0, committed = 0;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+    uint32_t it = 0, uc = 0, committed = 0;
+    int u = -1;
+    const uint64_t bdesc0 = smem_desc_sw128(sB);
+    while (ok) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+        ok = false;
+        break;
+      }
+      if (u < 0) break;
+      if (lane == 0) {
         const Unit t = load_unit(a, u);
         const int n_mma = max(16, (t.nrows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(kTileM, n_mma);
-        const int buf = uc % C::kNAcc;
-        const uint32_t use = uc / C::kNAcc;
-        if (!mbar_wait(bar(b_accempty(buf)), (use & 1u) ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait_sleep(bar(kBarAccEmpty), (committed & 1u) ^ 1u, abort_flag)) ok = false;
         tc_fence_after();
-        const uint32_t dcol = buf * C::kAccCols;
-        for (int st = 0; st < bstages; ++st, ++it) {
-          const int s = it % kNB, ai = it % kNA;
-          if (!mbar_wait(bar(b_bfull(s)), (it / kNB) & 1u, abort_flag) ||
-              !mbar_wait(bar(b_afull(ai)), (it / kNA) & 1u, abort_flag)) {
+        for (int st = 0; st < bstages && ok; ++st, ++it) {
+          const int s = it % kNS;
+          const uint32_t ph = (it / kNS) & 1u;
+          if (!mbar_wait_spin(bar(b_sfull(s)), ph, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bst = sB + s * kBStage;
+          // B descriptor of this slot (+2 per 16 elements = 32 bytes within an
+          // atom, +kBAtom/16 per atom), A columns: matrix m at +m*kKS/2
+          const uint64_t bd = bdesc0 + (uint64_t)(s * (kBStage >> 4));
+          const uint32_t a0 = tmem + kABase + s * kACols;
+          mma_bf16_ts(tmem, a0, bd, idesc, st != 0 ? 1u : 0u);
+          mma_bf16_ts(tmem + kTileN, a0 + kKS / 2, bd, idesc, st != 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kKA / 16; ++kk) {
-            const uint64_t bd = smem_desc_sw128(bst + kk * 32);
-#pragma unroll
-            for (int m = 0; m < C::kMats; ++m) {
-              const uint32_t acol = C::kABase + ai * C::kACols + m * (kKA / 2) + kk * 8;
-              mma_bf16_ts(tmem + dcol + m * kTileN, tmem + acol, bd, idesc,
-                          (st | kk) != 0 ? 1u : 0u);
-            }
+          for (int kk = 1; kk < kKS / 16; ++kk) {
+            const uint64_t bk = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
+            mma_bf16_ts_acc(tmem, a0 + kk * 8, bk, idesc);
+            mma_bf16_ts_acc(tmem + kTileN, a0 + kKS / 2 + kk * 8, bk, idesc);
           }
-          mma_commit(bar(b_bfree(s)));
-          mma_commit(bar(b_aempty(ai)));
+          mma_commit(bar(b_sfree(s)));  // frees this slot's B stage and A stage
         }
-        if (!ok) break;
-        mma_commit(bar(b_accfull(buf)));
-        ++committed;
+        if (ok) {
+          mma_commit(bar(kBarAccFull));
+          ++committed;
+        }
       }
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
       if (!ok) {
         set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 3);
         *abort_flag = 1;
@@ -313,49 +363,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       // commit targets, so no arrive can land after this CTA has exited (and
       // all MMAs are complete before TMEM is released).
       volatile int never = 0;
-      for (uint32_t i = it > (uint32_t)kNB ? it - kNB : 0u; i < it; ++i)
-        mbar_wait(bar(b_bfree(i % kNB)), (i / kNB) & 1u, &never);
-      for (uint32_t i = it > (uint32_t)kNA ? it - kNA : 0u; i < it; ++i)
-        mbar_wait(bar(b_aempty(i % kNA)), (i / kNA) & 1u, &never);
-      for (uint32_t i = committed > (uint32_t)C::kNAcc ? committed - C::kNAcc : 0u;
-           i < committed; ++i)
-        mbar_wait(bar(b_accfull(i % C::kNAcc)), (i / C::kNAcc) & 1u, &never);
+      for (uint32_t i = it > (uint32_t)kNS ? it - kNS : 0u; i < it; ++i)
+        mbar_wait(bar(b_sfree(i % kNS)), (i / kNS) & 1u, &never);
+      if (committed > 0) mbar_wait(bar(kBarAccFull), (committed - 1) & 1u, &never);
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue --
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // accumulator row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint32_t uc = 0;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-      const Unit t = load_unit(a, u);
-      const int buf = uc % C::kNAcc;
-      const uint32_t use = uc / C::kNAcc;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(b_accfull(buf)), use & 1u, abort_flag))) {
+    uint32_t uc = 0, done = 0;
+    int u = -1;
+    while (ok) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
         ok = false;
         break;
       }
+      if (u < 0) break;
+      const Unit t = load_unit(a, u);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(kBarAccFull), done & 1u, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++done;
       tc_fence_after();
-      const uint32_t dbase = tmem + lane_off + buf * C::kAccCols;
+      const uint32_t dbase = tmem + lane_off;
       const int nch = (t.nrows + 15) >> 4;  // >= 1
-      uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + t.mt * kTileM + r;
+      uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + t.mt * kMtRows + r;
       for (int ci = 0; ci < nch; ++ci) {
         uint32_t g[16], uu[16];
         tmem_ld16(dbase + ci * 16, g);
-        if (GATED) tmem_ld16(dbase + kTileN + ci * 16, uu);
+        tmem_ld16(dbase + kTileN + ci * 16, uu);
         tmem_wait_ld();
-        if (ci == nch - 1) {  // accumulator fully read: hand it back to the MMA
+        if (ci == nch - 1) {  // accumulators fully read: hand them back to the MMA
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(b_accempty(buf)));
+          if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
         }
         const int nlim = min(16, t.nrows - ci * 16);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (i < nlim) {
-            float v = __uint_as_float(g[i]);
-            if (GATED) v = v / (1.0f + expf(-v)) * __uint_as_float(uu[i]);
-            out[(size_t)(ci * 16 + i) * a.out_ld] = (uint16_t)f2bf(v);
+            uint16_t* o = out + (size_t)(ci * 16 + i) * a.out_ld;
+            const float gv = __uint_as_float(g[i]), uv = __uint_as_float(uu[i]);
+            if (GATED) {
+              o[0] = (uint16_t)f2bf(gv / (1.0f + expf(-gv)) * uv);
+            } else {
+              o[0] = (uint16_t)f2bf(gv);
+              o[kTileM] = (uint16_t)f2bf(uv);
+            }
           }
         }
       }
@@ -366,17 +422,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------ dequant into TMEM --
-    const int d = warp - 8;
-    const int quarter = warp & 3;
-    const int part = d >> 2;             // GATED: gate/up; else: half of the row slice
+    const int d = warp - 8;              // 0..15
+    const int quarter = warp & 3;        // TMEM lanes this warp may touch
+    const int grp = d >> 2;              // 0..3
+    const int mat = grp >> 1;            // matrix 0 / 1
+    const int kh = grp & 1;              // half of each 64-element slice
     const int r = quarter * 32 + lane;   // tile row == TMEM lane
-    const int mat = GATED ? part : 0;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t sw = (uint32_t)(r & 7);
-    uint32_t wit = 0, ait = 0;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    uint32_t wit = 0, ait = 0, uc = 0;
+    int u = -1;
+    while (ok) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+        ok = false;
+        break;
+      }
+      if (u < 0) break;
       const Unit t = load_unit(a, u);
-      const int wr = mat * a.half_rows + t.mt * kTileM + r;
+      const int wr = mat * a.half_rows + t.mt * kMtRows + r;
       const size_t goff = (size_t)wr * a.kgroups;
       const uint16_t* sp =
           (t.e < a.E ? a.s_exp + (size_t)t.e * a.rows_per_expert * a.kgroups : a.s_sh) + goff;
@@ -394,61 +457,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // this thread's 16-byte chunks of its row (128 B = 4 sub-stages x 2);
-        // chunk c of row r sits at chunk c ^ (r % 8) (128-byte swizzle)
-        uint4 wv[8];
-        const uint32_t rowaddr = sW + s * C::kWStage + mat * kWMat + r * 128;
+        // chunk 2j + kh of the row holds this thread's 32 elements of
+        // sub-stage j; chunk c of row r sits at chunk c ^ (r % 8) (128-byte swizzle)
+        uint4 wv[kKW / kKA];
+        const uint32_t rowaddr = sW + s * kWStage + mat * kWMat + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (GATED || (c & 1) == part) wv[c] = lds128(rowaddr + 16u * ((uint32_t)c ^ sw));
-        }
+        for (int j = 0; j < kKW / kKA; ++j)
+          wv[j] = lds128(rowaddr + 16u * ((uint32_t)(2 * j + kh) ^ sw));
         // the stage goes back to the TMA producer: order these generic-proxy
         // reads before its async-proxy refill (write-after-read across proxies)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(b_wfree(s)));
-        const int nsub = min(kSub, bstages - st * kSub);
+        const int nslot = min(kSlotsPerW, bstages - st * kSlotsPerW);
 #pragma unroll
-        for (int j = 0; j < kSub; ++j) {
-          if (j >= nsub) break;
-          const int ai = ait % kNA;
+        for (int js = 0; js < kSlotsPerW; ++js) {
+          if (js >= nslot) break;
+          const int as = ait % kNS;
           if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(bar(b_aempty(ai)), ((ait / kNA) & 1u) ^ 1u, abort_flag))) {
+                          mbar_wait(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u, abort_flag))) {
             ok = false;
             break;
           }
           ++ait;
           tc_fence_after();
-          // group 4*st + j of this row: scale/bias j of the 4 loaded
-          const uint32_t sv = (j & 2) ? s_cur.y : s_cur.x;
-          const uint32_t bv = (j & 2) ? b_cur.y : b_cur.x;
-          const uint32_t s2 = (j & 1) ? dup_hi(sv) : dup_lo(sv);
-          const uint32_t b2 = (j & 1) ? dup_hi(bv) : dup_lo(bv);
-          const uint32_t acol = C::kABase + ai * C::kACols + mat * (kKA / 2);
-          if (GATED) {
-            uint32_t v[32];
-            dequant_word(wv[2 * j].x, s2, b2, &v[0]);
-            dequant_word(wv[2 * j].y, s2, b2, &v[4]);
-            dequant_word(wv[2 * j].z, s2, b2, &v[8]);
-            dequant_word(wv[2 * j].w, s2, b2, &v[12]);
-            dequant_word(wv[2 * j + 1].x, s2, b2, &v[16]);
-            dequant_word(wv[2 * j + 1].y, s2, b2, &v[20]);
-            dequant_word(wv[2 * j + 1].z, s2, b2, &v[24]);
-            dequant_word(wv[2 * j + 1].w, s2, b2, &v[28]);
-            tmem_st32(tmem + lane_off + acol, v);
-          } else {
+#pragma unroll
+          for (int jj = 0; jj < kKS / kKA; ++jj) {
+            const int j = js * (kKS / kKA) + jj;  // 64-element group 4*st + j of this row
+            const uint32_t sv = (j & 2) ? s_cur.y : s_cur.x;
+            const uint32_t bv = (j & 2) ? b_cur.y : b_cur.x;
+            const uint32_t s2 = (j & 1) ? dup_hi(sv) : dup_lo(sv);
+            const uint32_t b2 = (j & 1) ? dup_hi(bv) : dup_lo(bv);
             uint32_t v[16];
-            const uint4 q = part ? wv[2 * j + 1] : wv[2 * j];
-            dequant_word(q.x, s2, b2, &v[0]);
-            dequant_word(q.y, s2, b2, &v[4]);
-            dequant_word(q.z, s2, b2, &v[8]);
-            dequant_word(q.w, s2, b2, &v[12]);
-            tmem_st16(tmem + lane_off + acol + part * 16, v);
+            dequant_word(wv[j].x, s2, b2, &v[0]);
+            dequant_word(wv[j].y, s2, b2, &v[4]);
+            dequant_word(wv[j].z, s2, b2, &v[8]);
+            dequant_word(wv[j].w, s2, b2, &v[12]);
+            tmem_st16(tmem + lane_off + kABase + as * kACols + mat * (kKS / 2) + jj * (kKA / 2) +
+                          kh * 16,
+                      v);
           }
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(b_afull(ai)));
+          if (lane == 0) mbar_arrive(bar(b_sfull(as)));
         }
       }
     }
@@ -462,14 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <bool GATED>
 static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& twsh, const CUtensorMap& tb,
                               const FfnArgs& a, int grid, cudaStream_t stream) {
-  using C = Cfg<GATED>;
   // the dynamic shared-memory opt-in is per device: set it once for each
   static std::atomic<unsigned long long> configured{0};
   int dev = 0;
@@ -478,11 +529,11 @@ static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& twsh, co
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(configured.load() & bit)) {
     e = cudaFuncSetAttribute(ffn_w4_kernel<GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  ffn_w4_kernel<GATED><<<grid, kThreads, C::kSmemBytes, stream>>>(tw, twsh, tb, a);
+  ffn_w4_kernel<GATED><<<grid, kThreads, kSmemBytes, stream>>>(tw, twsh, tb, a);
   return cudaGetLastError();
 }
 

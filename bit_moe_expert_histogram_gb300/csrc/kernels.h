@@ -33,6 +33,7 @@ struct FfnArgs {
   int out_ld;
   Ctrl* ctrl;
   int max_units;               // host bound on units
+  int shared_blocks;           // block-map entries of the shared expert (the last ones)
 };
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
