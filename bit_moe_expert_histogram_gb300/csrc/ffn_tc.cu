@@ -311,7 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- MMA issuer --
     uint32_t it = 0, uc = 0, committed = 0;
     int u = -1;
-    const uint64_t bdesc0 = smem_desc_sw128(sB);
+    // every operand address of a slot's 16 MMAs, computed once: B descriptor
+    // per 16-element step (+32 B inside an atom, next atom every 4 steps)
+    // and A columns (matrix m at +kKS/2), for both slots
+    uint64_t bdk[kNS][kKS / 16];
+    uint32_t ak[kNS][kKS / 16];
+#pragma unroll
+    for (int ss = 0; ss < kNS; ++ss)
+#pragma unroll
+      for (int kk = 0; kk < kKS / 16; ++kk) {
+        bdk[ss][kk] = smem_desc_sw128(sB + ss * kBStage + (kk >> 2) * kBAtom + (kk & 3) * 32);
+        ak[ss][kk] = tmem + kABase + ss * kACols + kk * 8;
+      }
     while (ok) {
       if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
         ok = false;
@@ -332,18 +343,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // B descriptor of this slot (+2 per 16 elements = 32 bytes within an
-          // atom, +kBAtom/16 per atom), A columns: matrix m at +m*kKS/2
-          const uint64_t bd = bdesc0 + (uint64_t)(s * (kBStage >> 4));
-          const uint32_t a0 = tmem + kABase + s * kACols;
-          mma_bf16_ts(tmem, a0, bd, idesc, st != 0 ? 1u : 0u);
-          mma_bf16_ts(tmem + kTileN, a0 + kKS / 2, bd, idesc, st != 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 1; kk < kKS / 16; ++kk) {
-            const uint64_t bk = bd + (uint64_t)((kk >> 2) * (kBAtom >> 4) + 2 * (kk & 3));
-            mma_bf16_ts_acc(tmem, a0 + kk * 8, bk, idesc);
-            mma_bf16_ts_acc(tmem + kTileN, a0 + kKS / 2 + kk * 8, bk, idesc);
+          const uint32_t acc = st != 0 ? 1u : 0u;
+          const uint32_t d1 = tmem + kTileN;
+#define MOE_SLOT_MMAS(SS)                                                  \
+  mma_bf16_ts(tmem, ak[SS][0], bdk[SS][0], idesc, acc);                    \
+  mma_bf16_ts(d1, ak[SS][0] + kKS / 2, bdk[SS][0], idesc, acc);            \
+  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk) {                \
+    mma_bf16_ts_acc(tmem, ak[SS][kk], bdk[SS][kk], idesc);                 \
+    mma_bf16_ts_acc(d1, ak[SS][kk] + kKS / 2, bdk[SS][kk], idesc);         \
+  }
+          if (s == 0) {
+            MOE_SLOT_MMAS(0)
+          } else {
+            MOE_SLOT_MMAS(1)
           }
+#undef MOE_SLOT_MMAS
           mma_commit(bar(b_sfree(s)));  // frees this slot's B stage and A stage
         }
         if (ok) {
@@ -453,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_next = load_groups(sp, 4 * (st + 1), a.kgroups);
           b_next = load_groups(bp, 4 * (st + 1), a.kgroups);
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(b_wfull(s)), (wit / kNW) & 1u, abort_flag))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(b_wfull(s)), (wit / kNW) & 1u, abort_flag))) {
           ok = false;
           break;
         }
@@ -474,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int js = 0; js < kSlotsPerW; ++js) {
           if (js >= nslot) break;
           const int as = ait % kNS;
-          if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u, abort_flag))) {
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u,
+                                                       abort_flag))) {
             ok = false;
             break;
           }
