@@ -270,14 +270,47 @@ class GpuWorkload:
         self.xa = torch.empty((T, S.H), dtype=torch.int16, device=dev)
         self.xb = torch.empty((T, S.H), dtype=torch.int16, device=dev)
         self.y_out = torch.empty((T * self.n_chunks, S.H), dtype=torch.int16, device=dev)
+        self.fused = m.moe_layer_path(self.shape) == 1
 
     def calls_per_layer(self):
-        return 7  # route: 2 kernels, plan: 2, ffn: 2, combine: 1
+        # fused decode: route, gate_up, down; else route: 2 kernels, plan: 2, ffn: 2, combine: 1
+        return 3 if self.fused else 7
+
+    def capture(self):
+        """CUDA graphs of the device step and of the host-buffer step (decode:
+        120 launches of about a microsecond each, so the host's launch rate
+        would otherwise set the pace)."""
+        torch = self.torch
+        self.x_pin = torch.from_numpy(self.x_host.view(np.int16)).pin_memory()
+        self.y_pin = torch.empty((self.tokens_per_step, self.S.H), dtype=torch.int16).pin_memory()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.step()
+            self.step_e2e(self.x_pin, self.y_pin)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_step):
+            self.step()
+        self.g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_e2e):
+            self.step_e2e(self.x_pin, self.y_pin)
+        torch.cuda.synchronize()
 
     def step(self, ev_pairs=None):
         """One pass of the hot path over the step's tokens (device-resident)."""
         m, S, T = self.m, self.S, self.T
         nl = len(self.layers)
+        if self.fused:
+            x = self.x_all[:T]
+            for l, (wr, bias, ex, sh) in enumerate(self.layers):
+                last = l == nl - 1
+                xn = None if last else (self.xa if l % 2 == 0 else self.xb)
+                m.moe_layer_w4(self.shape, x, wr, bias, ex, sh, self.y_out if last else self.y,
+                               self.ws, x_next=xn, topk_ids=self.ids, topk_w=self.w)
+                x = xn
+            return
         for c in range(self.n_chunks):
             x = self.x_all[c * T:(c + 1) * T]
             for l, (wr, bias, ex, sh) in enumerate(self.layers):
@@ -366,9 +399,17 @@ def run_ours(args, wl):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    if G.fused:
+        G.capture()
+        for _ in range(args.warmup):
+            G.g_step.replay()
+        torch.cuda.synchronize()
     t0.record(stream)
     for i in range(args.steps):
-        G.step(ffn_ev[i])
+        if G.fused:
+            G.g_step.replay()
+        else:
+            G.step(ffn_ev[i])
     t1.record(stream)
     torch.cuda.synchronize()
     if sampler:
@@ -378,7 +419,10 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1)
-    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
+    if G.fused:  # the unit is one layer call of the graph (3 kernels)
+        ffn_ms = ms / args.steps / len(G.layers)
+    else:
+        ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -387,26 +431,31 @@ def run_ours(args, wl):
     if st != 0:
         raise RuntimeError("device status %d after timed region" % st)
 
-    # e2e: host buffers in and out through moe_layer_w4
+    # e2e: host buffers in and out through moe_layer_w4 (decode: the same
+    # calls and copies replayed from a CUDA graph; eager calls also reported)
     x_pin = torch.from_numpy(G.x_host.view(np.int16)).pin_memory()
     y_pin = torch.empty((G.tokens_per_step, wl.shape.H), dtype=torch.int16).pin_memory()
     e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        G.step_e2e(x_pin, y_pin)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        G.step_e2e(x_pin, y_pin)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
+
+    def time_e2e(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / e_steps
+
+    e_eager_ms = time_e2e(lambda: G.step_e2e(x_pin, y_pin))
+    e_ms = time_e2e(G.g_e2e.replay) if G.fused else e_eager_ms
 
     hbm, bf16, bf16s, src = peaks()
     ms_step = ms / args.steps
     value = G.tokens_per_step * world / (ms_step / 1e3)
-    ffn_gbs = ffn_bytes / (ffn_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -434,18 +483,29 @@ def run_ours(args, wl):
                  "hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
                  "tensor_frac": round(step_flops / (ms_step / 1e3) / 1e12 / bf16s, 4),
                  "touched_experts": int((counts > 0).sum()), "max_group": int(counts.max())},
-        "roofline": {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)",
-                     "bound": "hbm", "achieved": round(ffn_gbs, 1), "peak": hbm,
-                     "peak_source": src, "unit": "GB/s", "frac": round(ffn_gbs / hbm, 4),
-                     "traffic": None, "ms_per_launch": round(ffn_ms, 5),
-                     "algorithmic_bytes_per_launch": ffn_bytes},
+        "roofline": ({"kernel": "moe_layer_w4 decode chain (dec_route, dec_gate_up, dec_down)"
+                                " per layer, CUDA graph of %d layers" % len(G.layers)}
+                     if G.fused else
+                     {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)"}),
         "e2e": {"value": round(G.tokens_per_step * world / (e_ms / 1e3), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
-                "steps": e_steps, "ms_per_step": round(e_ms, 5)},
+                "steps": e_steps, "ms_per_step": round(e_ms, 5),
+                "mode": "CUDA graph of the moe_layer_w4 calls and copies" if G.fused
+                        else "moe_layer_w4 calls",
+                "eager_value": round(G.tokens_per_step * world / (e_eager_ms / 1e3), 2)},
         "gpu_launches": G.calls_per_layer() * calls * args.steps,
+        "launch_mode": "CUDA graph replay, programmatic dependent launch" if G.fused
+                       else "eager stream launches",
         "clocks": clocks,
     }
+    unit_bytes = algo_bytes if G.fused else ffn_bytes
+    unit_gbs = unit_bytes / (ffn_ms / 1e3) / 1e9
+    line["roofline"].update({"bound": "hbm", "achieved": round(unit_gbs, 1), "peak": hbm,
+                             "peak_source": src, "unit": "GB/s",
+                             "frac": round(unit_gbs / hbm, 4), "traffic": None,
+                             "ms_per_launch": round(ffn_ms, 5),
+                             "algorithmic_bytes_per_launch": unit_bytes})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
     if rank == 0:

@@ -30,7 +30,7 @@ MOE_ERR_TIMEOUT = 6
 EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_route",
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
-           "moe_last_error", "moe_plan_noalloc")
+           "moe_last_error", "moe_plan_noalloc", "moe_layer_path")
 
 
 class MoeError(RuntimeError):
@@ -80,6 +80,8 @@ def load():
             L.moe_workspace_bytes.argtypes = [pS]
             L.moe_max_blocks.restype = I32
             L.moe_max_blocks.argtypes = [pS]
+            L.moe_layer_path.restype = I32
+            L.moe_layer_path.argtypes = [pS]
             for name, args in (
                     ("moe_workspace_init", [P, SZ, P]),
                     ("moe_route", [pS, P, P, P, P, P, P, SZ, P]),
@@ -132,6 +134,11 @@ def moe_workspace_bytes(shape):
 
 def moe_max_blocks(shape):
     return load().moe_max_blocks(C.byref(shape))
+
+
+def moe_layer_path(shape):
+    """1: moe_layer_w4 runs the fused decode kernels; 0: the four calls; -1: bad shape."""
+    return load().moe_layer_path(C.byref(shape))
 
 
 def moe_workspace_init(ws, stream=None):

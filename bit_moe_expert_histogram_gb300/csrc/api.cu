@@ -48,7 +48,8 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 }
 
 struct Layout {
-  size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, total;
+  size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
+      total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -74,6 +75,7 @@ Layout layout_of(const moe_shape_t* s) {
   L.bmap = take((size_t)max_blocks_of(s) * 12);
   L.nblk = take(4);
   L.yslots = take(S * (size_t)s->H * 2);
+  L.part = take(decode_part_floats(s->T, s->H) * 4);
   L.total = off;
   return L;
 }
@@ -253,6 +255,11 @@ size_t moe_workspace_bytes(const moe_shape_t* shape) {
   return shape_ok(shape) ? layout_of(shape).total : 0;
 }
 
+int32_t moe_layer_path(const moe_shape_t* shape) {
+  if (!shape_ok(shape)) return -1;
+  return decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared) ? 1 : 0;
+}
+
 int32_t moe_max_blocks(const moe_shape_t* shape) {
   return shape_ok(shape) ? (int32_t)max_blocks_of(shape) : 0;
 }
@@ -346,6 +353,30 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   plan.num_blocks_dev = reinterpret_cast<int32_t*>(ws + L.nblk);
   void* y_slots = ws + L.yslots;
   cudaStream_t st = (cudaStream_t)stream;
+  if (decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared)) {
+    DecodeArgs d{};
+    d.x = static_cast<const uint16_t*>(x_dev);
+    d.wr = static_cast<const uint16_t*>(w_router_dev);
+    d.bias = router_bias_dev;
+    d.T = shape->T;
+    d.H = shape->H;
+    d.E = shape->E;
+    d.K = shape->K;
+    d.I = shape->I;
+    d.ns = shape->n_shared;
+    d.ex = *experts;
+    d.sh = shape->n_shared ? *shared : *experts;
+    d.logits = reinterpret_cast<float*>(ws + L.logits);
+    d.ids = ids;
+    d.w = w;
+    d.h = reinterpret_cast<uint16_t*>(ws + L.h);
+    d.y = static_cast<uint16_t*>(y_dev);
+    d.x_next = static_cast<uint16_t*>(x_next_dev);
+    d.part = reinterpret_cast<float*>(ws + L.part);
+    d.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+    cudaError_t e = launch_decode_layer(d, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
+  }
   MOE_TRY(moe_route(shape, x_dev, w_router_dev, router_bias_dev, ids, w, ws_dev, ws_bytes, stream));
   MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
   MOE_TRY(run_ffn(shape, x_dev, experts, shared, &plan, y_slots, ws, st));

@@ -16,10 +16,12 @@ namespace moe {
 struct Ctrl {
   int err;           // first device error (moe_status_t), 0 = none
   int err_info[3];   // where it happened (kernel id, block, detail)
-  unsigned ticket;   // last-block counter of the fused decode router
+  unsigned ticket;   // reserved
   unsigned unit_next;  // grouped GEMM: next unit to hand out (reset by the last CTA)
   unsigned unit_done;  // grouped GEMM: CTAs finished handing out units
-  int pad[57];
+  unsigned ticket2;  // last-block counter of the decode down kernel (RMS norm)
+  unsigned routed;   // decode: 1 once this layer's ids / w are published
+  int pad[55];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
@@ -72,6 +74,23 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b
 
 __device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }
 __device__ __forceinline__ uint32_t dup_hi(uint32_t v) { return __byte_perm(v, 0, 0x3232); }
+
+// ------------------------------------------------ dependent launches --
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor in the stream finishes.
+// pdl_wait() blocks until the predecessor grid has completed and its writes
+// are visible; pdl_trigger() lets the successor launch once every block of
+// this grid has triggered or exited. Both are no-ops in a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Asks L2 to fetch [p, p + bytes) (16-byte aligned, bytes % 16 == 0); no
+// data reaches the thread, so the copy can never be stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // --------------------------------------------------------------- timing --
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -1,0 +1,542 @@
+// MoE layer for a few tokens (decode): only the selected experts' packed
+// bytes are streamed, with coalesced 16-byte loads, on the CUDA cores.
+//
+// "Perplexity Open Sources Lily: A Rust + Metal Inference Engine for
+// Qwen3.6-35B-A3B on Apple Silicon", section "Decode: Minimize Bytes Moved
+// Per Token": batch-1 decode reuses almost no weight, so bytes moved set the
+// time; kernel chains are fused so intermediates stay on chip. Three
+// launches per layer:
+//   dec_route   fixed-order fp32 router logits, one warp per token x expert
+//               (the prefill router's order, so the ids are bit-identical)
+//   dec_gate_up every block selects the top-K itself from the logits (no
+//               serial tail); block 0 publishes ids / weights. Warps take 4
+//               gate rows and the matching 4 up rows of one slot; SwiGLU -> h
+//   dec_down    one block per 8 output columns of a token, one warp per
+//               slot: the slot's down rows times its h, then the slots
+//               weighted and summed in fp32 in slot order (shared expert
+//               weight 1) -> bf16 y; with x_next the last block to finish
+//               writes the unit-RMS normalised next-layer input
+// A weight is rebuilt to bf16 exactly as in the grouped GEMM (one rounding
+// of scale*q + bias); products are exact and sums fp32.
+#include "common.cuh"
+#include "kernels.h"
+#include "topk.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kGuWarps = kTopkThreads / 32;  // gate_up: warps per block
+constexpr int kDownRows = 8;                 // down: output columns per block
+constexpr int kDownMaxWarps = 16;            // down: warps per block (slots beyond loop)
+constexpr int kGuPairs = 4;  // gate_up: gate rows (and as many up rows) per warp
+constexpr int kGuRows = 2 * kGuPairs;
+constexpr int kGuPre = 2;    // gate_up: 16-byte chunks per lane and row in one batch of loads
+
+// 8 nibbles -> 4 bf16x2 words; word i holds elements i (low half) and i+4
+// (high half), each bf16(s*q + b) with one rounding: the arithmetic of
+// dequant_word, paired (i, i+4) so that one shift and one mask place both
+// nibbles.
+__device__ __forceinline__ void dequant_word_i4(uint32_t w, uint32_t s2, uint32_t b2,
+                                                uint32_t out[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t m = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+    uint32_t q;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(m), "r"(0x3F803F80u), "r"(0xC300C300u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out[i]) : "r"(q), "r"(s2), "r"(b2));
+  }
+}
+
+// acc + lo(p)*half(xa) + hi(p)*half(xb), half = low (HI=0) or high (HI=1):
+// fp32 fma with bf16 operands (the product is exact, one rounding per fma,
+// the same result as converting both operands to fp32 first).
+template <int HI>
+__device__ __forceinline__ float fma_pair(uint32_t p, uint32_t xa, uint32_t xb, float acc) {
+  if (HI == 0)
+    asm("{\n\t.reg .b16 pl, ph, al, ah, bl, bh;\n\t"
+        "mov.b32 {pl, ph}, %1;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, pl, al, %0;\n\tfma.rn.f32.bf16 %0, ph, bl, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(p), "r"(xa), "r"(xb));
+  else
+    asm("{\n\t.reg .b16 pl, ph, al, ah, bl, bh;\n\t"
+        "mov.b32 {pl, ph}, %1;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, pl, ah, %0;\n\tfma.rn.f32.bf16 %0, ph, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(p), "r"(xa), "r"(xb));
+  return acc;
+}
+
+// acc + the 8 products of packed word q (group scale s2, bias b2 in both
+// halves) with 8 bf16 activations in natural pairs v = (x0x1, x2x3, x4x5,
+// x6x7): weight pair i of dequant_word_i4 meets (xi, xi+4).
+__device__ __forceinline__ float dot8(uint32_t q, uint32_t s2, uint32_t b2, const uint4& v,
+                                     float acc) {
+  uint32_t p[4];
+  dequant_word_i4(q, s2, b2, p);
+  acc = fma_pair<0>(p[0], v.x, v.z, acc);
+  acc = fma_pair<1>(p[1], v.x, v.z, acc);
+  acc = fma_pair<0>(p[2], v.y, v.w, acc);
+  acc = fma_pair<1>(p[3], v.y, v.w, acc);
+  return acc;
+}
+
+// acc + the 32 products of one 16-byte chunk of packed weights (4 words)
+// with the chunk's 32 activations (4 x 8 bf16).
+__device__ __forceinline__ float dot32(const uint4& q, uint32_t s2, uint32_t b2, const uint4 xv[4],
+                                      float acc) {
+  acc = dot8(q.x, s2, b2, xv[0], acc);
+  acc = dot8(q.y, s2, b2, xv[1], acc);
+  acc = dot8(q.z, s2, b2, xv[2], acc);
+  acc = dot8(q.w, s2, b2, xv[3], acc);
+  return acc;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+  return v;
+}
+
+// Activation rows in shared memory, bf16: chunk c (elements 32c..32c+31,
+// 64 bytes) keeps its 16-byte piece v at (v + c/2) mod 4. A lane reads the
+// four pieces of its own chunk and consecutive lanes take consecutive
+// chunks, so each 8-lane phase of a 16-byte load touches 8 distinct bank
+// quads.
+__device__ __forceinline__ int act_piece_off(int c, int v) { return c * 64 + 16 * ((v + (c >> 1)) & 3); }
+
+__device__ __forceinline__ void act_load_chunk(const uint8_t* row, int c, uint4 xv[4]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) xv[v] = *reinterpret_cast<const uint4*>(row + act_piece_off(c, v));
+}
+
+// Copies n bf16 (n % 32 == 0) written by an earlier kernel, read through L2,
+// into the layout above.
+__device__ __forceinline__ void act_stage(const uint16_t* __restrict__ src, uint8_t* dst, int n) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
+    *reinterpret_cast<uint4*>(dst + act_piece_off(i >> 2, i & 3)) = __ldcg(s + i);
+}
+
+struct SlotW {
+  const uint32_t* q;
+  const uint16_t* s;
+  const uint16_t* b;
+  bool ok;
+};
+
+// Weights of a slot: routed expert e (k < K; ok = e in [0, E)), else the
+// shared expert; rows = weight rows per expert, wpr / gpr = words / groups
+// per row.
+__device__ __forceinline__ SlotW slot_weights(const DecodeArgs& a, bool gate_up, int k, int e,
+                                              int rows, int wpr, int gpr) {
+  SlotW r;
+  if (k < a.K) {
+    r.ok = e >= 0 && e < a.E;
+    const size_t ee = r.ok ? (size_t)e : 0;
+    r.q = (gate_up ? a.ex.q_gate_up_dev : a.ex.q_down_dev) + ee * rows * wpr;
+    r.s = (gate_up ? a.ex.s_gate_up_dev : a.ex.s_down_dev) + ee * rows * gpr;
+    r.b = (gate_up ? a.ex.b_gate_up_dev : a.ex.b_down_dev) + ee * rows * gpr;
+  } else {
+    r.ok = true;
+    r.q = gate_up ? a.sh.q_gate_up_dev : a.sh.q_down_dev;
+    r.s = gate_up ? a.sh.s_gate_up_dev : a.sh.s_down_dev;
+    r.b = gate_up ? a.sh.b_gate_up_dev : a.sh.b_down_dev;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const unsigned* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel(unsigned* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// One batch of gate_up loads: chunks c = c0 + 32u (u < kGuPre) of the
+// warp's kGuRows rows; sb = scale (low half) | bias (high half).
+struct GuBatch {
+  uint4 q[kGuPre][kGuRows];
+  uint32_t sb[kGuPre][kGuRows];
+};
+__device__ __forceinline__ void gu_load(GuBatch& B, const SlotW& sw, const int* row, int wpr,
+                                        int gpr, int c0, int CH) {
+#pragma unroll
+  for (int u = 0; u < kGuPre; ++u) {
+    const int c = c0 + 32 * u;
+    if (c < CH) {
+#pragma unroll
+      for (int r = 0; r < kGuRows; ++r) {
+        const size_t rw = (size_t)row[r];
+        B.q[u][r] = __ldg(reinterpret_cast<const uint4*>(sw.q + rw * wpr) + c);
+        B.sb[u][r] = (uint32_t)__ldg(sw.s + rw * gpr + (c >> 1)) |
+                     ((uint32_t)__ldg(sw.b + rw * gpr + (c >> 1)) << 16);
+      }
+    }
+  }
+}
+
+// Down loads of one warp: its slot's rows n0 + r, r = s*RPS + lane/CR
+// (steps s < kDownRows/RPS, RPS = 32/CR rows per step), chunk c = lane mod
+// CR of each row; sb = scale (low half) | bias (high half).
+struct DownBatch {
+  uint4 q[kDownRows];
+  uint32_t sb[kDownRows];
+};
+__device__ __forceinline__ void down_load(DownBatch& B, const SlotW& sw, int n0, int lane, int CR,
+                                          int I) {
+  const int wpr = I >> 3, gpr = I >> 6, rps = 32 / CR, c = lane % CR;
+#pragma unroll
+  for (int st = 0; st < kDownRows; ++st) {
+    const int r = st * rps + lane / CR;
+    if (st * rps < kDownRows) {
+      const size_t rw = (size_t)(n0 + r);
+      B.q[st] = __ldg(reinterpret_cast<const uint4*>(sw.q + rw * wpr) + c);
+      B.sb[st] = (uint32_t)__ldg(sw.s + rw * gpr + (c >> 1)) |
+                 ((uint32_t)__ldg(sw.b + rw * gpr + (c >> 1)) << 16);
+    }
+  }
+}
+
+}  // namespace
+
+// Dependencies between the three kernels of a layer (all launched with
+// programmatic stream serialisation, see pdl_wait / pdl_trigger):
+//   dec_route   prefetches its router weights to L2, waits (for the
+//               previous layer, or whatever precedes the call), clears the
+//               routing-published flag, triggers, writes logits
+//   dec_gate_up starts once every router block has passed its wait, so all
+//               work before the call is complete: the shared expert's
+//               weights load before its wait. After it, each block selects
+//               the top-K; block 0 writes ids / w and sets the flag
+//               (release); every block then triggers
+//   dec_down    starts once every gate_up block has triggered; it acquires
+//               the flag, reads ids / w and loads its weights before its
+//               wait, and h (from dec_gate_up) after it; it triggers at
+//               once (the next router only prefetches before its wait)
+// Data written by an earlier kernel of the chain is read through L2
+// (ld.global.cg); only the weights use the non-coherent path.
+
+// ---------------------------------------------------------------- router --
+// One warp per (token, expert); logit order as in route_logits_kernel.
+__global__ void __launch_bounds__(128) dec_route_kernel(DecodeArgs a) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, E = a.E, H = a.H;
+  const bool valid = gw < T * E;
+  const int t = valid ? gw / E : 0, e = valid ? gw - t * E : 0;
+  if (valid && lane == 0) bulk_prefetch_l2(a.wr + (size_t)e * H, (uint32_t)H * 2);
+  pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl->routed = 0u;
+  pdl_trigger();
+  if (!valid) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  const uint4* wq = reinterpret_cast<const uint4*>(a.wr + (size_t)e * H);
+  float acc = 0.0f;  // partial `lane`: elements 8*(32j+lane)+i, j then i ascending
+#pragma unroll 8
+  for (int j = 0; j < (H >> 8); ++j) {
+    const uint4 xv = __ldcg(xr + 32 * j + lane), wv = __ldg(wq + 32 * j + lane);
+    acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
+    acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
+    acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
+    acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
+    acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
+    acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
+    acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
+    acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, d));
+  if (lane == 0) a.logits[(size_t)t * E + e] = a.bias ? __fadd_rn(acc, a.bias[e]) : acc;
+}
+
+// --------------------------------------------------------------- gate_up --
+// Warp gw -> slot (t, k) = gw / (I/kGuPairs), gate rows j..j+kGuPairs-1 and
+// the matching up rows I+j.. with j = kGuPairs * (gw mod I/kGuPairs).
+// Dynamic smem: the T activation rows.
+__global__ void __launch_bounds__(kTopkThreads) dec_gate_up_kernel(DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t xs[];
+  __shared__ TopkSmem S;
+  const int T = a.T, H = a.H, I = a.I, K = a.K, slots = K + a.ns;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kGuWarps + (threadIdx.x >> 5);
+  const int groups = I / kGuPairs;
+  const bool valid = gw < T * slots * groups;
+  const int sl = valid ? gw / groups : 0, j = valid ? kGuPairs * (gw - sl * groups) : 0;
+  const int t = sl / slots, k = sl - t * slots;
+  const int wpr = H >> 3, gpr = H >> 6, CH = H >> 5;  // words, groups, chunks per row
+  int row[kGuRows];
+#pragma unroll
+  for (int r = 0; r < kGuPairs; ++r) {
+    row[r] = j + r;
+    row[kGuPairs + r] = I + j + r;
+  }
+  GuBatch B;
+  SlotW sw = slot_weights(a, true, K, 0, 2 * I, wpr, gpr);  // the shared expert (k == K)
+  // the shared expert needs no routing: its weights load before the wait
+  if (valid && k == K) gu_load(B, sw, row, wpr, gpr, lane, CH);
+  pdl_wait();
+  topk_block(a.logits, T, a.E, K, S);  // ends with __syncthreads()
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
+      a.ids[i] = S.ids[i / K][i % K];
+      a.w[i] = S.w[i / K][i % K];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(&a.ctrl->routed, 1u);  // covers the block's writes
+  }
+  pdl_trigger();
+  int e = 0;
+  if (valid && k < K) {
+    e = S.ids[t][k];
+    sw = slot_weights(a, true, k, e, 2 * I, wpr, gpr);
+    if (sw.ok) gu_load(B, sw, row, wpr, gpr, lane, CH);
+  }
+  // the activations stream into shared memory behind the weight loads
+  for (int tt = 0; tt < T; ++tt) act_stage(a.x + (size_t)tt * H, xs + (size_t)tt * H * 2, H);
+  __syncthreads();
+  if (!valid) return;
+  if (!sw.ok) {
+    if (lane == 0) {
+      set_error(a.ctrl, MOE_ERR_BAD_INPUT, KID_DECODE, e);
+      for (int r = 0; r < kGuPairs; ++r) a.h[(size_t)sl * I + j + r] = 0;
+    }
+    return;
+  }
+  const uint8_t* xt = xs + (size_t)t * H * 2;
+  float acc[kGuRows];
+#pragma unroll
+  for (int r = 0; r < kGuRows; ++r) acc[r] = 0.0f;
+  for (int c0 = lane;;) {
+#pragma unroll
+    for (int u = 0; u < kGuPre; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < CH) {
+        uint4 xv[4];
+        act_load_chunk(xt, c, xv);
+#pragma unroll
+        for (int r = 0; r < kGuRows; ++r) {
+          const uint32_t sb = B.sb[u][r];
+          acc[r] = dot32(B.q[u][r], __byte_perm(sb, 0, 0x1010), __byte_perm(sb, 0, 0x3232), xv,
+                         acc[r]);
+        }
+      }
+    }
+    c0 += 32 * kGuPre;
+    if (c0 >= CH) break;
+    gu_load(B, sw, row, wpr, gpr, c0, CH);
+  }
+#pragma unroll
+  for (int r = 0; r < kGuRows; ++r) acc[r] = warp_sum(acc[r]);
+  if (lane == 0) {
+    uint16_t hv[kGuPairs];
+#pragma unroll
+    for (int r = 0; r < kGuPairs; ++r) {
+      const float g = acc[r], u = acc[kGuPairs + r];
+      hv[r] = (uint16_t)f2bf(g / (1.0f + expf(-g)) * u);
+    }
+    uint2 o;
+    o.x = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
+    o.y = (uint32_t)hv[2] | ((uint32_t)hv[3] << 16);
+    *reinterpret_cast<uint2*>(a.h + (size_t)sl * I + j) = o;
+  }
+}
+
+// ------------------------------------------------------ down + combine --
+// Block (bx, t): output columns n0 = kDownRows*bx .. n0+kDownRows-1 of token
+// t. Warp w takes slots k = w, w + nwarps, ..: lane `lane` holds chunk
+// c = lane mod CR (CR = I/32 chunks per row) of the slot's h in registers
+// and multiplies it with chunk c of the rows it is given (32/CR rows per
+// step); the lanes of a row are summed by shuffles, the slots in order
+// through shared memory.
+__global__ void __launch_bounds__(kDownMaxWarps * 32) dec_down_kernel(DecodeArgs a) {
+  __shared__ int sid[32];
+  __shared__ float swt[32];
+  __shared__ float dsl[33][kDownRows];  // slot results of the block's columns
+  __shared__ float red[kDownMaxWarps + 1];
+  __shared__ int flag_ok, last;
+  pdl_trigger();
+  const int H = a.H, I = a.I, K = a.K, slots = a.K + a.ns;
+  const int t = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int n0 = blockIdx.x * kDownRows;
+  const int CR = I >> 5, rps = 32 / CR, c = lane % CR;
+  // routing published by dec_gate_up (release / acquire): the selected
+  // down weights stream in before the wait
+  if (threadIdx.x == 0) {
+    bool ok = ld_acquire(&a.ctrl->routed) == 1u;
+    if (!ok) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!(ok = ld_acquire(&a.ctrl->routed) == 1u) && globaltimer_ns() - t0 < 20000000ull) {
+      }
+    }
+    flag_ok = ok;
+  }
+  __syncthreads();
+  const bool early = flag_ok != 0;
+  if (early && threadIdx.x < K) {
+    sid[threadIdx.x] = __ldcg(a.ids + t * K + threadIdx.x);
+    swt[threadIdx.x] = __ldcg(a.w + t * K + threadIdx.x);
+  }
+  __syncthreads();
+  DownBatch B;
+  SlotW sw = slot_weights(a, false, warp, warp < K && early ? sid[warp] : 0, H, I >> 3, I >> 6);
+  if (early && warp < slots && sw.ok) down_load(B, sw, n0, lane, CR, I);
+  pdl_wait();
+  if (!early) {  // the flag did not show within the bound: read after the wait
+    if (threadIdx.x < K) {
+      sid[threadIdx.x] = __ldcg(a.ids + t * K + threadIdx.x);
+      swt[threadIdx.x] = __ldcg(a.w + t * K + threadIdx.x);
+    }
+    __syncthreads();
+    sw = slot_weights(a, false, warp, warp < K ? sid[warp] : 0, H, I >> 3, I >> 6);
+    if (warp < slots && sw.ok) down_load(B, sw, n0, lane, CR, I);
+  }
+  for (int k = warp; k < slots; k += nwarps) {
+    if (k != warp) {
+      sw = slot_weights(a, false, k, k < K ? sid[k] : 0, H, I >> 3, I >> 6);
+      if (sw.ok) down_load(B, sw, n0, lane, CR, I);
+    }
+    uint4 hv[4];
+    const uint4* hr = reinterpret_cast<const uint4*>(a.h + ((size_t)t * slots + k) * I) + 4 * c;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) hv[v] = __ldcg(hr + v);
+    float part[kDownRows];
+#pragma unroll
+    for (int st = 0; st < kDownRows; ++st) {
+      part[st] = 0.0f;
+      if (st * rps < kDownRows && sw.ok)
+        part[st] = dot32(B.q[st], __byte_perm(B.sb[st], 0, 0x1010),
+                         __byte_perm(B.sb[st], 0, 0x3232), hv, 0.0f);
+    }
+    // sum the CR lanes of each row (lanes of a row are consecutive)
+#pragma unroll
+    for (int st = 0; st < kDownRows; ++st) {
+      if (st * rps < kDownRows) {
+        for (int d = CR >> 1; d >= 1; d >>= 1) part[st] += __shfl_xor_sync(0xFFFFFFFFu, part[st], d);
+        if (c == 0) dsl[k][st * rps + lane / CR] = part[st];
+      }
+    }
+    if (!sw.ok && lane == 0) set_error(a.ctrl, MOE_ERR_BAD_INPUT, KID_DECODE, sid[k]);
+  }
+  __syncthreads();
+  // y = sum_k w_k d_k (slot order) + d_shared, one thread per column
+  float ysq = 0.0f;
+  if (threadIdx.x < kDownRows) {
+    const int r = threadIdx.x;
+    float acc = 0.0f;
+    for (int k = 0; k < K; ++k) acc = __fmaf_rn(swt[k], dsl[k][r], acc);
+    if (a.ns) acc += dsl[K][r];
+    const uint32_t yb = f2bf(acc);
+    a.y[(size_t)t * H + n0 + r] = (uint16_t)yb;
+    const float yr = __uint_as_float(yb << 16);
+    ysq = yr * yr;
+  }
+  if (!a.x_next) return;
+  // unit-RMS normalisation of the bf16 y: block partials of y^2, then the
+  // last block sums them in block order and writes every token's x_next
+  if (warp == 0) {
+    ysq = warp_sum(ysq);
+    __syncwarp();  // orders lanes 0..kDownRows-1's y stores before lane 0's release
+    if (lane == 0) {
+      a.part[(size_t)t * gridDim.x + blockIdx.x] = ysq;
+      // release: this block's y and partial (lanes 0..kDownRows-1 of this
+      // warp wrote them); acquire: every other block's, for the last one
+      last = atom_add_acq_rel(&a.ctrl->ticket2, 1u) == gridDim.x * gridDim.y - 1;
+    }
+  }
+  __syncthreads();
+  if (!last) return;
+  const int nb = gridDim.x, nth = blockDim.x;
+  for (int tt = 0; tt < a.T; ++tt) {
+    // every load of the token first (one round trip), then the sums
+    float pp[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = threadIdx.x + u * nth;
+      pp[u] = i < nb ? __ldcg(a.part + (size_t)tt * nb + i) : 0.0f;
+    }
+    const uint32_t* yr = reinterpret_cast<const uint32_t*>(a.y + (size_t)tt * H);
+    uint32_t* xr = reinterpret_cast<uint32_t*>(a.x_next + (size_t)tt * H);
+    uint32_t yv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = threadIdx.x + u * nth;
+      yv[u] = i < (H >> 1) ? __ldcg(yr + i) : 0u;
+    }
+    float ss = 0.0f;
+    for (int i = threadIdx.x + 4 * nth; i < nb; i += nth) ss += __ldcg(a.part + (size_t)tt * nb + i);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ss += pp[u];
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float tot = 0.0f;
+      for (int i = 0; i < nwarps; ++i) tot += red[i];
+      red[kDownMaxWarps] = tot;
+    }
+    __syncthreads();
+    const float inv = 1.0f / sqrtf(red[kDownMaxWarps] / (float)H + 1e-6f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = threadIdx.x + u * nth;
+      if (i < (H >> 1)) xr[i] = pack_bf2(bf_lo(yv[u]) * inv, bf_hi(yv[u]) * inv);
+    }
+    for (int i = threadIdx.x + 8 * nth; i < (H >> 1); i += nth) {
+      const uint32_t v = __ldcg(yr + i);
+      xr[i] = pack_bf2(bf_lo(v) * inv, bf_hi(v) * inv);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.ctrl->ticket2 = 0u;
+}
+
+bool decode_supported(int T, int H, int E, int K, int I, int ns) {
+  // I/32 chunks per down row must divide the 32 lanes (I = 128..1024, power of two)
+  const bool i_ok = I >= 128 && I <= 1024 && (I & (I - 1)) == 0;
+  return T >= 1 && T <= kDecodeMaxT && T <= kTopkMaxT && ((E + 31) / 32) * K <= kTopkMaxCand &&
+         (size_t)T * H * 2 + sizeof(TopkSmem) <= 48 * 1024 && i_ok && K + ns <= 33;
+}
+
+size_t decode_part_floats(int T, int H) { return (size_t)T * ((H + kDownRows - 1) / kDownRows); }
+
+namespace {
+// Launch with programmatic stream serialisation (the kernel may start while
+// its predecessor in the stream is still running; it waits in pdl_wait).
+cudaError_t launch_pdl(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, const DecodeArgs& a) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+}  // namespace
+
+cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
+  const int T = a.T, slots = a.K + a.ns;
+  cudaError_t err = launch_pdl(dec_route_kernel, dim3((T * a.E + 3) / 4), dim3(128), 0, stream, a);
+  if (err != cudaSuccess) return err;
+  const int warps = T * slots * (a.I / kGuPairs);
+  err = launch_pdl(dec_gate_up_kernel, dim3((warps + kGuWarps - 1) / kGuWarps),
+                   dim3(kTopkThreads), (size_t)T * a.H * 2, stream, a);
+  if (err != cudaSuccess) return err;
+  const int nw = slots < kDownMaxWarps ? slots : kDownMaxWarps;
+  return launch_pdl(dec_down_kernel, dim3(a.H / kDownRows, T), dim3(nw * 32), 0, stream, a);
+}
+
+}  // namespace moe

@@ -36,6 +36,29 @@ struct FfnArgs {
   int shared_blocks;           // block-map entries of the shared expert (the last ones)
 };
 
+// Arguments of the fused decode layer (decode.cu): every pointer device,
+// ids / w / logits / h / part in the workspace or the caller's buffers.
+constexpr int kDecodeMaxT = 4;  // moe_layer_w4 takes the decode kernels up to this T
+struct DecodeArgs {
+  const uint16_t* x;    // bf16 [T][H]
+  const uint16_t* wr;   // bf16 [E][H]
+  const float* bias;    // [E] or null
+  int T, H, E, K, I, ns;
+  moe_w4_weights_t ex;  // routed experts
+  moe_w4_weights_t sh;  // shared expert (used when ns == 1)
+  float* logits;        // [T][E]
+  int32_t* ids;         // [T][K]
+  float* w;             // [T][K]
+  uint16_t* h;          // bf16 [T][K+ns][I]
+  uint16_t* y;          // bf16 [T][H]
+  uint16_t* x_next;     // bf16 [T][H] or null
+  float* part;          // [decode_part_floats(T, H)]
+  Ctrl* ctrl;
+};
+bool decode_supported(int T, int H, int E, int K, int I, int ns);
+size_t decode_part_floats(int T, int H);
+cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
+
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
                          int E, int K, float* logits, int32_t* ids, float* w,
                          cudaStream_t stream);

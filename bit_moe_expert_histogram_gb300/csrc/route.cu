@@ -11,6 +11,7 @@
 // the natural coalesced warp order: lane L reads 16-byte chunk 32j+L.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -87,65 +88,13 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t* __res
   }
 }
 
-// (value, id) a beats b: larger value, or equal value and lower id.
-__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
-  return (ib < 0) || (va > vb) || (va == vb && ia < ib);
-}
-
-// One warp per token: K rounds of a warp-wide arg-max over the E logits
-// (lane l owns experts l, l+32, ...), ties to the lower id; then the
-// softmax over the K selected logits, renormalised.
+// One warp per token: top-K and renormalised softmax weights (topk.cuh).
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int K, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  const float* l = logits + (size_t)t * E;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? l[e] : 0.0f;
-  }
-  uint32_t taken = 0;
-  float my_l = 0.0f;
-  int my_id = 0;
-  for (int k = 0; k < K; ++k) {
-    float bv = 0.0f;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && beats(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, d);
-      if (oi >= 0 && beats(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == k) {
-      my_l = bv;
-      my_id = bi;
-    }
-  }
-  const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-  const float ex = (lane < K) ? expf(my_l - l0) : 0.0f;
-  float z = ex;
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
-  if (lane < K) {
-    ids[(size_t)t * K + lane] = my_id;
-    w[(size_t)t * K + lane] = ex / z;
-  }
+  topk_warp(logits + (size_t)t * E, E, K, threadIdx.x & 31, ids + (size_t)t * K, w + (size_t)t * K);
 }
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,

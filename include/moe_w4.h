@@ -183,6 +183,17 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
                           int32_t* topk_ids_dev, float* topk_w_dev, void* ws_dev,
                           size_t ws_bytes, moe_stream_t stream);
 
+/* Which kernels moe_layer_w4 runs for `shape`: 1 = the fused decode
+ * kernels, 0 = the four calls above (route, plan, grouped GEMMs, combine),
+ * -1 = unsupported shape. The decode kernels take T <= 4 with I one of 128,
+ * 256, 512, 1024, ceil(E/32)*K <= 512, K + n_shared <= 33 and
+ * T*H*2 + 17936 <= 49152 (the activations and the top-K scratch in one
+ * block's shared memory). Host only; enqueues nothing. The decode kernels
+ * are launched with programmatic stream serialisation: a layer may start
+ * while the work before it in the stream finishes, but it reads nothing
+ * that work writes before that work has completed. */
+int32_t moe_layer_path(const moe_shape_t* shape);
+
 /* moe_plan without a workspace: same inputs, same outputs, bit-identical
  * results. The pages have no counterpart; this entry point exists for
  * callers that cannot allocate device memory where they build the plan (code

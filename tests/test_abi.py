@@ -51,6 +51,20 @@ def test_workspace_and_block_bounds(lib):
     assert m.moe_max_blocks(s1) == 1 + 8 + 1
 
 
+def test_layer_path_choice(lib):
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 512, 1, 128)) == 1
+    assert m.moe_layer_path(m.make_shape(4, 2048, 256, 8, 512, 1, 128)) == 1
+    assert m.moe_layer_path(m.make_shape(5, 2048, 256, 8, 512, 1, 128)) == 0
+    assert m.moe_layer_path(m.make_shape(512, 2048, 256, 8, 512, 1, 128)) == 0
+    assert m.moe_layer_path(m.make_shape(1, 8192, 256, 8, 512, 1, 128)) == 1
+    assert m.moe_layer_path(m.make_shape(4, 8192, 256, 8, 512, 1, 128)) == 0   # 64 KiB of x
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 384, 1, 128)) == 0   # I not 2^n
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 2048, 1, 128)) == 0  # I > 1024
+    assert m.moe_layer_path(m.make_shape(1, 2048, 1024, 32, 512, 1, 128)) == 0  # 1024 candidates
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 32, 1024, 1, 128)) == 1  # 33 slots
+    assert m.moe_layer_path(m.make_shape(0, 2048, 256, 8, 512, 1, 128)) == -1
+
+
 @pytest.mark.parametrize("bad", [dict(H=200), dict(H=128), dict(I=64), dict(K=0), dict(K=17, E=16),
                                  dict(E=2048), dict(n_shared=2), dict(tile_rows=0),
                                  dict(tile_rows=129), dict(T=0), dict(K=33, E=64)])
