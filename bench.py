@@ -21,6 +21,7 @@ HBM copy bandwidth; cpu_baseline = the CPU oracle on a bounded sample.
 --impl reference times the CPU oracle itself on the same workload.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -38,6 +39,25 @@ import synth  # noqa: E402
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
+
+
+def measured_traffic(workload):
+    """DRAM bytes per roofline unit from the committed ncu capture of this
+    workload (profiles/traffic.json), or None when there is none or the
+    kernel sources changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not entry:
+        return None
+    h = hashlib.sha256()
+    for name in entry["sources"]:
+        with open(os.path.join(ROOT, "bit_moe_expert_histogram_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return entry["dram_bytes"] if h.hexdigest()[:16] == entry["source_sha256_16"] else None
 
 
 def peaks():
@@ -503,7 +523,8 @@ def run_ours(args, wl):
     unit_gbs = unit_bytes / (ffn_ms / 1e3) / 1e9
     line["roofline"].update({"bound": "hbm", "achieved": round(unit_gbs, 1), "peak": hbm,
                              "peak_source": src, "unit": "GB/s",
-                             "frac": round(unit_gbs / hbm, 4), "traffic": None,
+                             "frac": round(unit_gbs / hbm, 4),
+                             "traffic": measured_traffic(wl.name if wl.layers == synth.CONFIGS[wl.name].layers else ""),
                              "ms_per_launch": round(ffn_ms, 5),
                              "algorithmic_bytes_per_launch": unit_bytes})
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -523,10 +544,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="stacked layers (default: the workload's); a smaller case for profilers")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     wl = synth.CONFIGS[args.workload]
+    if args.layers > 0:
+        wl = dataclasses.replace(wl, layers=args.layers)
     if args.impl == "reference":
         run_reference(args, wl)
     else:
