@@ -8,8 +8,8 @@
 // launches per layer:
 //   dec_route   fixed-order fp32 router logits, one warp per token x expert
 //               (the prefill router's order, so the ids are bit-identical)
-//   dec_gate_up every block selects the top-K itself from the logits (no
-//               serial tail); block 0 publishes ids / weights. Warps take 4
+//   dec_gate_up every block selects the top-K itself from the logits (one
+//               warp per token, no serial tail); block 0 publishes ids / w. Warps take 4
 //               gate rows and the matching 4 up rows of one slot; SwiGLU -> h
 //   dec_down    one block per 8 output columns of a token, one warp per
 //               slot: the slot's down rows times its h, then the slots
@@ -26,7 +26,9 @@ namespace moe {
 
 namespace {
 
-constexpr int kGuWarps = kTopkThreads / 32;  // gate_up: warps per block
+constexpr int kGuWarps = 8;                  // gate_up: warps per block
+constexpr int kDecCand = 256;                // top-K candidates per token (<= E)
+constexpr int kDecMaxE = 256;                // routed experts (8 logits per lane in the top-K)
 constexpr int kDownRows = 8;                 // down: output columns per block
 constexpr int kDownMaxWarps = 16;            // down: warps per block (slots beyond loop)
 constexpr int kGuPairs = 4;  // gate_up: gate rows (and as many up rows) per warp
@@ -109,14 +111,6 @@ __device__ __forceinline__ int act_piece_off(int c, int v) { return c * 64 + 16 
 __device__ __forceinline__ void act_load_chunk(const uint8_t* row, int c, uint4 xv[4]) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) xv[v] = *reinterpret_cast<const uint4*>(row + act_piece_off(c, v));
-}
-
-// Copies n bf16 (n % 32 == 0) written by an earlier kernel, read through L2,
-// into the layout above.
-__device__ __forceinline__ void act_stage(const uint16_t* __restrict__ src, uint8_t* dst, int n) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
-    *reinterpret_cast<uint4*>(dst + act_piece_off(i >> 2, i & 3)) = __ldcg(s + i);
 }
 
 struct SlotW {
@@ -206,6 +200,38 @@ __device__ __forceinline__ void down_load(DownBatch& B, const SlotW& sw, int n0,
   }
 }
 
+// L2 prefetch of the down weights of every slot: the packed rows in pieces
+// of kPrefetchBytes, spread over the grid's blocks, and the scale / bias
+// arrays (one piece each). Called by one thread per block.
+constexpr uint32_t kPrefetchBytes = 32768;
+__device__ __forceinline__ void prefetch_down_weights(const DecodeArgs& a,
+                                                      const int (*sid)[32]) {
+  const size_t qbytes = (size_t)a.H * (a.I / 8) * 4, sbytes = (size_t)a.H * (a.I / 64) * 2;
+  const int qpieces = (int)((qbytes + kPrefetchBytes - 1) / kPrefetchBytes);
+  const int per_region = qpieces + 2;
+  const int regions = a.T * a.K + a.ns;  // routed slots of every token, then the shared expert
+  for (int p = blockIdx.x; p < regions * per_region; p += gridDim.x) {
+    const int rg = p / per_region, piece = p - rg * per_region;
+    const moe_w4_weights_t* wt = &a.ex;
+    size_t e = 0;
+    if (rg < a.T * a.K) {
+      const int id = sid[rg / a.K][rg % a.K];
+      if (id < 0 || id >= a.E) continue;
+      e = (size_t)id;
+    } else {
+      wt = &a.sh;
+    }
+    if (piece < qpieces) {
+      const size_t off = (size_t)piece * kPrefetchBytes;
+      const uint32_t n = (uint32_t)min((size_t)kPrefetchBytes, qbytes - off);
+      bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(wt->q_down_dev) + e * qbytes + off, n);
+    } else {
+      const uint16_t* base = piece == qpieces ? wt->s_down_dev : wt->b_down_dev;
+      bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(base) + e * sbytes, (uint32_t)sbytes);
+    }
+  }
+}
+
 }  // namespace
 
 // Dependencies between the three kernels of a layer (all launched with
@@ -261,9 +287,11 @@ __global__ void __launch_bounds__(128) dec_route_kernel(DecodeArgs a) {
 // Warp gw -> slot (t, k) = gw / (I/kGuPairs), gate rows j..j+kGuPairs-1 and
 // the matching up rows I+j.. with j = kGuPairs * (gw mod I/kGuPairs).
 // Dynamic smem: the T activation rows.
-__global__ void __launch_bounds__(kTopkThreads) dec_gate_up_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(kGuWarps * 32) dec_gate_up_kernel(DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t xs[];
-  __shared__ TopkSmem S;
+  __shared__ TopkWarpSmem<kDecCand> TS[kDecodeMaxT];
+  __shared__ int sid[kDecodeMaxT][32];
+  __shared__ float swt[kDecodeMaxT][32];
   const int T = a.T, H = a.H, I = a.I, K = a.K, slots = K + a.ns;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kGuWarps + (threadIdx.x >> 5);
@@ -283,24 +311,53 @@ __global__ void __launch_bounds__(kTopkThreads) dec_gate_up_kernel(DecodeArgs a)
   // the shared expert needs no routing: its weights load before the wait
   if (valid && k == K) gu_load(B, sw, row, wpr, gpr, lane, CH);
   pdl_wait();
-  topk_block(a.logits, T, a.E, K, S);  // ends with __syncthreads()
+  // the activations are fetched now and stored to shared memory after the
+  // top-K, so their L2 latency hides behind it
+  uint4 xreg[kDecodeMaxT * 2048 / 8 / (kGuWarps * 32)];
+  const int xn = T * H / 8;  // 16-byte pieces of all T rows
+#pragma unroll
+  for (int u = 0; u < (int)(sizeof(xreg) / sizeof(uint4)); ++u) {
+    const int i = threadIdx.x + u * kGuWarps * 32;
+    if (i < xn) xreg[u] = __ldcg(reinterpret_cast<const uint4*>(a.x) + i);
+  }
+  // every block selects the experts itself: warp t takes token t
+  const int warp = threadIdx.x >> 5;
+  if (warp < T)
+    topk_warp<kDecCand, kDecMaxE / 32>(a.logits + (size_t)warp * a.E, a.E, K, lane, TS[warp],
+                                       sid[warp], swt[warp]);
+  __syncthreads();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
-      a.ids[i] = S.ids[i / K][i % K];
-      a.w[i] = S.w[i / K][i % K];
+      a.ids[i] = sid[i / K][i % K];
+      a.w[i] = swt[i / K][i % K];
     }
     __syncthreads();
     if (threadIdx.x == 0) st_release(&a.ctrl->routed, 1u);  // covers the block's writes
   }
   pdl_trigger();
+  // the selected experts' down weights go to L2 now, so that dec_down (which
+  // cannot share an SM with this kernel) finds them there
+  if (threadIdx.x == 0) prefetch_down_weights(a, sid);
   int e = 0;
   if (valid && k < K) {
-    e = S.ids[t][k];
+    e = sid[t][k];
     sw = slot_weights(a, true, k, e, 2 * I, wpr, gpr);
     if (sw.ok) gu_load(B, sw, row, wpr, gpr, lane, CH);
   }
-  // the activations stream into shared memory behind the weight loads
-  for (int tt = 0; tt < T; ++tt) act_stage(a.x + (size_t)tt * H, xs + (size_t)tt * H * 2, H);
+#pragma unroll
+  for (int u = 0; u < (int)(sizeof(xreg) / sizeof(uint4)); ++u) {
+    const int i = threadIdx.x + u * kGuWarps * 32;
+    if (i < xn) {
+      const int tt = i / (H / 8), ii = i - tt * (H / 8);
+      *reinterpret_cast<uint4*>(xs + (size_t)tt * H * 2 + act_piece_off(ii >> 2, ii & 3)) = xreg[u];
+    }
+  }
+  for (int i = threadIdx.x + (int)(sizeof(xreg) / sizeof(uint4)) * kGuWarps * 32; i < xn;
+       i += kGuWarps * 32) {  // rows beyond the register budget (T*H > 8192)
+    const int tt = i / (H / 8), ii = i - tt * (H / 8);
+    *reinterpret_cast<uint4*>(xs + (size_t)tt * H * 2 + act_piece_off(ii >> 2, ii & 3)) =
+        __ldcg(reinterpret_cast<const uint4*>(a.x) + i);
+  }
   __syncthreads();
   if (!valid) return;
   if (!sw.ok) {
@@ -356,7 +413,9 @@ __global__ void __launch_bounds__(kTopkThreads) dec_gate_up_kernel(DecodeArgs a)
 // and multiplies it with chunk c of the rows it is given (32/CR rows per
 // step); the lanes of a row are summed by shuffles, the slots in order
 // through shared memory.
-__global__ void __launch_bounds__(kDownMaxWarps * 32) dec_down_kernel(DecodeArgs a) {
+// 96 registers: two blocks of nine warps fit one SM's register file (16
+// warps of 110 registers would not).
+__global__ void __maxnreg__(96) dec_down_kernel(DecodeArgs a) {
   __shared__ int sid[32];
   __shared__ float swt[32];
   __shared__ float dsl[33][kDownRows];  // slot results of the block's columns
@@ -502,8 +561,9 @@ __global__ void __launch_bounds__(kDownMaxWarps * 32) dec_down_kernel(DecodeArgs
 bool decode_supported(int T, int H, int E, int K, int I, int ns) {
   // I/32 chunks per down row must divide the 32 lanes (I = 128..1024, power of two)
   const bool i_ok = I >= 128 && I <= 1024 && (I & (I - 1)) == 0;
-  return T >= 1 && T <= kDecodeMaxT && T <= kTopkMaxT && ((E + 31) / 32) * K <= kTopkMaxCand &&
-         (size_t)T * H * 2 + sizeof(TopkSmem) <= 48 * 1024 && i_ok && K + ns <= 33;
+  return T >= 1 && T <= kDecodeMaxT && E <= kDecMaxE &&
+         (size_t)T * H * 2 + kDecodeMaxT * (sizeof(TopkWarpSmem<kDecCand>) + 256) <= 48 * 1024 &&
+         i_ok && K + ns <= 33;
 }
 
 size_t decode_part_floats(int T, int H) { return (size_t)T * ((H + kDownRows - 1) / kDownRows); }
@@ -533,7 +593,7 @@ cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const int warps = T * slots * (a.I / kGuPairs);
   err = launch_pdl(dec_gate_up_kernel, dim3((warps + kGuWarps - 1) / kGuWarps),
-                   dim3(kTopkThreads), (size_t)T * a.H * 2, stream, a);
+                   dim3(kGuWarps * 32), (size_t)T * a.H * 2, stream, a);
   if (err != cudaSuccess) return err;
   const int nw = slots < kDownMaxWarps ? slots : kDownMaxWarps;
   return launch_pdl(dec_down_kernel, dim3(a.H / kDownRows, T), dim3(nw * 32), 0, stream, a);

@@ -89,12 +89,16 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t* __res
 }
 
 // One warp per token: top-K and renormalised softmax weights (topk.cuh).
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int K, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w) {
+constexpr int kTopkWarps = 4;
+__global__ void __launch_bounds__(kTopkWarps * 32) route_topk_kernel(const float* __restrict__ logits,
+                                                                    int T, int E, int K,
+                                                                    int32_t* __restrict__ ids,
+                                                                    float* __restrict__ w) {
+  __shared__ TopkWarpSmem<1024> S[kTopkWarps];
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
-  topk_warp(logits + (size_t)t * E, E, K, threadIdx.x & 31, ids + (size_t)t * K, w + (size_t)t * K);
+  topk_warp<1024, 32>(logits + (size_t)t * E, E, K, threadIdx.x & 31, S[threadIdx.x >> 5],
+            ids + (size_t)t * K, w + (size_t)t * K);
 }
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
@@ -109,7 +113,8 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bia
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  route_topk_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, T, E, K, ids, w);
+  route_topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(
+      logits, T, E, K, ids, w);
   return cudaGetLastError();
 }
 

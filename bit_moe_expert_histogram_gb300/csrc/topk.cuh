@@ -20,134 +20,83 @@ __device__ __forceinline__ float topk_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Called by all 32 lanes; l = the token's E logits (E <= 1024, K <= 32).
-// Lane L holds experts L + 32i. Each pick takes the warp maximum of the
-// lanes' best untaken keys, then the lowest id among the lanes holding it;
-// only the lane that owned the pick rescans its own keys.
+// Composite key: the logit key, then the lower id first. Unique per expert;
+// 0 is below every expert's key.
+__device__ __forceinline__ unsigned long long topk_ckey(float v, int e) {
+  return ((unsigned long long)topk_key(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+}
+
+// Per-warp scratch of topk_warp in shared memory, for at most CAP
+// candidates (CAP >= E).
+template <int CAP>
+struct TopkWarpSmem {
+  unsigned long long cand[CAP];
+  unsigned long long sel[32];
+};
+
+// Called by all 32 lanes of a warp; l = the token's E logits, read through
+// L2 (E <= 32 * NMAX, K <= 32, E <= CAP). Lane L holds experts L + 32i.
+// theta = the K-th largest of the lanes' largest logit keys: at least K
+// experts have a key >= theta, so every member of the top K does (any
+// other would be beaten by K of them). Those candidates are ranked by the
+// composite key; a candidate's rank is its slot. With fewer than K lanes
+// holding experts, every expert is a candidate. Writes ids[0..K), w[0..K).
+template <int CAP, int NMAX>
 __device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int K, int lane,
-                                          int32_t* __restrict__ ids, float* __restrict__ w) {
+                                          TopkWarpSmem<CAP>& S, int32_t* ids, float* w) {
   const int n = (E + 31) >> 5;
-  uint32_t key[32];
+  unsigned long long c[NMAX];
+  uint32_t kmax = 0u;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NMAX; ++i) {
     const int e = lane + 32 * i;
-    key[i] = (i < n && e < E) ? topk_key(__ldcg(l + e)) : 0u;
+    c[i] = (i < n && e < E) ? topk_ckey(__ldcg(l + e), e) : 0ull;
+    kmax = max(kmax, (uint32_t)(c[i] >> 32));
   }
-  uint32_t taken = 0, bk = 0, bi = 0xFFFFFFFFu;
-  // the lane's best untaken key; ties go to the lowest i (the lowest id)
-  auto rescan = [&]() {
-    bk = 0;
-    bi = 0xFFFFFFFFu;
+  int r = 0;  // lanes whose largest key is larger than this lane's
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (i >= n) break;
-      if (!((taken >> i) & 1u) && key[i] > bk) {
-        bk = key[i];
-        bi = (uint32_t)(lane + 32 * i);
-      }
-    }
-  };
-  rescan();
-  float my_l = 0.0f;
-  int my_id = 0;
-  for (int k = 0; k < K; ++k) {
-    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == m ? bi : 0xFFFFFFFFu);
-    if (lane == k) {
-      my_l = topk_value(m);
-      my_id = (int)win;
-    }
-    if ((int)(win & 31u) == lane) {
-      taken |= 1u << (win >> 5);
-      rescan();
-    }
+  for (int j = 0; j < 32; ++j) r += __shfl_sync(0xFFFFFFFFu, kmax, j) > kmax;
+  const int holders = __popc(__ballot_sync(0xFFFFFFFFu, kmax != 0u));
+  uint32_t theta = __reduce_min_sync(0xFFFFFFFFu, (r < K && kmax != 0u) ? kmax : 0xFFFFFFFFu);
+  if (holders < K) theta = 1u;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i) cnt += (uint32_t)(c[i] >> 32) >= theta;
+  int pre = cnt;  // inclusive scan of the counts over the lanes
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
+    if (lane >= d) pre += v;
   }
+  const int total = __shfl_sync(0xFFFFFFFFu, pre, 31);
+  int pos = pre - cnt;
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i)
+    if ((uint32_t)(c[i] >> 32) >= theta) S.cand[pos++] = c[i];
+  __syncwarp();
+  for (int i = lane; i < total; i += 32) {
+    const unsigned long long ci = S.cand[i];
+    int rk = 0, j = 0;
+    for (; j + 8 <= total; j += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rk += S.cand[j + u] > ci;
+    }
+    for (; j < total; ++j) rk += S.cand[j] > ci;
+    if (rk < K) S.sel[rk] = ci;
+  }
+  __syncwarp();
+  const unsigned long long mine = lane < K ? S.sel[lane] : 0ull;
+  const float my_l = topk_value((uint32_t)(mine >> 32));
   const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
   const float ex = (lane < K) ? expf(my_l - l0) : 0.0f;
   float z = ex;
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
   if (lane < K) {
-    ids[lane] = my_id;
+    ids[lane] = (int)(0xFFFFFFFFu - (uint32_t)mine);
     w[lane] = ex / z;
   }
-}
-
-// Block-wide top-K of T tokens at once (T <= 4), for a block of kTopkThreads
-// threads. Same order and weights as topk_warp, bit for bit. Stage 1: each
-// warp takes 32-expert chunks of a token and counts, for every expert, the
-// chunk members that beat it; the chunk's top K (rank < K) become candidates
-// (every member of the token's top K is one). Stage 2: a candidate's rank
-// among the token's candidates is its slot. Stage 3: the softmax weights, in
-// topk_warp's arithmetic.
-constexpr int kTopkThreads = 256;
-constexpr int kTopkMaxT = 4;
-constexpr int kTopkMaxCand = 512;  // per token: ceil(E/32) * K candidates at most
-
-struct TopkSmem {
-  unsigned long long cand[kTopkMaxT][kTopkMaxCand];
-  int ncand[kTopkMaxT];
-  float lsel[kTopkMaxT][32];
-  int ids[kTopkMaxT][32];
-  float w[kTopkMaxT][32];
-};
-
-// composite key: order-preserving logit key, then the lower id first
-__device__ __forceinline__ unsigned long long topk_ckey(float v, int e) {
-  return ((unsigned long long)topk_key(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-}
-
-// l: logits [T][E] (read through L2). Results in S.ids / S.w [t][k].
-// Requires ceil(E/32) * K <= kTopkMaxCand. Ends with __syncthreads().
-__device__ __forceinline__ void topk_block(const float* __restrict__ l, int T, int E, int K,
-                                           TopkSmem& S) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = kTopkThreads / 32;
-  const int nch = (E + 31) >> 5;
-  if (threadIdx.x < kTopkMaxT) S.ncand[threadIdx.x] = 0;
-  __syncthreads();
-  for (int job = warp; job < T * nch; job += nw) {
-    const int t = job / nch, e = (job - t * nch) * 32 + lane;
-    const unsigned long long c = e < E ? topk_ckey(__ldcg(l + (size_t)t * E + e), e) : 0ull;
-    int r = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r += __shfl_sync(0xFFFFFFFFu, c, j) > c;
-    if (e < E && r < K) S.cand[t][atomicAdd(&S.ncand[t], 1)] = c;
-  }
-  __syncthreads();
-  // four threads per candidate (consecutive lanes), each comparing it with a
-  // quarter of the token's candidates; the quarters' counts are summed by
-  // shuffles. Every lane of a warp runs the same iterations.
-  for (int t = 0; t < T; ++t) {
-    const int n = S.ncand[t], q = (n + 3) >> 2;
-    const int work = ((4 * n + kTopkThreads - 1) / kTopkThreads) * kTopkThreads;
-    for (int idx = threadIdx.x; idx < work; idx += kTopkThreads) {
-      const int i = idx >> 2, part = idx & 3;
-      const unsigned long long c = i < n ? S.cand[t][i] : 0ull;
-      int r = 0;
-      const int j0 = part * q, j1 = min(n, j0 + q);
-      if (i < n) {
-#pragma unroll 4
-        for (int j = j0; j < j1; ++j) r += S.cand[t][j] > c;
-      }
-      r += __shfl_xor_sync(0xFFFFFFFFu, r, 1);
-      r += __shfl_xor_sync(0xFFFFFFFFu, r, 2);
-      if (i < n && part == 0 && r < K) {
-        S.ids[t][r] = (int)(0xFFFFFFFFu - (uint32_t)c);
-        S.lsel[t][r] = topk_value((uint32_t)(c >> 32));
-      }
-    }
-  }
-  __syncthreads();
-  if (warp < T) {
-    const float my_l = lane < K ? S.lsel[warp][lane] : 0.0f;
-    const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-    const float ex = (lane < K) ? expf(my_l - l0) : 0.0f;
-    float z = ex;
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
-    if (lane < K) S.w[warp][lane] = ex / z;
-  }
-  __syncthreads();
+  __syncwarp();
 }
 
 }  // namespace moe

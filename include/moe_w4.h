@@ -185,10 +185,10 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
 
 /* Which kernels moe_layer_w4 runs for `shape`: 1 = the fused decode
  * kernels, 0 = the four calls above (route, plan, grouped GEMMs, combine),
- * -1 = unsupported shape. The decode kernels take T <= 4 with I one of 128,
- * 256, 512, 1024, ceil(E/32)*K <= 512, K + n_shared <= 33 and
- * T*H*2 + 17936 <= 49152 (the activations and the top-K scratch in one
- * block's shared memory). Host only; enqueues nothing. The decode kernels
+ * -1 = unsupported shape. The decode kernels take T <= 4 with E <= 256,
+ * I one of 128, 256, 512, 1024, K + n_shared <= 33 and T*H*2 + 10240 <=
+ * 49152 (the activations and the top-K scratch in one block's shared
+ * memory). Host only; enqueues nothing. The decode kernels
  * are launched with programmatic stream serialisation: a layer may start
  * while the work before it in the stream finishes, but it reads nothing
  * that work writes before that work has completed. */

@@ -60,7 +60,8 @@ def test_layer_path_choice(lib):
     assert m.moe_layer_path(m.make_shape(4, 8192, 256, 8, 512, 1, 128)) == 0   # 64 KiB of x
     assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 384, 1, 128)) == 0   # I not 2^n
     assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 2048, 1, 128)) == 0  # I > 1024
-    assert m.moe_layer_path(m.make_shape(1, 2048, 1024, 32, 512, 1, 128)) == 0  # 1024 candidates
+    assert m.moe_layer_path(m.make_shape(1, 2048, 1024, 32, 512, 1, 128)) == 0  # E > 256
+    assert m.moe_layer_path(m.make_shape(1, 2048, 512, 8, 512, 1, 128)) == 0    # E > 256
     assert m.moe_layer_path(m.make_shape(1, 2048, 256, 32, 1024, 1, 128)) == 1  # 33 slots
     assert m.moe_layer_path(m.make_shape(0, 2048, 256, 8, 512, 1, 128)) == -1
 
