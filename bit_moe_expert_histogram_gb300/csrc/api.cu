@@ -297,7 +297,8 @@ moe_status_t moe_plan(const moe_shape_t* shape, const int32_t* topk_ids_dev,
   const Layout L = layout_of(shape);
   cudaError_t e = launch_plan(topk_ids_dev, shape->T, shape->K, shape->E, shape->n_shared,
                               shape->tile_rows, *plan, reinterpret_cast<int32_t*>(ws + L.hist),
-                              reinterpret_cast<Ctrl*>(ws + L.ctrl), (cudaStream_t)stream);
+                              reinterpret_cast<Ctrl*>(ws + L.ctrl), kPlanChunk,
+                              (cudaStream_t)stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_plan launch");
 }
 

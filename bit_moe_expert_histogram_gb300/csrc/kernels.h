@@ -10,7 +10,8 @@ namespace moe {
 
 struct Ctrl;
 
-constexpr int kPlanChunk = 2048;  // routed rows per plan block
+constexpr int kPlanChunk = 256;         // routed rows per plan block (workspace path)
+constexpr int kPlanChunkNoalloc = 2048; // routed rows per plan block (moe_plan_noalloc)
 
 // Arguments of one grouped W4A16 GEMM launch (gate_up or down).
 struct FfnArgs {
@@ -63,7 +64,8 @@ cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bia
                          int E, int K, float* logits, int32_t* ids, float* w,
                          cudaStream_t stream);
 cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, int BM,
-                        const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, cudaStream_t stream);
+                        const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, int chunk,
+                        cudaStream_t stream);
 cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
                                const CUtensorMap& tx, const FfnArgs& a, int grid,
                                cudaStream_t stream);

@@ -22,14 +22,14 @@ constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kMaxE = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* __restrict__ ids,
-                                                                 int R, int E,
+                                                                 int R, int E, int chunk,
                                                                  int32_t* __restrict__ hist,
                                                                  Ctrl* ctrl) {
   __shared__ int h[kMaxE];
   for (int e = threadIdx.x; e < E; e += kPlanThreads) h[e] = 0;
   __syncthreads();
-  const int f0 = blockIdx.x * kPlanChunk;
-  const int f1 = min(f0 + kPlanChunk, R);
+  const int f0 = blockIdx.x * chunk;
+  const int f1 = min(f0 + chunk, R);
   for (int f = f0 + threadIdx.x; f < f1; f += kPlanThreads) {
     const int e = ids[f];
     if (e < 0 || e >= E)
@@ -71,7 +71,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 
 __global__ void __launch_bounds__(kPlanThreads)
     plan_scatter_kernel(const int32_t* __restrict__ ids, int T, int K, int E, int n_shared,
-                        int BM, const int32_t* __restrict__ hist, int nchunks, moe_plan_t plan) {
+                        int BM, const int32_t* __restrict__ hist, int nchunks, int chunk,
+                        moe_plan_t plan) {
   __shared__ int base[kMaxE];                 // this block's next position per expert
   __shared__ int wcnt[kPlanWarps][kMaxE];     // per-round, per-warp counts -> prefixes
   __shared__ int warp_sums[32];
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     const int e = tid * EPT + i;
     int t = 0, p = 0;
     if (e < E) {
+#pragma unroll 8
       for (int c = 0; c < nchunks; ++c) {
         const int v = hist[(size_t)c * E + e];
         t += v;
@@ -144,8 +146,8 @@ __global__ void __launch_bounds__(kPlanThreads)
   for (int i = tid; i < kPlanWarps * E; i += kPlanThreads) wcnt[i / E][i % E] = 0;
   __syncthreads();
 
-  const int f0 = blockIdx.x * kPlanChunk;
-  const int f1 = min(f0 + kPlanChunk, R);
+  const int f0 = blockIdx.x * chunk;
+  const int f1 = min(f0 + chunk, R);
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int r0 = f0; r0 < f1; r0 += kPlanThreads) {
     const int f = r0 + tid;
@@ -192,14 +194,15 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, int BM,
-                        const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, cudaStream_t stream) {
+                        const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, int chunk,
+                        cudaStream_t stream) {
   const int R = T * K;
-  const int nchunks = (R + kPlanChunk - 1) / kPlanChunk;
-  plan_hist_kernel<<<nchunks, kPlanThreads, 0, stream>>>(ids, R, E, hist, ctrl);
+  const int nchunks = (R + chunk - 1) / chunk;
+  plan_hist_kernel<<<nchunks, kPlanThreads, 0, stream>>>(ids, R, E, chunk, hist, ctrl);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   plan_scatter_kernel<<<nchunks, kPlanThreads, 0, stream>>>(ids, T, K, E, n_shared, BM, hist,
-                                                           nchunks, plan);
+                                                           nchunks, chunk, plan);
   return cudaGetLastError();
 }
 

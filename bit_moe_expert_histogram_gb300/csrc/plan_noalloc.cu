@@ -42,7 +42,7 @@ extern "C" moe_status_t moe_plan_noalloc(const moe_shape_t* shape, const int32_t
       !plan->num_blocks_dev)
     return MOE_ERR_INVALID_ARG;
   const int64_t R = (int64_t)shape->T * shape->K;
-  const int64_t nchunks = (R + kPlanChunk - 1) / kPlanChunk;
+  const int64_t nchunks = (R + kPlanChunkNoalloc - 1) / kPlanChunkNoalloc;
   if (kCtrlInts + nchunks * shape->E > (int64_t)kScratchInts) {
     set_last_error("moe_plan_noalloc: ceil(T*K/2048)*E exceeds the 65472-entry static scratch");
     return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -79,7 +79,7 @@ extern "C" moe_status_t moe_plan_noalloc(const moe_shape_t* shape, const int32_t
     return MOE_ERR_CUDA;
   }
   e = launch_plan(topk_ids_dev, shape->T, shape->K, shape->E, shape->n_shared, shape->tile_rows,
-                  *plan, base + kCtrlInts, reinterpret_cast<Ctrl*>(base), st);
+                  *plan, base + kCtrlInts, reinterpret_cast<Ctrl*>(base), kPlanChunkNoalloc, st);
   if (e != cudaSuccess) {
     set_last_cuda_error(e, "moe_plan_noalloc launch");
     return MOE_ERR_CUDA;
