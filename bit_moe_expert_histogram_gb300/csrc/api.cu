@@ -49,7 +49,7 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 
 struct Layout {
   size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
-      total;
+      rpart, total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -76,6 +76,9 @@ Layout layout_of(const moe_shape_t* s) {
   L.nblk = take(4);
   L.yslots = take(S * (size_t)s->H * 2);
   L.part = take(decode_part_floats(s->T, s->H) * 4);
+  L.rpart = route_tc_supported(s->T, s->H, s->E, s->K)
+                ? take(route_tc_partial_floats(s->T, s->H, s->E) * 4)
+                : off;
   L.total = off;
   return L;
 }
@@ -279,6 +282,19 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x_dev, const void* 
   MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
   uint8_t* ws = static_cast<uint8_t*>(ws_dev);
   const Layout L = layout_of(shape);
+  if (route_tc_supported(shape->T, shape->H, shape->E, shape->K)) {
+    CUtensorMap tw, tx;
+    MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_router_dev, shape->H, shape->E, 64,
+                   128, CU_TENSOR_MAP_SWIZZLE_128B));
+    MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_dev, shape->H, shape->T, 64, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B));
+    cudaError_t e = launch_route_tc(
+        tw, tx, static_cast<const uint16_t*>(x_dev), static_cast<const uint16_t*>(w_router_dev),
+        router_bias_dev, shape->T, shape->H, shape->E, shape->K,
+        reinterpret_cast<float*>(ws + L.rpart), topk_ids_dev, topk_w_dev,
+        reinterpret_cast<Ctrl*>(ws + L.ctrl), (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
+  }
   cudaError_t e = launch_route(static_cast<const uint16_t*>(x_dev),
                                static_cast<const uint16_t*>(w_router_dev), router_bias_dev,
                                shape->T, shape->H, shape->E, shape->K,

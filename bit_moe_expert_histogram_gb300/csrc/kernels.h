@@ -60,6 +60,14 @@ bool decode_supported(int T, int H, int E, int K, int I, int ns);
 size_t decode_part_floats(int T, int H);
 cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
 
+// Tensor-core screened router (route_tc.cu), taken from this many tokens on.
+constexpr int kRouteTcMinT = 64;
+bool route_tc_supported(int T, int H, int E, int K);
+size_t route_tc_partial_floats(int T, int H, int E);
+cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const uint16_t* x,
+                            const uint16_t* wr, const float* bias, int T, int H, int E, int K,
+                            float* part, int32_t* ids, float* w, Ctrl* ctrl, cudaStream_t stream);
+
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
                          int E, int K, float* logits, int32_t* ids, float* w,
                          cudaStream_t stream);

@@ -86,6 +86,50 @@ def test_route_ties_lower_id():
     assert np.allclose(c.w.cpu().numpy(), 1.0 / TINY.K, atol=1e-7)
 
 
+def test_route_screen_all_ties():
+    """T >= 64 takes the tensor-core screen: equal router rows tie every
+    logit, so every expert is a candidate and ids are 0..K-1."""
+    L = layer(128, FULL, 0)
+    c = Case(L, 128, FULL)
+    row = d16(L.w_router[:1], c.dev)
+    c.wr.copy_(row.expand(FULL.E, -1))
+    m.moe_route(c.shape, c.x, c.wr, None, c.ids, c.w, c.ws)
+    assert m.moe_query_device_status(c.ws) == 0
+    assert (c.ids.cpu().numpy() == np.arange(FULL.K)).all()
+    assert np.allclose(c.w.cpu().numpy(), 1.0 / FULL.K, atol=1e-7)
+
+
+def test_route_screen_near_ties():
+    """Router rows that differ in one element by one bf16 step: logits closer
+    than the screen's margin, so the fixed-order logits decide, bit-exactly."""
+    L = layer(256, FULL, 0)
+    base = synth.bf16_bits_to_f32(L.w_router[:1]).astype(np.float64)
+    rng = np.random.default_rng(11)
+    wr = np.repeat(base, FULL.E, axis=0)
+    k0 = 5
+    wr[:, k0] = base[0, k0] * (1.0 + rng.integers(-4, 5, FULL.E) * 2.0 ** -7)
+    wbits = synth.bf16_bits(wr)
+    c = Case(L, 256, FULL)
+    c.wr.copy_(d16(wbits, c.dev))
+    m.moe_route(c.shape, c.x, c.wr, c.bias, c.ids, c.w, c.ws)
+    assert m.moe_query_device_status(c.ws) == 0
+    ids, _, w64 = oracle.topk(oracle.router_logits(L.x, wbits, L.router_bias), FULL.K)
+    assert np.array_equal(c.ids.cpu().numpy(), ids)
+    assert np.abs(c.w.cpu().numpy() - w64).max() <= 1e-6
+
+
+def test_route_screen_ragged_experts_and_tokens():
+    """E = 100 (a partial expert tile) and T = 200 (a partial token tile)."""
+    shape = synth.LayerShape(H=512, E=100, K=4, I=128, n_shared=1)
+    L = synth.gen_layer(200, shape, seed=9, zipf_s=1.1)
+    c = Case(L, 200, shape)
+    m.moe_route(c.shape, c.x, c.wr, c.bias, c.ids, c.w, c.ws)
+    assert m.moe_query_device_status(c.ws) == 0
+    ids, _, w64 = oracle.route(L, shape.K)
+    assert np.array_equal(c.ids.cpu().numpy(), ids)
+    assert np.abs(c.w.cpu().numpy() - w64).max() <= 1e-6
+
+
 # ------------------------------------------------------------------- plan --
 @pytest.mark.parametrize("T,shape,zipf,bm", [(16, TINY, 0.0, 128), (16, TINY, 0.0, 1),
                                              (512, FULL, 0.0, 128), (512, FULL, 0.0, 16),
