@@ -242,9 +242,38 @@ def run_reference(args, wl):
 METRIC = "W4 MoE layer tokens/s at T=1/512/2048; % of HBM or tensor roofline"
 
 
+# ------------------------------------------------------ multi-rank --
+def dist_env():
+    """(rank, world, local rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_token_seed(rank, chunk=0):
+    """Seed of a rank's hidden states: every rank holds its own tokens (token-
+    sharded replicas: the weights are the same on every rank, the tokens
+    are not). Rank 0 keeps the single-GPU inputs."""
+    return 10 ** 6 + chunk + 7919 * rank
+
+
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (a step time): the job is as slow as
+    its slowest rank."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step, world, ms_per_step):
+    """Tokens per second of the whole job: every rank's tokens over the
+    slowest rank's step time."""
+    return tokens_per_rank_step * world / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------- GPU arm --
 class GpuWorkload:
-    def __init__(self, wl, dev, m, tile_rows=128):
+    def __init__(self, wl, dev, m, tile_rows=128, rank=0):
         import torch
         self.wl, self.dev, self.m, self.torch = wl, dev, m, torch
         S = wl.shape
@@ -270,14 +299,14 @@ class GpuWorkload:
             del L
         if wl.chunk:
             self.n_chunks = wl.total_tokens // wl.chunk
-            xs = [synth.gen_tokens(T, S.H, 10 ** 6 + c) for c in range(self.n_chunks)]
+            xs = [synth.gen_tokens(T, S.H, rank_token_seed(rank, c)) for c in range(self.n_chunks)]
             self.x_host = np.concatenate(xs)
         elif wl.name == "decode":
             self.n_chunks = 1
-            self.x_host = synth.gen_tokens(1, S.H, 10 ** 6)
+            self.x_host = synth.gen_tokens(1, S.H, rank_token_seed(rank))
         else:
             self.n_chunks = 1
-            self.x_host = x0
+            self.x_host = x0 if rank == 0 else synth.gen_tokens(T, S.H, rank_token_seed(rank))
         self.tokens_per_step = T * self.n_chunks
         self.x_all = torch.from_numpy(self.x_host.view(np.int16)).to(dev)
         self.ws = m.alloc_workspace(self.shape, dev)
@@ -375,9 +404,7 @@ def run_ours(args, wl):
     import torch
     import torch.distributed as dist
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = dist_env()
     if world > 1:
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
@@ -388,7 +415,7 @@ def run_ours(args, wl):
     import bit_moe_expert_histogram_gb300 as m
     m.load()
 
-    G = GpuWorkload(wl, dev, m)
+    G = GpuWorkload(wl, dev, m, rank=rank)
     counts = G.realised_counts()
     algo_bytes, flops, ffn_bytes = layer_algo(G.T, wl.shape, counts)
     calls = G.n_chunks * len(G.layers)
@@ -444,9 +471,7 @@ def run_ours(args, wl):
     else:
         ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, dev)
     st = m.moe_query_device_status(G.ws)
     if st != 0:
         raise RuntimeError("device status %d after timed region" % st)
@@ -472,10 +497,13 @@ def run_ours(args, wl):
 
     e_eager_ms = time_e2e(lambda: G.step_e2e(x_pin, y_pin))
     e_ms = time_e2e(G.g_e2e.replay) if G.fused else e_eager_ms
+    if world > 1:
+        e_eager_ms = max_over_ranks(e_eager_ms, dist, dev)
+        e_ms = max_over_ranks(e_ms, dist, dev)
 
     hbm, bf16, bf16s, src = peaks()
     ms_step = ms / args.steps
-    value = G.tokens_per_step * world / (ms_step / 1e3)
+    value = job_throughput(G.tokens_per_step, world, ms_step)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -507,13 +535,14 @@ def run_ours(args, wl):
                                 " per layer, CUDA graph of %d layers" % len(G.layers)}
                      if G.fused else
                      {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)"}),
-        "e2e": {"value": round(G.tokens_per_step * world / (e_ms / 1e3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(G.tokens_per_step, world, e_ms), 2),
+                "unit": "tokens/s",
                 "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "steps": e_steps, "ms_per_step": round(e_ms, 5),
                 "mode": "CUDA graph of the moe_layer_w4 calls and copies" if G.fused
                         else "moe_layer_w4 calls",
-                "eager_value": round(G.tokens_per_step * world / (e_eager_ms / 1e3), 2)},
+                "eager_value": round(job_throughput(G.tokens_per_step, world, e_eager_ms), 2)},
         "gpu_launches": G.calls_per_layer() * calls * args.steps,
         "launch_mode": "CUDA graph replay, programmatic dependent launch" if G.fused
                        else "eager stream launches",

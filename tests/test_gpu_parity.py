@@ -331,3 +331,39 @@ def test_back_to_back_steps_match_single_step():
     assert m.moe_query_device_status(c.ws) == 0
     assert np.array_equal(h16(c.y), y1)
     _ffn_check(c, L, np.arange(0, 512, 8))
+
+
+def test_chunked_prefill_reuses_one_workspace():
+    """A prompt in two chunks of 256 tokens through two stacked layers with one
+    workspace ("Prefill": a long prompt runs in bounded chunks): each call's
+    routing is bit-exact and its output within tolerance of the oracle on the
+    GPU's own input (teacher-forced), sampled on 24 tokens per call."""
+    Tc, S = 256, FULL
+    dev = torch.device("cuda")
+    layers = [synth.gen_layer(Tc, S, seed=30 + l) for l in range(2)]
+    wts = []
+    for L in layers:
+        wts.append((d16(L.w_router, dev),
+                    m.ExpertWeights.from_numpy(L.q_gate_up, L.s_gate_up, L.b_gate_up, L.q_down,
+                                               L.s_down, L.b_down, dev),
+                    m.ExpertWeights.from_numpy(L.sh_q_gate_up, L.sh_s_gate_up, L.sh_b_gate_up,
+                                               L.sh_q_down, L.sh_s_down, L.sh_b_down, dev)))
+    shape = m.make_shape(Tc, S.H, S.E, S.K, S.I, S.n_shared, 128)
+    ws = m.alloc_workspace(shape, dev)
+    ids = torch.empty((Tc, S.K), dtype=torch.int32, device=dev)
+    w = torch.empty((Tc, S.K), dtype=torch.float32, device=dev)
+    y = torch.empty((Tc, S.H), dtype=torch.int16, device=dev)
+    xn = [torch.empty((Tc, S.H), dtype=torch.int16, device=dev) for _ in range(2)]
+    rng = np.random.default_rng(3)
+    for c in range(2):
+        x = d16(synth.gen_tokens(Tc, S.H, 500 + c), dev)
+        for l, (L, (wr, ex, sh)) in enumerate(zip(layers, wts)):
+            m.moe_layer_w4(shape, x, wr, None, ex, sh, y, ws, x_next=xn[l], topk_ids=ids, topk_w=w)
+            assert m.moe_query_device_status(ws) == 0
+            xin = h16(x)
+            ids_o, _, w64 = oracle.topk(oracle.router_logits(xin, L.w_router, None), S.K)
+            assert np.array_equal(ids.cpu().numpy(), ids_o)
+            tok = np.sort(rng.choice(Tc, 24, replace=False))
+            y_o = oracle.layer_tokens(L, ids_o, w64, tokens=tok, x=xin)
+            close(f64(h16(y))[tok], f64(y_o), "chunk %d layer %d" % (c, l))
+            x = xn[l]
