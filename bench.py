@@ -320,10 +320,11 @@ class GpuWorkload:
         self.xb = torch.empty((T, S.H), dtype=torch.int16, device=dev)
         self.y_out = torch.empty((T * self.n_chunks, S.H), dtype=torch.int16, device=dev)
         self.fused = m.moe_layer_path(self.shape) == 1
+        self.table = m.decode_layer_table(self.layers) if self.fused else None
 
     def calls_per_layer(self):
         # fused decode: route, gate_up, down; else route: 2 kernels, plan: 2, ffn: 2, combine: 1
-        return 3 if self.fused else 7
+        return 3 if self.fused else 7  # per layer
 
     def capture(self):
         """CUDA graphs of the device step and of the host-buffer step (decode:
@@ -351,14 +352,8 @@ class GpuWorkload:
         """One pass of the hot path over the step's tokens (device-resident)."""
         m, S, T = self.m, self.S, self.T
         nl = len(self.layers)
-        if self.fused:
-            x = self.x_all[:T]
-            for l, (wr, bias, ex, sh) in enumerate(self.layers):
-                last = l == nl - 1
-                xn = None if last else (self.xa if l % 2 == 0 else self.xb)
-                m.moe_layer_w4(self.shape, x, wr, bias, ex, sh, self.y_out if last else self.y,
-                               self.ws, x_next=xn, topk_ids=self.ids, topk_w=self.w)
-                x = xn
+        if self.fused:  # every layer in one call (moe_decode_layers)
+            m.moe_decode_layers(self.shape, self.table, self.x_all[:T], self.y_out, self.ws)
             return
         for c in range(self.n_chunks):
             x = self.x_all[c * T:(c + 1) * T]
@@ -378,9 +373,14 @@ class GpuWorkload:
                 x = xn
 
     def step_e2e(self, x_pin, y_pin):
-        """The same through moe_layer_w4 with host buffers copied in and out."""
+        """The same through the public calls with host buffers copied in and out."""
         m, T = self.m, self.T
         nl = len(self.layers)
+        if self.fused:
+            self.xa.copy_(x_pin[:T], non_blocking=True)
+            m.moe_decode_layers(self.shape, self.table, self.xa, self.y, self.ws)
+            y_pin[:T].copy_(self.y, non_blocking=True)
+            return
         for c in range(self.n_chunks):
             self.xa.copy_(x_pin[c * T:(c + 1) * T], non_blocking=True)
             x = self.xa
@@ -531,7 +531,7 @@ def run_ours(args, wl):
                  "hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
                  "tensor_frac": round(step_flops / (ms_step / 1e3) / 1e12 / bf16s, 4),
                  "touched_experts": int((counts > 0).sum()), "max_group": int(counts.max())},
-        "roofline": ({"kernel": "moe_layer_w4 decode chain (dec_route, dec_gate_up, dec_down)"
+        "roofline": ({"kernel": "moe_decode_layers chain (dec_route, dec_gate_up, dec_down)"
                                 " per layer, CUDA graph of %d layers" % len(G.layers)}
                      if G.fused else
                      {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)"}),
@@ -540,7 +540,7 @@ def run_ours(args, wl):
                 "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "steps": e_steps, "ms_per_step": round(e_ms, 5),
-                "mode": "CUDA graph of the moe_layer_w4 calls and copies" if G.fused
+                "mode": "CUDA graph of the moe_decode_layers call and copies" if G.fused
                         else "moe_layer_w4 calls",
                 "eager_value": round(job_throughput(G.tokens_per_step, world, e_eager_ms), 2)},
         "gpu_launches": G.calls_per_layer() * calls * args.steps,

@@ -30,7 +30,7 @@ MOE_ERR_TIMEOUT = 6
 EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_route",
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
-           "moe_last_error", "moe_plan_noalloc", "moe_layer_path")
+           "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers")
 
 
 class MoeError(RuntimeError):
@@ -54,6 +54,11 @@ class Shape(C.Structure):
 class W4Weights(C.Structure):
     _fields_ = [("q_gate_up", C.c_void_p), ("s_gate_up", C.c_void_p), ("b_gate_up", C.c_void_p),
                 ("q_down", C.c_void_p), ("s_down", C.c_void_p), ("b_down", C.c_void_p)]
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [("w_router", C.c_void_p), ("router_bias", C.c_void_p),
+                ("experts", W4Weights), ("shared", W4Weights)]
 
 
 class PlanPtrs(C.Structure):
@@ -91,7 +96,8 @@ def load():
                     ("moe_layer_w4", [pS, P, P, P, pW, pW, P, P, P, P, P, SZ, P]),
                     ("moe_query_device_status", [P, SZ, P]),
                     ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P]),
-                    ("moe_plan_noalloc", [pS, P, pP, P])):
+                    ("moe_plan_noalloc", [pS, P, pP, P]),
+                    ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -172,6 +178,26 @@ def moe_plan_noalloc(shape, topk_ids, plan, stream=None):
 def moe_combine(shape, y_slots, row_pos, topk_w, y, x_next=None, stream=None):
     _check(load().moe_combine(C.byref(shape), _p(y_slots), _p(row_pos), _p(topk_w), _p(y),
                               _p(x_next), _s(stream)), "moe_combine")
+
+
+def decode_layer_table(layers):
+    """Host array of moe_layer_weights_t from (w_router, router_bias or None,
+    experts, shared or None) tuples; keep it alive while it is used."""
+    arr = (LayerWeights * len(layers))()
+    for i, (wr, bias, ex, sh) in enumerate(layers):
+        arr[i].w_router = _p(wr)
+        arr[i].router_bias = _p(bias)
+        arr[i].experts = ex.ptrs
+        if sh is not None:
+            arr[i].shared = sh.ptrs
+    return arr
+
+
+def moe_decode_layers(shape, layer_table, x, y, ws, x_next=None, stream=None):
+    """n stacked decode layers (layer_table from decode_layer_table)."""
+    _check(load().moe_decode_layers(C.byref(shape), len(layer_table),
+                                    C.cast(layer_table, C.c_void_p), _p(x), _p(y), _p(x_next),
+                                    _p(ws), ws.numel(), _s(stream)), "moe_decode_layers")
 
 
 def moe_layer_w4(shape, x, w_router, router_bias, experts, shared, y, ws, x_next=None,

@@ -49,7 +49,7 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 
 struct Layout {
   size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
-      rpart, total;
+      rpart, part2, ybuf, total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -79,6 +79,10 @@ Layout layout_of(const moe_shape_t* s) {
   L.rpart = route_tc_supported(s->T, s->H, s->E, s->K)
                 ? take(route_tc_partial_floats(s->T, s->H, s->E) * 4)
                 : off;
+  // stacked decode: a second partial buffer and two y buffers (ping-pong)
+  const bool dec = decode_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
+  L.part2 = dec ? take(decode_part_floats(s->T, s->H) * 4) : off;
+  L.ybuf = dec ? take((size_t)2 * T * s->H * 2) : off;
   L.total = off;
   return L;
 }
@@ -244,6 +248,31 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   return MOE_OK;
 }
 
+// Arguments of one decode layer with every workspace intermediate; the
+// caller sets x / y_prev, ids, w, y, x_next and the stacking fields.
+DecodeArgs decode_args(const moe_shape_t* s, const void* w_router, const float* bias,
+                       const moe_w4_weights_t* experts, const moe_w4_weights_t* shared,
+                       uint8_t* ws, const Layout& L) {
+  DecodeArgs d{};
+  d.wr = static_cast<const uint16_t*>(w_router);
+  d.bias = bias;
+  d.T = s->T;
+  d.H = s->H;
+  d.E = s->E;
+  d.K = s->K;
+  d.I = s->I;
+  d.ns = s->n_shared;
+  d.ex = *experts;
+  d.sh = s->n_shared ? *shared : *experts;
+  d.logits = reinterpret_cast<float*>(ws + L.logits);
+  d.ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  d.w = reinterpret_cast<float*>(ws + L.w);
+  d.h = reinterpret_cast<uint16_t*>(ws + L.h);
+  d.part = reinterpret_cast<float*>(ws + L.part);
+  d.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  return d;
+}
+
 }  // namespace
 
 namespace moe {
@@ -371,26 +400,12 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   void* y_slots = ws + L.yslots;
   cudaStream_t st = (cudaStream_t)stream;
   if (decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared)) {
-    DecodeArgs d{};
+    DecodeArgs d = decode_args(shape, w_router_dev, router_bias_dev, experts, shared, ws, L);
     d.x = static_cast<const uint16_t*>(x_dev);
-    d.wr = static_cast<const uint16_t*>(w_router_dev);
-    d.bias = router_bias_dev;
-    d.T = shape->T;
-    d.H = shape->H;
-    d.E = shape->E;
-    d.K = shape->K;
-    d.I = shape->I;
-    d.ns = shape->n_shared;
-    d.ex = *experts;
-    d.sh = shape->n_shared ? *shared : *experts;
-    d.logits = reinterpret_cast<float*>(ws + L.logits);
     d.ids = ids;
     d.w = w;
-    d.h = reinterpret_cast<uint16_t*>(ws + L.h);
     d.y = static_cast<uint16_t*>(y_dev);
     d.x_next = static_cast<uint16_t*>(x_next_dev);
-    d.part = reinterpret_cast<float*>(ws + L.part);
-    d.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
     cudaError_t e = launch_decode_layer(d, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
   }
@@ -398,6 +413,51 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
   MOE_TRY(run_ffn(shape, x_dev, experts, shared, &plan, y_slots, ws, st));
   return moe_combine(shape, y_slots, plan.row_pos_dev, w, y_dev, x_next_dev, stream);
+}
+
+moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
+                               const moe_layer_weights_t* layers_host, const void* x_dev,
+                               void* y_dev, void* x_next_dev, void* ws_dev, size_t ws_bytes,
+                               moe_stream_t stream) {
+  if (!shape_ok(shape) ||
+      !decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n_layers < 1 || !layers_host || !x_dev || !y_dev || !aligned16(x_dev) || !aligned16(y_dev) ||
+      (x_next_dev && !aligned16(x_next_dev)))
+    return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_layer_weights_t& lw = layers_host[l];
+    if (!lw.w_router_dev || !aligned16(lw.w_router_dev) || !weights_ok(&lw.experts))
+      return MOE_ERR_INVALID_ARG;
+    if (shape->n_shared && !weights_ok(&lw.shared)) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  const Layout L = layout_of(shape);
+  float* part[2] = {reinterpret_cast<float*>(ws + L.part), reinterpret_cast<float*>(ws + L.part2)};
+  uint16_t* ybuf[2] = {reinterpret_cast<uint16_t*>(ws + L.ybuf),
+                       reinterpret_cast<uint16_t*>(ws + L.ybuf) + (size_t)shape->T * shape->H};
+  const int nb = (int)(decode_part_floats(shape->T, shape->H) / shape->T);
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_layer_weights_t& lw = layers_host[l];
+    DecodeArgs d = decode_args(shape, lw.w_router_dev, lw.router_bias_dev, &lw.experts,
+                               &lw.shared, ws, L);
+    if (l == 0) {
+      d.x = static_cast<const uint16_t*>(x_dev);
+    } else {
+      d.y_prev = ybuf[(l - 1) & 1];
+      d.part_prev = part[(l - 1) & 1];
+      d.nb_prev = nb;
+    }
+    const bool last = l == n_layers - 1;
+    d.y = last ? static_cast<uint16_t*>(y_dev) : ybuf[l & 1];
+    d.part = part[l & 1];
+    d.x_next = last ? static_cast<uint16_t*>(x_next_dev) : nullptr;
+    d.has_next = last ? 0 : 1;
+    cudaError_t e = launch_decode_layer(d, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode layer launch");
+  }
+  return MOE_OK;
 }
 
 moe_status_t moe_query_device_status(void* ws_dev, size_t ws_bytes, moe_stream_t stream) {

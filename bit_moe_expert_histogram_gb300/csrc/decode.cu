@@ -101,6 +101,27 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// 1 / sqrt(mean(y^2) + 1e-6) of one token from its nb block partials of y^2,
+// summed in one fixed order: partial i to lane i mod 32 (ascending), then an
+// xor butterfly over distances 16..1. Called by a whole warp; every lane
+// returns the same value.
+__device__ __forceinline__ float rms_inv_warp(const float* part, int nb, int H, int lane) {
+  float s = 0.0f;
+#pragma unroll 8
+  for (int i = lane; i < nb; i += 32) s += __ldcg(part + i);
+  s = warp_sum(s);
+  return 1.0f / sqrtf(s / (float)H + 1e-6f);
+}
+// the normalised next-layer input: bf16(y * inv) of 8 packed bf16 y values
+__device__ __forceinline__ uint4 norm_chunk(const uint4& v, float inv) {
+  uint4 o;
+  o.x = pack_bf2(bf_lo(v.x) * inv, bf_hi(v.x) * inv);
+  o.y = pack_bf2(bf_lo(v.y) * inv, bf_hi(v.y) * inv);
+  o.z = pack_bf2(bf_lo(v.z) * inv, bf_hi(v.z) * inv);
+  o.w = pack_bf2(bf_lo(v.w) * inv, bf_hi(v.w) * inv);
+  return o;
+}
+
 // Activation rows in shared memory, bf16: chunk c (elements 32c..32c+31,
 // 64 bytes) keeps its 16-byte piece v at (v + c/2) mod 4. A lane reads the
 // four pieces of its own chunk and consecutive lanes take consecutive
@@ -263,20 +284,38 @@ __global__ void __launch_bounds__(128) dec_route_kernel(DecodeArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ctrl->routed = 0u;
   pdl_trigger();
   if (!valid) return;
-  const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
+  const bool stacked = a.y_prev != nullptr;
+  const uint4* xr =
+      reinterpret_cast<const uint4*>((stacked ? a.y_prev : a.x) + (size_t)t * H);
   const uint4* wq = reinterpret_cast<const uint4*>(a.wr + (size_t)e * H);
+  // the token's input chunks are loaded with the normalisation's partials
+  // (one round trip), then normalised
+  constexpr int kRouteJ = 8;  // chunks per lane held in registers (H <= 2048)
+  const int nj = H >> 8;
+  uint4 xin[kRouteJ];
+#pragma unroll
+  for (int j = 0; j < kRouteJ; ++j)
+    if (j < nj) xin[j] = __ldcg(xr + 32 * j + lane);
+  const float inv = stacked ? rms_inv_warp(a.part_prev + (size_t)t * a.nb_prev, a.nb_prev, H, lane)
+                            : 1.0f;
   float acc = 0.0f;  // partial `lane`: elements 8*(32j+lane)+i, j then i ascending
-#pragma unroll 8
-  for (int j = 0; j < (H >> 8); ++j) {
-    const uint4 xv = __ldcg(xr + 32 * j + lane), wv = __ldg(wq + 32 * j + lane);
-    acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
-    acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
-    acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
-    acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
-    acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
-    acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
-    acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
-    acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+#pragma unroll
+  for (int j = 0; j < kRouteJ + 1; ++j) {
+    if (j < kRouteJ && j >= nj) break;
+    // j == kRouteJ: the chunks past the registers (H > 2048), in order
+    for (int jj = (j < kRouteJ ? j : kRouteJ); jj < (j < kRouteJ ? j + 1 : nj); ++jj) {
+      const uint4 xraw = j < kRouteJ ? xin[j] : __ldcg(xr + 32 * jj + lane);
+      const uint4 xv = stacked ? norm_chunk(xraw, inv) : xraw;
+      const uint4 wv = __ldg(wq + 32 * jj + lane);
+      acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
+      acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
+      acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
+      acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
+      acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
+      acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
+      acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
+      acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
+    }
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, d));
@@ -292,6 +331,7 @@ __global__ void __launch_bounds__(kGuWarps * 32) dec_gate_up_kernel(DecodeArgs a
   __shared__ TopkWarpSmem<kDecCand> TS[kDecodeMaxT];
   __shared__ int sid[kDecodeMaxT][32];
   __shared__ float swt[kDecodeMaxT][32];
+  __shared__ float xinv[kDecodeMaxT];
   const int T = a.T, H = a.H, I = a.I, K = a.K, slots = K + a.ns;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kGuWarps + (threadIdx.x >> 5);
@@ -315,16 +355,24 @@ __global__ void __launch_bounds__(kGuWarps * 32) dec_gate_up_kernel(DecodeArgs a
   // top-K, so their L2 latency hides behind it
   uint4 xreg[kDecodeMaxT * 2048 / 8 / (kGuWarps * 32)];
   const int xn = T * H / 8;  // 16-byte pieces of all T rows
+  const bool stacked = a.y_prev != nullptr;
+  const uint16_t* xsrc = stacked ? a.y_prev : a.x;
 #pragma unroll
   for (int u = 0; u < (int)(sizeof(xreg) / sizeof(uint4)); ++u) {
     const int i = threadIdx.x + u * kGuWarps * 32;
-    if (i < xn) xreg[u] = __ldcg(reinterpret_cast<const uint4*>(a.x) + i);
+    if (i < xn) xreg[u] = __ldcg(reinterpret_cast<const uint4*>(xsrc) + i);
   }
-  // every block selects the experts itself: warp t takes token t
+  // every block selects the experts itself: warp t takes token t; with a
+  // stacked input, warp kGuWarps-1-t forms token t's normalisation meanwhile
   const int warp = threadIdx.x >> 5;
   if (warp < T)
     topk_warp<kDecCand, kDecMaxE / 32>(a.logits + (size_t)warp * a.E, a.E, K, lane, TS[warp],
                                        sid[warp], swt[warp]);
+  if (stacked && warp >= kGuWarps - T) {
+    const int tt = kGuWarps - 1 - warp;
+    const float v = rms_inv_warp(a.part_prev + (size_t)tt * a.nb_prev, a.nb_prev, H, lane);
+    if (lane == 0) xinv[tt] = v;
+  }
   __syncthreads();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < T * K; i += blockDim.x) {
@@ -349,14 +397,16 @@ __global__ void __launch_bounds__(kGuWarps * 32) dec_gate_up_kernel(DecodeArgs a
     const int i = threadIdx.x + u * kGuWarps * 32;
     if (i < xn) {
       const int tt = i / (H / 8), ii = i - tt * (H / 8);
-      *reinterpret_cast<uint4*>(xs + (size_t)tt * H * 2 + act_piece_off(ii >> 2, ii & 3)) = xreg[u];
+      *reinterpret_cast<uint4*>(xs + (size_t)tt * H * 2 + act_piece_off(ii >> 2, ii & 3)) =
+          stacked ? norm_chunk(xreg[u], xinv[tt]) : xreg[u];
     }
   }
   for (int i = threadIdx.x + (int)(sizeof(xreg) / sizeof(uint4)) * kGuWarps * 32; i < xn;
        i += kGuWarps * 32) {  // rows beyond the register budget (T*H > 8192)
     const int tt = i / (H / 8), ii = i - tt * (H / 8);
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(xsrc) + i);
     *reinterpret_cast<uint4*>(xs + (size_t)tt * H * 2 + act_piece_off(ii >> 2, ii & 3)) =
-        __ldcg(reinterpret_cast<const uint4*>(a.x) + i);
+        stacked ? norm_chunk(v, xinv[tt]) : v;
   }
   __syncthreads();
   if (!valid) return;
@@ -498,9 +548,10 @@ __global__ void __maxnreg__(96) dec_down_kernel(DecodeArgs a) {
     const float yr = __uint_as_float(yb << 16);
     ysq = yr * yr;
   }
-  if (!a.x_next) return;
-  // unit-RMS normalisation of the bf16 y: block partials of y^2, then the
-  // last block sums them in block order and writes every token's x_next
+  if (!a.x_next && !a.has_next) return;
+  // unit-RMS normalisation of the bf16 y: block partials of y^2 (for a
+  // stacked next layer, which folds the normalisation into its own
+  // kernels), and with x_next the last block writes every token's x_next
   if (warp == 0) {
     ysq = warp_sum(ysq);
     __syncwarp();  // orders lanes 0..kDownRows-1's y stores before lane 0's release
@@ -508,20 +559,15 @@ __global__ void __maxnreg__(96) dec_down_kernel(DecodeArgs a) {
       a.part[(size_t)t * gridDim.x + blockIdx.x] = ysq;
       // release: this block's y and partial (lanes 0..kDownRows-1 of this
       // warp wrote them); acquire: every other block's, for the last one
-      last = atom_add_acq_rel(&a.ctrl->ticket2, 1u) == gridDim.x * gridDim.y - 1;
+      if (a.x_next) last = atom_add_acq_rel(&a.ctrl->ticket2, 1u) == gridDim.x * gridDim.y - 1;
     }
   }
+  if (!a.x_next) return;
   __syncthreads();
   if (!last) return;
   const int nb = gridDim.x, nth = blockDim.x;
   for (int tt = 0; tt < a.T; ++tt) {
-    // every load of the token first (one round trip), then the sums
-    float pp[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = threadIdx.x + u * nth;
-      pp[u] = i < nb ? __ldcg(a.part + (size_t)tt * nb + i) : 0.0f;
-    }
+    // the token's y loads first, then the normalisation (rms_inv_warp's order)
     const uint32_t* yr = reinterpret_cast<const uint32_t*>(a.y + (size_t)tt * H);
     uint32_t* xr = reinterpret_cast<uint32_t*>(a.x_next + (size_t)tt * H);
     uint32_t yv[8];
@@ -530,20 +576,12 @@ __global__ void __maxnreg__(96) dec_down_kernel(DecodeArgs a) {
       const int i = threadIdx.x + u * nth;
       yv[u] = i < (H >> 1) ? __ldcg(yr + i) : 0u;
     }
-    float ss = 0.0f;
-    for (int i = threadIdx.x + 4 * nth; i < nb; i += nth) ss += __ldcg(a.part + (size_t)tt * nb + i);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) ss += pp[u];
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float tot = 0.0f;
-      for (int i = 0; i < nwarps; ++i) tot += red[i];
-      red[kDownMaxWarps] = tot;
+    if (warp == 0) {
+      const float v = rms_inv_warp(a.part + (size_t)tt * nb, nb, H, lane);
+      if (lane == 0) red[kDownMaxWarps] = v;
     }
     __syncthreads();
-    const float inv = 1.0f / sqrtf(red[kDownMaxWarps] / (float)H + 1e-6f);
+    const float inv = red[kDownMaxWarps];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = threadIdx.x + u * nth;

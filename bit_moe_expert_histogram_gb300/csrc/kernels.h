@@ -55,6 +55,14 @@ struct DecodeArgs {
   uint16_t* x_next;     // bf16 [T][H] or null
   float* part;          // [decode_part_floats(T, H)]
   Ctrl* ctrl;
+  // stacked layers (moe_decode_layers): with y_prev, the input is
+  // bf16(y_prev * inv) with inv from part_prev (the previous layer's block
+  // partials, nb_prev per token) instead of x; with has_next, dec_down writes
+  // its block partials for the next layer
+  const uint16_t* y_prev;
+  const float* part_prev;
+  int nb_prev;
+  int has_next;
 };
 bool decode_supported(int T, int H, int E, int K, int I, int ns);
 size_t decode_part_floats(int T, int H);

@@ -194,6 +194,33 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
  * that work writes before that work has completed. */
 int32_t moe_layer_path(const moe_shape_t* shape);
 
+/* One stacked layer's weights for moe_decode_layers. */
+typedef struct moe_layer_weights {
+  const void* w_router_dev;       /* bf16 [E][H] */
+  const float* router_bias_dev;   /* fp32 [E] or NULL */
+  moe_w4_weights_t experts;       /* the E routed experts */
+  moe_w4_weights_t shared;        /* the shared expert (ignored when n_shared == 0) */
+} moe_layer_weights_t;
+
+/* n_layers stacked layers for a few tokens ([Lily] "Decode": the kernel
+ * chain of a decode step, with nothing leaving the GPU between layers).
+ * Layer 0 takes x_dev; layer l > 0 takes the unit-RMS normalisation of
+ * layer l-1's output, bf16(y / sqrt(mean(y^2) + 1e-6)), exactly what
+ * moe_layer_w4 writes to x_next, and the results are bit-identical to that
+ * chain of moe_layer_w4 calls. Between layers the normalisation is folded
+ * into the next layer's kernels: no intermediate x_next is written and no
+ * block waits for the last one to normalise.
+ *  layers_host  host array of n_layers entries, read during the call
+ *  x_dev        bf16 [T][H] input of layer 0
+ *  y_dev        bf16 [T][H] output of the last layer
+ *  x_next_dev   bf16 [T][H] normalised last output, or NULL
+ * Requires moe_layer_path(shape) == 1 (else MOE_ERR_UNSUPPORTED_SHAPE) and
+ * n_layers >= 1. Graph-capturable; allocates nothing. */
+moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
+                               const moe_layer_weights_t* layers_host, const void* x_dev,
+                               void* y_dev, void* x_next_dev, void* ws_dev, size_t ws_bytes,
+                               moe_stream_t stream);
+
 /* moe_plan without a workspace: same inputs, same outputs, bit-identical
  * results. The pages have no counterpart; this entry point exists for
  * callers that cannot allocate device memory where they build the plan (code

@@ -117,3 +117,15 @@ def test_status_strings(lib):
     for code in range(7):
         assert lib.moe_status_string(code)
     assert lib.moe_status_string(99) == b"unknown status"
+
+
+def test_decode_layers_argument_errors(lib):
+    s = m.make_shape(1, 256, 16, 2, 128, 1, 128)
+    big = m.make_shape(5, 256, 16, 2, 128, 1, 128)   # T=5 takes the grouped-GEMM path
+    table = (m.LayerWeights * 1)()
+    assert lib.moe_decode_layers(C.byref(big), 1, C.cast(table, C.c_void_p), None, None, None,
+                                 None, 0, None) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_decode_layers(C.byref(s), 0, C.cast(table, C.c_void_p), None, None, None,
+                                 None, 0, None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_layers(C.byref(s), 1, None, None, None, None, None, 0,
+                                 None) == m.MOE_ERR_INVALID_ARG

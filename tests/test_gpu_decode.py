@@ -129,3 +129,29 @@ def test_decode_stacked_layers_teacher_forced():
             c.x.copy_(cs[i - 1].x_next)
         c.run_layer(x_next=True)
         check_layer(c, Ls[i], h16(c.x))
+
+
+@pytest.mark.parametrize("shape,T", [(FULL, 1), (FULL, 3), (TINY, 2), (NOSH, 1)],
+                         ids=["full-1", "full-3", "tiny-2", "noshared-1"])
+def test_decode_layers_equal_the_moe_layer_chain(shape, T):
+    """moe_decode_layers (normalisation folded into the next layer, next
+    layer's weights prefetched) gives the bits of the moe_layer_w4 chain."""
+    dev = torch.device("cuda")
+    Ls = [synth.gen_layer(T, shape, seed=40 + i) for i in range(3)]
+    cs = [Case(L, T, shape) for L in Ls]
+    x0 = cs[0].x.clone()
+    for i, c in enumerate(cs):
+        if i:
+            c.x.copy_(cs[i - 1].x_next)
+        c.run_layer(x_next=True)
+    y_chain = h16(cs[-1].y).copy()
+    xn_chain = h16(cs[-1].x_next).copy()
+    table = m.decode_layer_table([(c.wr, c.bias, c.ex, c.sh) for c in cs])
+    ws = m.alloc_workspace(cs[0].shape, dev)
+    y = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
+    xn = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
+    for _ in range(2):   # twice: the ping-pong buffers and flags start from any state
+        m.moe_decode_layers(cs[0].shape, table, x0, y, ws, x_next=xn)
+        assert m.moe_query_device_status(ws) == 0
+        assert np.array_equal(h16(y), y_chain)
+        assert np.array_equal(h16(xn), xn_chain)
