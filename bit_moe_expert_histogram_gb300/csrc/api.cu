@@ -49,7 +49,7 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 
 struct Layout {
   size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
-      rpart, part2, ybuf, total;
+      rpart, part2, ybuf, tags, xmid, total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -83,6 +83,12 @@ Layout layout_of(const moe_shape_t* s) {
   const bool dec = decode_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
   L.part2 = dec ? take(decode_part_floats(s->T, s->H) * 4) : off;
   L.ybuf = dec ? take((size_t)2 * T * s->H * 2) : off;
+  // persistent decode: the epoch-tagged block-to-block words, and the
+  // normalised input handed from one launch of up to kPersistMaxLayers
+  // layers to the next
+  const bool ps = persist_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
+  L.tags = ps ? take(persist_tags(s->T, s->H, s->E, s->K, s->I, s->n_shared).total * 8) : off;
+  L.xmid = ps ? take(T * (size_t)s->H * 2) : off;
   L.total = off;
   return L;
 }
@@ -273,6 +279,45 @@ DecodeArgs decode_args(const moe_shape_t* s, const void* w_router, const float* 
   return d;
 }
 
+// moe_decode_layers on the persistent kernel: launches of up to
+// kPersistMaxLayers layers; between two launches the normalised input
+// passes through the workspace (the bits the next layer would form itself).
+moe_status_t decode_persistent(const moe_shape_t* s, int n_layers,
+                               const moe_layer_weights_t* layers, const void* x, void* y,
+                               void* x_next, int32_t* ids, float* w, uint8_t* ws,
+                               const Layout& L, int grid, size_t smem, cudaStream_t stream) {
+  PersistArgs a{};
+  a.T = s->T;
+  a.H = s->H;
+  a.E = s->E;
+  a.K = s->K;
+  a.I = s->I;
+  a.ns = s->n_shared;
+  a.y = static_cast<uint16_t*>(y);
+  a.ids = ids ? ids : reinterpret_cast<int32_t*>(ws + L.ids);
+  a.w = w ? w : reinterpret_cast<float*>(ws + L.w);
+  uint64_t* tags = reinterpret_cast<uint64_t*>(ws + L.tags);
+  const PersistTags tl = persist_tags(s->T, s->H, s->E, s->K, s->I, s->n_shared);
+  a.logits_tag = tags + tl.logits;
+  a.h_tag = tags + tl.h;
+  a.y_tag = tags + tl.y;
+  a.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  uint16_t* xmid = reinterpret_cast<uint16_t*>(ws + L.xmid);
+  for (int l0 = 0; l0 < n_layers; l0 += kPersistMaxLayers) {
+    const int n = n_layers - l0 < kPersistMaxLayers ? n_layers - l0 : kPersistMaxLayers;
+    a.n_layers = n;
+    a.x = l0 == 0 ? static_cast<const uint16_t*>(x) : xmid;
+    a.x_next = l0 + n == n_layers ? static_cast<uint16_t*>(x_next) : xmid;
+    for (int i = 0; i < n; ++i) {
+      a.layer[i] = layers[l0 + i];
+      if (!s->n_shared) a.layer[i].shared = a.layer[i].experts;
+    }
+    cudaError_t e = launch_decode_persist(a, grid, smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "persistent decode launch");
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 namespace moe {
@@ -298,7 +343,7 @@ int32_t moe_max_blocks(const moe_shape_t* shape) {
 
 moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, moe_stream_t stream) {
   if (!ws_dev || ws_bytes < sizeof(Ctrl)) return MOE_ERR_INVALID_ARG;
-  cudaError_t e = cudaMemsetAsync(ws_dev, 0, sizeof(Ctrl), (cudaStream_t)stream);
+  cudaError_t e = cudaMemsetAsync(ws_dev, 0, ws_bytes, (cudaStream_t)stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
 }
 
@@ -399,6 +444,18 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   plan.num_blocks_dev = reinterpret_cast<int32_t*>(ws + L.nblk);
   void* y_slots = ws + L.yslots;
   cudaStream_t st = (cudaStream_t)stream;
+  int grid = 0;
+  size_t smem = 0;
+  if (persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid,
+                     &smem)) {
+    moe_layer_weights_t lw;
+    lw.w_router_dev = w_router_dev;
+    lw.router_bias_dev = router_bias_dev;
+    lw.experts = *experts;
+    lw.shared = shape->n_shared ? *shared : *experts;
+    return decode_persistent(shape, 1, &lw, x_dev, y_dev, x_next_dev, ids, w, ws, L, grid, smem,
+                             st);
+  }
   if (decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared)) {
     DecodeArgs d = decode_args(shape, w_router_dev, router_bias_dev, experts, shared, ws, L);
     d.x = static_cast<const uint16_t*>(x_dev);
@@ -434,6 +491,12 @@ moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
   MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
   uint8_t* ws = static_cast<uint8_t*>(ws_dev);
   const Layout L = layout_of(shape);
+  int grid = 0;
+  size_t smem = 0;
+  if (persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid,
+                     &smem))
+    return decode_persistent(shape, n_layers, layers_host, x_dev, y_dev, x_next_dev, nullptr,
+                             nullptr, ws, L, grid, smem, (cudaStream_t)stream);
   float* part[2] = {reinterpret_cast<float*>(ws + L.part), reinterpret_cast<float*>(ws + L.part2)};
   uint16_t* ybuf[2] = {reinterpret_cast<uint16_t*>(ws + L.ybuf),
                        reinterpret_cast<uint16_t*>(ws + L.ybuf) + (size_t)shape->T * shape->H};

@@ -21,7 +21,10 @@ struct Ctrl {
   unsigned unit_done;  // grouped GEMM: CTAs finished handing out units
   unsigned ticket2;  // last-block counter of the decode down kernel (RMS norm)
   unsigned routed;   // decode: 1 once this layer's ids / w are published
-  int pad[55];
+  unsigned ps_seq;   // persistent decode: launches so far (epoch base of the next one)
+  unsigned ps_exit;  // persistent decode: blocks finished (reset by the last one)
+  unsigned ps_abort; // persistent decode: a wait ran out; every block stops waiting
+  int pad[52];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 

@@ -68,6 +68,37 @@ bool decode_supported(int T, int H, int E, int K, int I, int ns);
 size_t decode_part_floats(int T, int H);
 cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream);
 
+// Persistent decode through stacked layers (decode_persist.cu): one
+// cooperative launch runs up to kPersistMaxLayers layers.
+constexpr int kPersistMaxLayers = 48;
+struct PersistArgs {
+  int T, H, E, K, I, ns, n_layers;
+  const uint16_t* x;    // bf16 [T][H]: the first layer's input
+  uint16_t* y;          // bf16 [T][H]: the last layer's output
+  uint16_t* x_next;     // bf16 [T][H] or null: its unit-RMS normalisation
+  int32_t* ids;         // [T][K]: routing of the last layer
+  float* w;             // [T][K]
+  // cross-block words (epoch << 32 | payload), laid out by persist_tags():
+  // 16-word lines, each written by one warp
+  uint64_t* logits_tag; // line t*E+e: word 0 = fp32 logit
+  uint64_t* h_tag;      // line per gate_up tile: words 4 col + r = bf16 pair (h_r, h_r+4)
+  uint64_t* y_tag;      // line t*(H/8)+g: words 0..3 = bf16 pairs (y_r, y_r+4), word 4 = y^2 partial
+  Ctrl* ctrl;
+  moe_layer_weights_t layer[kPersistMaxLayers];
+};
+bool persist_supported(int T, int H, int E, int K, int I, int ns);
+// Word offsets of the three tagged buffers in one region, and its size.
+struct PersistTags {
+  size_t logits, h, y, total;
+};
+PersistTags persist_tags(int T, int H, int E, int K, int I, int ns);
+// Grid and dynamic shared memory of a launch on the current device; false
+// when the shape's blocks do not fit on it (the caller takes the per-layer
+// kernels then).
+bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t* smem);
+cudaError_t launch_decode_persist(const PersistArgs& a, int grid, size_t smem,
+                                  cudaStream_t stream);
+
 // Tensor-core screened router (route_tc.cu), taken from this many tokens on.
 constexpr int kRouteTcMinT = 64;
 bool route_tc_supported(int T, int H, int E, int K);

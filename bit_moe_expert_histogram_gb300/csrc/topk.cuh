@@ -41,16 +41,18 @@ struct TopkWarpSmem {
 // other would be beaten by K of them). Those candidates are ranked by the
 // composite key; a candidate's rank is its slot. With fewer than K lanes
 // holding experts, every expert is a candidate. Writes ids[0..K), w[0..K).
+// topk_warp_vals takes the logits already in registers: v[i] = the logit
+// of expert lane + 32i (ignored for an expert >= E).
 template <int CAP, int NMAX>
-__device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int K, int lane,
-                                          TopkWarpSmem<CAP>& S, int32_t* ids, float* w) {
+__device__ __forceinline__ void topk_warp_vals(const float (&v)[NMAX], int E, int K, int lane,
+                                               TopkWarpSmem<CAP>& S, int32_t* ids, float* w) {
   const int n = (E + 31) >> 5;
   unsigned long long c[NMAX];
   uint32_t kmax = 0u;
 #pragma unroll
   for (int i = 0; i < NMAX; ++i) {
     const int e = lane + 32 * i;
-    c[i] = (i < n && e < E) ? topk_ckey(__ldcg(l + e), e) : 0ull;
+    c[i] = (i < n && e < E) ? topk_ckey(v[i], e) : 0ull;
     kmax = max(kmax, (uint32_t)(c[i] >> 32));
   }
   int r = 0;  // lanes whose largest key is larger than this lane's
@@ -97,6 +99,19 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, in
     w[lane] = ex / z;
   }
   __syncwarp();
+}
+
+template <int CAP, int NMAX>
+__device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int K, int lane,
+                                          TopkWarpSmem<CAP>& S, int32_t* ids, float* w) {
+  const int n = (E + 31) >> 5;
+  float v[NMAX];
+#pragma unroll
+  for (int i = 0; i < NMAX; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (i < n && e < E) ? __ldcg(l + e) : 0.0f;
+  }
+  topk_warp_vals<CAP, NMAX>(v, E, K, lane, S, ids, w);
 }
 
 }  // namespace moe

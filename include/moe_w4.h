@@ -117,7 +117,8 @@ size_t moe_workspace_bytes(const moe_shape_t* shape);
  * sized without reading the device count back. 0 if unsupported. */
 int32_t moe_max_blocks(const moe_shape_t* shape);
 
-/* Zero-fill the workspace's status area (enqueued on stream). */
+/* Zero-fill the workspace (enqueued on stream): its status word, the
+ * kernels' counters and the persistent decode's tagged words. */
 moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, moe_stream_t stream);
 
 /* Router: logits, top-K, renormalised softmax ([Lily] "Three Workload
@@ -209,7 +210,13 @@ typedef struct moe_layer_weights {
  * moe_layer_w4 writes to x_next, and the results are bit-identical to that
  * chain of moe_layer_w4 calls. Between layers the normalisation is folded
  * into the next layer's kernels: no intermediate x_next is written and no
- * block waits for the last one to normalise.
+ * block waits for the last one to normalise. When T <= 4, T*H <= 8192 and
+ * E <= 256 and the device holds one block of 512 threads per SM with the
+ * shape's shared memory, the layers run in one persistent cooperative
+ * launch per 48 layers (all blocks resident; the blocks hand the layer's
+ * intermediates to each other through the workspace, with bounded waits
+ * that record MOE_ERR_TIMEOUT); otherwise three kernels per layer. The
+ * workspace must have been zero-filled by moe_workspace_init.
  *  layers_host  host array of n_layers entries, read during the call
  *  x_dev        bf16 [T][H] input of layer 0
  *  y_dev        bf16 [T][H] output of the last layer

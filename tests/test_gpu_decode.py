@@ -131,11 +131,11 @@ def test_decode_stacked_layers_teacher_forced():
         check_layer(c, Ls[i], h16(c.x))
 
 
-@pytest.mark.parametrize("shape,T", [(FULL, 1), (FULL, 3), (TINY, 2), (NOSH, 1)],
-                         ids=["full-1", "full-3", "tiny-2", "noshared-1"])
+@pytest.mark.parametrize("shape,T", [(FULL, 1), (FULL, 3), (FULL, 4), (TINY, 2), (NOSH, 1)],
+                         ids=["full-1", "full-3", "full-4", "tiny-2", "noshared-1"])
 def test_decode_layers_equal_the_moe_layer_chain(shape, T):
-    """moe_decode_layers (normalisation folded into the next layer, next
-    layer's weights prefetched) gives the bits of the moe_layer_w4 chain."""
+    """moe_decode_layers (one persistent launch; the normalisation folded
+    into the next layer) gives the bits of the moe_layer_w4 chain."""
     dev = torch.device("cuda")
     Ls = [synth.gen_layer(T, shape, seed=40 + i) for i in range(3)]
     cs = [Case(L, T, shape) for L in Ls]
@@ -150,8 +150,49 @@ def test_decode_layers_equal_the_moe_layer_chain(shape, T):
     ws = m.alloc_workspace(cs[0].shape, dev)
     y = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
     xn = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
-    for _ in range(2):   # twice: the ping-pong buffers and flags start from any state
+    for _ in range(3):   # repeated: the epochs and counters carry over between calls
         m.moe_decode_layers(cs[0].shape, table, x0, y, ws, x_next=xn)
         assert m.moe_query_device_status(ws) == 0
         assert np.array_equal(h16(y), y_chain)
         assert np.array_equal(h16(xn), xn_chain)
+
+
+def test_decode_layers_split_over_launches():
+    """More layers than one persistent launch runs (48): the normalised input
+    is handed from launch to launch, and the result is the chain's."""
+    dev = torch.device("cuda")
+    n, T = 50, 2
+    Ls = [synth.gen_layer(T, NOSH, seed=100 + i) for i in range(n)]
+    cs = [Case(L, T, NOSH) for L in Ls]
+    x0 = cs[0].x.clone()
+    for i, c in enumerate(cs):
+        if i:
+            c.x.copy_(cs[i - 1].x_next)
+        c.run_layer(x_next=True)
+    table = m.decode_layer_table([(c.wr, c.bias, c.ex, c.sh) for c in cs])
+    ws = m.alloc_workspace(cs[0].shape, dev)
+    y = torch.zeros((T, NOSH.H), dtype=torch.int16, device=dev)
+    xn = torch.zeros((T, NOSH.H), dtype=torch.int16, device=dev)
+    m.moe_decode_layers(cs[0].shape, table, x0, y, ws, x_next=xn)
+    assert m.moe_query_device_status(ws) == 0
+    assert np.array_equal(h16(y), h16(cs[-1].y))
+    assert np.array_equal(h16(xn), h16(cs[-1].x_next))
+
+
+def test_decode_layers_share_a_workspace_with_single_layers():
+    """moe_layer_w4 calls between moe_decode_layers calls on one workspace
+    leave the stacked result unchanged."""
+    dev = torch.device("cuda")
+    T = 1
+    Ls = [synth.gen_layer(T, TINY, seed=60 + i) for i in range(4)]
+    cs = [Case(L, T, TINY) for L in Ls]
+    table = m.decode_layer_table([(c.wr, c.bias, c.ex, c.sh) for c in cs])
+    ws = cs[0].ws
+    y = torch.zeros((T, TINY.H), dtype=torch.int16, device=dev)
+    m.moe_decode_layers(cs[0].shape, table, cs[0].x, y, ws)
+    y0 = h16(y).copy()
+    for _ in range(3):
+        cs[0].run_layer(x_next=True)
+        m.moe_decode_layers(cs[0].shape, table, cs[0].x, y, ws)
+        assert m.moe_query_device_status(ws) == 0
+        assert np.array_equal(h16(y), y0)
