@@ -319,17 +319,24 @@ class GpuWorkload:
         self.xa = torch.empty((T, S.H), dtype=torch.int16, device=dev)
         self.xb = torch.empty((T, S.H), dtype=torch.int16, device=dev)
         self.y_out = torch.empty((T * self.n_chunks, S.H), dtype=torch.int16, device=dev)
-        self.fused = m.moe_layer_path(self.shape) == 1
+        self.path = m.moe_layer_path(self.shape)
+        self.fused = self.path in (1, 2)
+        self.persistent = self.path == 2
         self.table = m.decode_layer_table(self.layers) if self.fused else None
 
-    def calls_per_layer(self):
-        # fused decode: route, gate_up, down; else route: 2 kernels, plan: 2, ffn: 2, combine: 1
-        return 3 if self.fused else 7  # per layer
+    def launches_per_step(self):
+        """Kernel launches of one step: the persistent decode kernel runs up
+        to 48 layers per launch; the per-layer decode path launches route,
+        gate_up, down per layer; otherwise route 2, plan 2, ffn 2, combine 1."""
+        calls = self.n_chunks * len(self.layers)
+        if self.persistent:
+            return -(-len(self.layers) // 48)
+        return (3 if self.fused else 7) * calls
 
     def capture(self):
-        """CUDA graphs of the device step and of the host-buffer step (decode:
-        120 launches of about a microsecond each, so the host's launch rate
-        would otherwise set the pace)."""
+        """CUDA graphs of the device step and of the host-buffer step (the
+        host's launch rate would otherwise add to a step of well under a
+        millisecond: copies, the decode launch, the read-back)."""
         torch = self.torch
         self.x_pin = torch.from_numpy(self.x_host.view(np.int16)).pin_memory()
         self.y_pin = torch.empty((self.tokens_per_step, self.S.H), dtype=torch.int16).pin_memory()
@@ -466,7 +473,9 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     ms = t0.elapsed_time(t1)
-    if G.fused:  # the unit is one layer call of the graph (3 kernels)
+    if G.persistent:  # the unit is one launch of the persistent kernel (all layers)
+        ffn_ms = ms / args.steps / G.launches_per_step()
+    elif G.fused:  # the unit is one layer call of the graph (3 kernels)
         ffn_ms = ms / args.steps / len(G.layers)
     else:
         ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
@@ -531,7 +540,9 @@ def run_ours(args, wl):
                  "hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
                  "tensor_frac": round(step_flops / (ms_step / 1e3) / 1e12 / bf16s, 4),
                  "touched_experts": int((counts > 0).sum()), "max_group": int(counts.max())},
-        "roofline": ({"kernel": "moe_decode_layers chain (dec_route, dec_gate_up, dec_down)"
+        "roofline": ({"kernel": "dec_persist_kernel: %d layers in one cooperative launch"
+                                % len(G.layers)} if G.persistent else
+                     {"kernel": "moe_decode_layers chain (dec_route, dec_gate_up, dec_down)"
                                 " per layer, CUDA graph of %d layers" % len(G.layers)}
                      if G.fused else
                      {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)"}),
@@ -543,12 +554,14 @@ def run_ours(args, wl):
                 "mode": "CUDA graph of the moe_decode_layers call and copies" if G.fused
                         else "moe_layer_w4 calls",
                 "eager_value": round(job_throughput(G.tokens_per_step, world, e_eager_ms), 2)},
-        "gpu_launches": G.calls_per_layer() * calls * args.steps,
-        "launch_mode": "CUDA graph replay, programmatic dependent launch" if G.fused
-                       else "eager stream launches",
+        "gpu_launches": G.launches_per_step() * args.steps,
+        "launch_mode": ("CUDA graph replay of one cooperative launch per step" if G.persistent
+                        else "CUDA graph replay, programmatic dependent launch" if G.fused
+                        else "eager stream launches"),
         "clocks": clocks,
     }
-    unit_bytes = algo_bytes if G.fused else ffn_bytes
+    unit_bytes = (algo_bytes * len(G.layers) // G.launches_per_step() if G.persistent
+                  else algo_bytes if G.fused else ffn_bytes)
     unit_gbs = unit_bytes / (ffn_ms / 1e3) / 1e9
     line["roofline"].update({"bound": "hbm", "achieved": round(unit_gbs, 1), "peak": hbm,
                              "peak_source": src, "unit": "GB/s",

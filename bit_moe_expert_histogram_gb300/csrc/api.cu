@@ -334,6 +334,10 @@ size_t moe_workspace_bytes(const moe_shape_t* shape) {
 
 int32_t moe_layer_path(const moe_shape_t* shape) {
   if (!shape_ok(shape)) return -1;
+  int grid = 0;
+  size_t smem = 0;
+  if (persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid, &smem))
+    return 2;
   return decode_supported(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared) ? 1 : 0;
 }
 

@@ -22,12 +22,12 @@
 //            routed expert (one token) or of the shared expert (all tokens),
 //            split along H over the 4 warps of a warp group; the partial
 //            sums meet in shared memory -> SwiGLU -> h. Each warp sends its
-//            down rows to L2 behind its first gate_up loads and loads them
-//            once its gate_up work is done, while h is awaited
-//   down     units (t, g, k): output rows 8g..8g+7 of token t times slot k's
-//            h, one warp each; the slots are weighted and summed in slot
-//            order (shared expert weight 1) -> bf16 y, and each row group's
-//            y^2 partial for the next normalisation
+//            down rows to L2 behind its first gate_up loads
+//   down     items (t, g, pair of slots): output rows 8g..8g+7 of token t
+//            for two slots, each times its slot's h, one warp each; the
+//            slots are weighted and summed in slot order (shared expert
+//            weight 1) -> bf16 y, and each row group's y^2 partial for the
+//            next normalisation
 //
 // The expert GEMVs run on the tensor cores (mma.sync m16n8k16, bf16 in,
 // fp32 accumulate) with the weights rebuilt exactly on the CUDA cores:
@@ -312,39 +312,51 @@ __device__ __forceinline__ void gu_batch_load(GuBatch& B, const uint32_t* q, con
 }
 
 // ---------------------------------------------------------------- down --
-// One down unit: output rows 8g..8g+7 of one slot, tile row g = output
-// row 8g+g over the first half of I, tile row g+8 the same row over the
-// second half; B column 0 = h's first half, column 1 its second half.
-// Lane c keeps the scale | bias << 16 of segments c, c+4, .. of both
-// halves; the other lanes of the row fetch them by shuffle.
+// One down item: output rows 8g..8g+7 of two slots k1, k2 (k2 may be
+// absent): tile row g is slot k1's weight row 8g+g, tile row g+8 slot k2's
+// same row, over all of I; B column 0 is h of slot k1, column 1 h of k2.
+// Lane c keeps the scale | bias << 16 of segments c, c+4, .. of both rows;
+// the other lanes of the row fetch them by shuffle.
 template <int I>
 struct DownUnit {
-  static constexpr int kSeg = I / 128;                  // segments per half
+  static constexpr int kSeg = I / 64;                   // segments per row
   static constexpr int kOwn = kSeg > 4 ? kSeg / 4 : 1;  // segments whose scales a lane keeps
   uint2 wg[kSeg], wh[kSeg];
   uint32_t sg[kOwn], sh[kOwn];
 };
 
+// Row rowg of wtg (slot k1) and, if wth, row rowh of wth (slot k2; else
+// zero weights).
 template <int I>
-__device__ __forceinline__ void down_load(DownUnit<I>& D, const moe_w4_weights_t& wt, size_t row,
-                                          int c) {
-  constexpr int kSeg = DownUnit<I>::kSeg, kOwn = DownUnit<I>::kOwn, kGrp = I / 64;
-  const uint32_t* q = wt.q_down_dev + row * (I / 8);
-  const uint16_t* s = wt.s_down_dev + row * kGrp;
-  const uint16_t* b = wt.b_down_dev + row * kGrp;
+__device__ __forceinline__ void down_load(DownUnit<I>& D, const moe_w4_weights_t& wtg, size_t rowg,
+                                          const moe_w4_weights_t* wth, size_t rowh, int c) {
+  constexpr int kSeg = DownUnit<I>::kSeg, kOwn = DownUnit<I>::kOwn;
+  const uint32_t* qg = wtg.q_down_dev + rowg * (I / 8);
 #pragma unroll
-  for (int i = 0; i < kSeg; ++i) {
-    D.wg[i] = __ldg(reinterpret_cast<const uint2*>(q + i * 8 + 2 * c));
-    D.wh[i] = __ldg(reinterpret_cast<const uint2*>(q + I / 16 + i * 8 + 2 * c));
-  }
+  for (int i = 0; i < kSeg; ++i) D.wg[i] = __ldg(reinterpret_cast<const uint2*>(qg + i * 8 + 2 * c));
 #pragma unroll
   for (int o = 0; o < kOwn; ++o) {
-    const int i = c + 4 * o;  // segment i of each half: groups i and kSeg + i
-    D.sg[o] = D.sh[o] = 0;
-    if (i < kSeg) {
-      D.sg[o] = (uint32_t)__ldg(s + i) | ((uint32_t)__ldg(b + i) << 16);
-      D.sh[o] = (uint32_t)__ldg(s + kSeg + i) | ((uint32_t)__ldg(b + kSeg + i) << 16);
+    const int i = c + 4 * o;
+    D.sg[o] = i < kSeg ? (uint32_t)__ldg(wtg.s_down_dev + rowg * kSeg + i) |
+                             ((uint32_t)__ldg(wtg.b_down_dev + rowg * kSeg + i) << 16)
+                       : 0u;
+  }
+  if (wth) {
+    const uint32_t* qh = wth->q_down_dev + rowh * (I / 8);
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) D.wh[i] = __ldg(reinterpret_cast<const uint2*>(qh + i * 8 + 2 * c));
+#pragma unroll
+    for (int o = 0; o < kOwn; ++o) {
+      const int i = c + 4 * o;
+      D.sh[o] = i < kSeg ? (uint32_t)__ldg(wth->s_down_dev + rowh * kSeg + i) |
+                               ((uint32_t)__ldg(wth->b_down_dev + rowh * kSeg + i) << 16)
+                         : 0u;
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) D.wh[i] = make_uint2(0u, 0u);
+#pragma unroll
+    for (int o = 0; o < kOwn; ++o) D.sh[o] = 0u;
   }
 }
 
@@ -388,7 +400,8 @@ __global__ void __launch_bounds__(kPsThreads, 1)
   const int nseg = H / (64 * kGuSlices);      // segments of a gate_up slice
   const int wg_ = warp / kGuSlices, qs = warp % kGuSlices;  // warp group, slice
   const int u0 = blockIdx.x + G * warp;       // the warp's first router unit
-  const int nit = nud * slots;                // down items of the block
+  const int npair = (slots + 1) / 2;          // slot pairs of a row group
+  const int nit = nud * npair;                // down items of the block
 
   for (int l = 0; l < a.n_layers; ++l) {
     const moe_layer_weights_t& Lw = a.layer[l];
@@ -473,35 +486,46 @@ __global__ void __launch_bounds__(kPsThreads, 1)
         a.w[i] = S.swt[i / K][i % K];
       }
     }
-    // the slot expert of down item it (recorded if the top-K gave none)
-    auto item_expert = [&](int it, int& t, int& rgp, int& k) -> size_t {
-      const int ud = it / slots;
-      k = it - ud * slots;
-      const int un = blockIdx.x + ud * G;
-      t = un / nb;
-      rgp = un - t * nb;
+    // down item it = (row group ud, slot pair p): slots 2p and 2p+1
+    auto slot_row = [&](int t, int k, int rgp) -> size_t {  // first weight row, by slot
       int e = k < K ? S.sid[t][k] : 0;
-      if (e < 0 || e >= E) {
+      if (e < 0 || e >= E) {  // not produced by the top-K; recorded, expert 0 read instead
         if (c == 0 && g == 0) set_error(ctrl, MOE_ERR_BAD_INPUT, KID_DECODE, e);
         e = 0;
       }
-      return (size_t)e;
+      return (size_t)e * H + (size_t)rgp * kPsGroup;
+    };
+    auto item_of = [&](int it, int& ud, int& t, int& rgp, int& k1) {
+      ud = it / npair;
+      k1 = 2 * (it - ud * npair);
+      const int un = blockIdx.x + ud * G;
+      t = un / nb;
+      rgp = un - t * nb;
+    };
+    auto load_item = [&](DownUnit<I>& D, int it) {
+      int ud, t, rgp, k1;
+      item_of(it, ud, t, rgp, k1);
+      const int k2 = k1 + 1;
+      down_load<I>(D, k1 < K ? Lw.experts : Lw.shared, slot_row(t, k1, rgp) + g,
+                   k2 < slots ? (k2 < K ? &Lw.experts : &Lw.shared) : nullptr,
+                   k2 < slots ? slot_row(t, k2, rgp) + g : 0, c);
     };
     // ------------------------------------------------------- gate_up --
-    // the warp's down rows go to L2 behind its first gate_up loads; they
-    // are loaded into registers after the gate_up work, while h is awaited
+    // the warp's down rows go to L2 behind its first gate_up loads
     bool pref = false;
     auto prefetch_down = [&]() {
       pref = true;
       if (lane != 0) return;
       for (int it = warp; it < nit; it += kPsWarps) {
-        int tt, rgp, kk;
-        const size_t ee = item_expert(it, tt, rgp, kk);
-        const moe_w4_weights_t& dw = kk < K ? Lw.experts : Lw.shared;
-        const size_t row0 = ee * H + (size_t)rgp * kPsGroup;
-        bulk_prefetch_l2(dw.q_down_dev + row0 * (I / 8), kPsGroup * (I / 2));
-        bulk_prefetch_l2(dw.s_down_dev + row0 * (I / 64), kPsGroup * (I / 64) * 2);
-        bulk_prefetch_l2(dw.b_down_dev + row0 * (I / 64), kPsGroup * (I / 64) * 2);
+        int ud, tt, rgp, k1;
+        item_of(it, ud, tt, rgp, k1);
+        for (int k = k1; k < k1 + 2 && k < slots; ++k) {
+          const moe_w4_weights_t& dw = k < K ? Lw.experts : Lw.shared;
+          const size_t row0 = slot_row(tt, k, rgp);
+          bulk_prefetch_l2(dw.q_down_dev + row0 * (I / 8), kPsGroup * (I / 2));
+          bulk_prefetch_l2(dw.s_down_dev + row0 * (I / 64), kPsGroup * (I / 64) * 2);
+          bulk_prefetch_l2(dw.b_down_dev + row0 * (I / 64), kPsGroup * (I / 64) * 2);
+        }
       }
     };
     for (int i = wg_, r = 0; ; i += kPsWarps / kGuSlices, ++r) {
@@ -579,12 +603,6 @@ __global__ void __launch_bounds__(kPsThreads, 1)
       }
     }
     if (!pref) prefetch_down();
-    DownUnit<I> D;
-    if (warp < nit) {
-      int tt, rgp, kk;
-      const size_t ee = item_expert(warp, tt, rgp, kk);
-      down_load<I>(D, kk < K ? Lw.experts : Lw.shared, ee * H + (size_t)rgp * kPsGroup + g, c);
-    }
     // ------------------------------------------------------------ down --
     // h of every slot -> shared memory (pair layout: the tagged words' order)
     // word i of the pair layout: row (t, k) = i / (I/2), pair word m = i % (I/2)
@@ -598,12 +616,13 @@ __global__ void __launch_bounds__(kPsThreads, 1)
         T * slots * (I / 2), ep, ctrl, 5, [&](int i, uint32_t v) { reinterpret_cast<uint32_t*>(hp)[i] = v; });
     __syncthreads();
     for (int it = warp; it < nit; it += kPsWarps) {
-      int t, rgp, k;
-      const size_t e = item_expert(it, t, rgp, k);
-      if (it != warp) down_load<I>(D, k < K ? Lw.experts : Lw.shared, e * H + (size_t)rgp * kPsGroup + g, c);
-      // B: lanes of group 0 the first half of h, group 1 the second half
-      const bool bact = g < 2;
-      const uint4* hb = hp + ((size_t)t * slots + k) * (I / 8) + (g == 1 ? I / 16 : 0);
+      int ud, t, rgp, k1;
+      item_of(it, ud, t, rgp, k1);
+      DownUnit<I> D;  // L2 hits: prefetched during the gate_up work
+      load_item(D, it);
+      // B: lanes of group 0 h of slot k1, group 1 h of slot k1 + 1
+      const bool bact = g == 0 || (g == 1 && k1 + 1 < slots);
+      const uint4* hb = hp + ((size_t)t * slots + k1 + (g == 1 ? 1 : 0)) * (I / 8);
       float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i2 = 0; i2 < DownUnit<I>::kSeg; ++i2) {
@@ -615,8 +634,12 @@ __global__ void __launch_bounds__(kPsThreads, 1)
         const uint32_t sh = __shfl_sync(0xFFFFFFFFu, D.sh[i2 >> 2], src);
         mma_segment(d0, d1, D.wg[i2], D.wh[i2], sg, sh, xa, xc);
       }
-      // output row 8 rgp + g: column 0 of tile row g plus column 1 of row g+8
-      if (c == 0) dsl[(size_t)it * kPsGroup + g] = (d0[0] + d1[0]) + (d0[3] + d1[3]);
+      // output row 8 rgp + g: slot k1 in column 0 of tile row g, slot k1+1
+      // in column 1 of tile row g+8
+      if (c == 0) {
+        dsl[((size_t)ud * slots + k1) * kPsGroup + g] = d0[0] + d1[0];
+        if (k1 + 1 < slots) dsl[((size_t)ud * slots + k1 + 1) * kPsGroup + g] = d0[3] + d1[3];
+      }
     }
     __syncthreads();
     // y = sum_k w_k d_k (slot order) + d_shared; one warp per row group, lane

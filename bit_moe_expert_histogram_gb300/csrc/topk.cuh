@@ -26,6 +26,26 @@ __device__ __forceinline__ unsigned long long topk_ckey(float v, int e) {
   return ((unsigned long long)topk_key(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
 }
 
+// Slots 0..K-1 of sel hold the selected composite keys in order: writes
+// ids[k] and the renormalised softmax weights w[k] = exp(l_k - l_0) / z,
+// z summed over the slots by an xor butterfly of the warp's lanes (slot k
+// on lane k). Whole warp.
+__device__ __forceinline__ void topk_emit(const unsigned long long* sel, int K, int lane,
+                                          int32_t* ids, float* w) {
+  const unsigned long long mine = lane < K ? sel[lane] : 0ull;
+  const float my_l = topk_value((uint32_t)(mine >> 32));
+  const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
+  const float ex = (lane < K) ? expf(my_l - l0) : 0.0f;
+  float z = ex;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
+  if (lane < K) {
+    ids[lane] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+    w[lane] = ex / z;
+  }
+  __syncwarp();
+}
+
 // Per-warp scratch of topk_warp in shared memory, for at most CAP
 // candidates (CAP >= E).
 template <int CAP>
@@ -87,18 +107,7 @@ __device__ __forceinline__ void topk_warp_vals(const float (&v)[NMAX], int E, in
     if (rk < K) S.sel[rk] = ci;
   }
   __syncwarp();
-  const unsigned long long mine = lane < K ? S.sel[lane] : 0ull;
-  const float my_l = topk_value((uint32_t)(mine >> 32));
-  const float l0 = __shfl_sync(0xFFFFFFFFu, my_l, 0);
-  const float ex = (lane < K) ? expf(my_l - l0) : 0.0f;
-  float z = ex;
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
-  if (lane < K) {
-    ids[lane] = (int)(0xFFFFFFFFu - (uint32_t)mine);
-    w[lane] = ex / z;
-  }
-  __syncwarp();
+  topk_emit(S.sel, K, lane, ids, w);
 }
 
 template <int CAP, int NMAX>

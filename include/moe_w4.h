@@ -184,15 +184,17 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
                           int32_t* topk_ids_dev, float* topk_w_dev, void* ws_dev,
                           size_t ws_bytes, moe_stream_t stream);
 
-/* Which kernels moe_layer_w4 runs for `shape`: 1 = the fused decode
- * kernels, 0 = the four calls above (route, plan, grouped GEMMs, combine),
- * -1 = unsupported shape. The decode kernels take T <= 4 with E <= 256,
- * I one of 128, 256, 512, 1024, K + n_shared <= 33 and T*H*2 + 10240 <=
- * 49152 (the activations and the top-K scratch in one block's shared
- * memory). Host only; enqueues nothing. The decode kernels
- * are launched with programmatic stream serialisation: a layer may start
- * while the work before it in the stream finishes, but it reads nothing
- * that work writes before that work has completed. */
+/* Which kernels moe_layer_w4 and moe_decode_layers run for `shape` on the
+ * current device: 2 = the persistent decode kernel (T <= 4, T*H <= 8192,
+ * E <= 256, I one of 128, 256, 512, 1024, K + n_shared <= 33, and one block
+ * of 512 threads with the shape's shared memory fits an SM), 1 = the three
+ * decode kernels per layer (the same limits but T*H*2 + 10240 <= 49152 in
+ * place of T*H <= 8192, when the persistent kernel does not fit), 0 = the
+ * four calls above (route, plan, grouped GEMMs, combine), -1 = unsupported
+ * shape. Host only; enqueues nothing. The three decode kernels are
+ * launched with programmatic stream serialisation: a layer may start while
+ * the work before it in the stream finishes, but it reads nothing that
+ * work writes before that work has completed. */
 int32_t moe_layer_path(const moe_shape_t* shape);
 
 /* One stacked layer's weights for moe_decode_layers. */

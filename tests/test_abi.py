@@ -52,17 +52,19 @@ def test_workspace_and_block_bounds(lib):
 
 
 def test_layer_path_choice(lib):
-    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 512, 1, 128)) == 1
-    assert m.moe_layer_path(m.make_shape(4, 2048, 256, 8, 512, 1, 128)) == 1
+    # 2 (persistent kernel) needs a device that holds its blocks; without one, 1
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 512, 1, 128)) in (1, 2)
+    assert m.moe_layer_path(m.make_shape(4, 2048, 256, 8, 512, 1, 128)) in (1, 2)
     assert m.moe_layer_path(m.make_shape(5, 2048, 256, 8, 512, 1, 128)) == 0
     assert m.moe_layer_path(m.make_shape(512, 2048, 256, 8, 512, 1, 128)) == 0
-    assert m.moe_layer_path(m.make_shape(1, 8192, 256, 8, 512, 1, 128)) == 1
+    assert m.moe_layer_path(m.make_shape(1, 8192, 256, 8, 512, 1, 128)) in (1, 2)
+    assert m.moe_layer_path(m.make_shape(2, 8192, 256, 8, 512, 1, 128)) == 1   # T*H > 8192
     assert m.moe_layer_path(m.make_shape(4, 8192, 256, 8, 512, 1, 128)) == 0   # 64 KiB of x
     assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 384, 1, 128)) == 0   # I not 2^n
     assert m.moe_layer_path(m.make_shape(1, 2048, 256, 8, 2048, 1, 128)) == 0  # I > 1024
     assert m.moe_layer_path(m.make_shape(1, 2048, 1024, 32, 512, 1, 128)) == 0  # E > 256
     assert m.moe_layer_path(m.make_shape(1, 2048, 512, 8, 512, 1, 128)) == 0    # E > 256
-    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 32, 1024, 1, 128)) == 1  # 33 slots
+    assert m.moe_layer_path(m.make_shape(1, 2048, 256, 32, 1024, 1, 128)) in (1, 2)  # 33 slots
     assert m.moe_layer_path(m.make_shape(0, 2048, 256, 8, 512, 1, 128)) == -1
 
 

@@ -196,3 +196,37 @@ def test_decode_layers_share_a_workspace_with_single_layers():
         m.moe_decode_layers(cs[0].shape, table, cs[0].x, y, ws)
         assert m.moe_query_device_status(ws) == 0
         assert np.array_equal(h16(y), y0)
+
+
+WIDE = synth.LayerShape(H=8192, E=16, K=2, I=128, n_shared=1)
+
+
+def test_layer_path_on_the_device():
+    """The decode shapes take the persistent kernel; T*H > 8192 the three
+    per-layer kernels."""
+    for T in (1, 2, 3, 4):
+        assert m.moe_layer_path(m.make_shape(T, FULL.H, FULL.E, FULL.K, FULL.I, FULL.n_shared, 128)) == 2
+    assert m.moe_layer_path(m.make_shape(1, TINY.H, TINY.E, TINY.K, TINY.I, TINY.n_shared, 128)) == 2
+    assert m.moe_layer_path(m.make_shape(2, WIDE.H, WIDE.E, WIDE.K, WIDE.I, WIDE.n_shared, 128)) == 1
+
+
+def test_per_layer_decode_kernels_wide_hidden():
+    """The three-kernel decode path (taken when the persistent kernel does
+    not hold the shape): one layer against the oracle, and stacked layers
+    against the chain of single layers."""
+    T = 2
+    Ls = [synth.gen_layer(T, WIDE, seed=80 + i) for i in range(3)]
+    cs = [Case(L, T, WIDE) for L in Ls]
+    for i, c in enumerate(cs):
+        if i:
+            c.x.copy_(cs[i - 1].x_next)
+        c.run_layer(x_next=True)
+        check_layer(c, Ls[i], h16(c.x))
+    table = m.decode_layer_table([(c.wr, c.bias, c.ex, c.sh) for c in cs])
+    dev = torch.device("cuda")
+    ws = m.alloc_workspace(cs[0].shape, dev)
+    y = torch.zeros((T, WIDE.H), dtype=torch.int16, device=dev)
+    x0 = d16(Ls[0].x[:T], dev)
+    m.moe_decode_layers(cs[0].shape, table, x0, y, ws)
+    assert m.moe_query_device_status(ws) == 0
+    assert np.array_equal(h16(y), h16(cs[-1].y))
