@@ -49,7 +49,7 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 
 struct Layout {
   size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
-      rpart, part2, ybuf, tags, xmid, total;
+      rpart, part2, ybuf, tags, xmid, xs, total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -75,6 +75,7 @@ Layout layout_of(const moe_shape_t* s) {
   L.bmap = take((size_t)max_blocks_of(s) * 12);
   L.nblk = take(4);
   L.yslots = take(S * (size_t)s->H * 2);
+  L.xs = take(S * (size_t)s->H * 2);  // the grouped GEMM's activations in plan order
   L.part = take(decode_part_floats(s->T, s->H) * 4);
   L.rpart = route_tc_supported(s->T, s->H, s->E, s->K)
                 ? take(route_tc_partial_floats(s->T, s->H, s->E) * 4)
@@ -204,7 +205,12 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
                  (uint64_t)E * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_gate_up_dev, H / 8,
                  (uint64_t)(s->n_shared ? 1 : E) * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, 64, 1,
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
+  cudaError_t ge = launch_gather_x(static_cast<const uint16_t*>(x), plan->sorted_rows_dev, K, R, S,
+                                   T, H, xs, ctrl, nsm, stream);
+  if (ge != cudaSuccess) return cuda_fail(ge, "activation gather launch");
+  // operand rows: boxes of 16 rows x 64 elements
+  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, S, 64, 16,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   FfnArgs a{};
   a.block_map = plan->block_map_dev;
@@ -234,7 +240,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
                  wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_down_dev, I / 8,
                  (uint64_t)(s->n_shared ? 1 : E) * H, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-  MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, 1,
+  MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, 16,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   a.sorted_rows = nullptr;
   a.rows_per_expert = H;

@@ -25,8 +25,10 @@
 //                 the CTA through a small shared-memory queue, and loads the
 //                 packed nibble tiles by TMA, 128 rows x 128 B (256 reduction
 //                 elements) per matrix, 128-byte swizzle
-//   warp 1        B producer: the entry's activation rows, 64 elements each,
-//                 gathered four rows per TMA (tile::gather4, 128-byte swizzle)
+//   warp 1        B producer: the entry's activation rows, consecutive in
+//                 the plan-ordered operand (x gathered by gather_x_kernel,
+//                 or h), loaded as TMA tiles of 16 rows x 64 elements
+//                 (128-byte swizzle)
 //   warp 2        TMEM allocator and MMA issuer (one thread)
 //   warps 4..7    epilogue: tcgen05.ld of the fp32 accumulators, released as
 //                 soon as they are in registers, then SwiGLU (or plain) -> bf16
@@ -35,7 +37,7 @@
 // Rings: kNW shared-memory W stages (freed by the dequant warps once read,
 // behind a proxy fence); kNS slots of kKS reduction elements, each a
 // shared-memory B stage plus a TMEM A stage, filled under one barrier (the
-// dequant warps' arrivals and the B gathers' bytes) and freed together by
+// dequant warps' arrivals and the B tiles' bytes) and freed together by
 // one MMA commit, so the MMA thread synchronises once per 16 MMAs; one
 // accumulator pair (freed by the epilogue). Roles that mostly wait sleep in their barrier waits. Every
 // wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains what
@@ -106,14 +108,6 @@ __device__ __forceinline__ uint2 load_groups(const uint16_t* row, int g0, int kg
   v.x = __ldg(reinterpret_cast<const unsigned int*>(row + g0));
   v.y = (g0 + 2 < kgroups) ? __ldg(reinterpret_cast<const unsigned int*>(row + g0 + 2)) : 0u;
   return v;
-}
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tm), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
@@ -264,6 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- B producer --
+    // activation rows are read again by the unit's other weight tiles
+    const uint64_t bpol = policy_evict_last();
     uint32_t it = 0, uc = 0;
     int u = -1;
     while (ok) {
@@ -273,15 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (u < 0) break;
       const Unit t = load_unit(a, u);
-      const int ngroups = (t.nrows + 3) >> 2;  // gather4 groups of rows
-      int src[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = min(4 * lane + j, t.nrows - 1);  // pad with the last row
-        const int r = t.row0 + n;
-        src[j] = GATED ? (r < a.R ? a.sorted_rows[r] / a.K : r - a.R) : r;
-      }
-      const uint32_t bytes = (uint32_t)ngroups * 4 * 128 * (kKS / kKA);
+      // the unit's rows are consecutive rows of the plan-ordered operand:
+      // boxes of 16 rows, one per lane and 64-wide atom (rows past the
+      // unit's are other units' or zero past the end; their columns are
+      // never read back)
+      const int nbox = (t.nrows + 15) >> 4;
+      const uint32_t bytes = (uint32_t)nbox * 16 * 128 * (kKS / kKA);
       for (int st = 0; st < bstages; ++st, ++it) {
         const int s = it % kNS;
         bool good = true;
@@ -292,11 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(b_sfull(s)), bytes);
         __syncwarp();
-        if (lane < ngroups) {
-#pragma unroll
-          for (int at = 0; at < kKS / kKA; ++at)
-            tma_gather4(sB + s * kBStage + at * kBAtom + lane * 512, &tm_b, st * kKS + at * kKA,
-                        src[0], src[1], src[2], src[3], bar(b_sfull(s)));
+        if (lane < nbox * (kKS / kKA)) {
+          const int bx = lane / (kKS / kKA), at = lane % (kKS / kKA);
+          tma_load_2d(sB + s * kBStage + at * kBAtom + bx * 16 * 128, &tm_b, st * kKS + at * kKA,
+                      t.row0 + 16 * bx, bar(b_sfull(s)), bpol);
         }
       }
     }
@@ -559,6 +551,38 @@ cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
 cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, const CUtensorMap& th,
                             const FfnArgs& a, int grid, cudaStream_t stream) {
   return launch_one<false>(tw, twsh, th, a, grid, stream);
+}
+
+// The grouped GEMM's activations in plan order: xs[p] = x[t(p)] for the
+// routed rows p < R (t = sorted_rows[p] / K) and x[p - R] for the shared
+// expert's rows, so a unit's rows are consecutive and load as plain TMA
+// tiles. A row index outside [0, T) is recorded and copied as zeros.
+__global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__ x,
+                                                       const int32_t* __restrict__ sorted_rows,
+                                                       int K, int R, int S, int T, int hv,
+                                                       uint4* __restrict__ xs, Ctrl* ctrl) {
+  const size_t n = (size_t)S * hv;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+    const int p = (int)(i / hv), c = (int)(i - (size_t)p * hv);
+    const int src = p < R ? __ldg(sorted_rows + p) / K : p - R;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (src >= 0 && src < T)
+      v = __ldg(x + (size_t)src * hv + c);
+    else if (c == 0)
+      set_error(ctrl, MOE_ERR_BAD_INPUT, KID_FFN, p);
+    xs[i] = v;
+  }
+}
+
+cudaError_t launch_gather_x(const uint16_t* x, const int32_t* sorted_rows, int K, int R, int S,
+                            int T, int H, uint16_t* xs, Ctrl* ctrl, int nsm, cudaStream_t stream) {
+  const size_t n = (size_t)S * (H / 8);
+  const size_t want = (n + 255) / 256;
+  const int grid = (int)(want < (size_t)nsm * 8 ? want : (size_t)nsm * 8);
+  gather_x_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(x), sorted_rows, K, R, S, T, H / 8, reinterpret_cast<uint4*>(xs),
+      ctrl);
+  return cudaGetLastError();
 }
 
 int ffn_tile_m() { return kTileM; }

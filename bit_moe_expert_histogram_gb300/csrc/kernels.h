@@ -17,7 +17,7 @@ constexpr int kPlanChunkNoalloc = 2048; // routed rows per plan block (moe_plan_
 struct FfnArgs {
   const int32_t* block_map;    // [max_blocks][3] (expert, row_start, nrows)
   const int32_t* num_blocks;   // device count of block-map entries
-  const int32_t* sorted_rows;  // gate_up: routed row -> f = t*K + k
+  const int32_t* sorted_rows;  // unused by the kernel (the operand rows come in plan order)
   int K;                       // experts per token
   int R;                       // routed rows (T*K)
   int E;                       // routed experts; entry expert E = shared
@@ -118,6 +118,10 @@ cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
                                cudaStream_t stream);
 cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, const CUtensorMap& th,
                             const FfnArgs& a, int grid, cudaStream_t stream);
+// xs[p] = x row of plan row p (routed rows through sorted_rows, then the
+// shared expert's rows in token order), S rows of H bf16
+cudaError_t launch_gather_x(const uint16_t* x, const int32_t* sorted_rows, int K, int R, int S,
+                            int T, int H, uint16_t* xs, Ctrl* ctrl, int nsm, cudaStream_t stream);
 cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, const float* w, int T,
                            int H, int K, int n_shared, uint16_t* y, uint16_t* x_next,
                            cudaStream_t stream);
