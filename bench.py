@@ -545,7 +545,8 @@ def run_ours(args, wl):
                      {"kernel": "moe_decode_layers chain (dec_route, dec_gate_up, dec_down)"
                                 " per layer, CUDA graph of %d layers" % len(G.layers)}
                      if G.fused else
-                     {"kernel": "moe_expert_ffn_w4 (gate_up+SwiGLU, down grouped GEMMs)"}),
+                     {"kernel": "moe_expert_ffn_w4 (activation gather, gate_up+SwiGLU and down "
+                                "grouped GEMMs)"}),
         "e2e": {"value": round(job_throughput(G.tokens_per_step, world, e_ms), 2),
                 "unit": "tokens/s",
                 "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
