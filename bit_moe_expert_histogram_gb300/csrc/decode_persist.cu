@@ -75,6 +75,7 @@ constexpr int kSegBatch = 8;    // 64-element segments of a gate_up slice in reg
 constexpr int kPsMaxT = 4;
 constexpr int kPsMaxE = 256;    // logits per lane in the top-K: 8
 constexpr int kPsMaxTH = 8192;  // T * H
+static_assert(kPsMaxTH / 8 <= 4 * 2 * 4 * 4 * 16, "the input phase's partials fit the reduction buffer");
 constexpr uint32_t kPsEpochStride = 64;  // epochs per launch (> kPersistMaxLayers)
 // Tagged words are grouped by writer, one 128-byte line (16 words) per
 // writer: a line that several SMs write while others poll it is handed
@@ -365,7 +366,9 @@ struct PsShared {
   int32_t sid[kPsMaxT][32];
   float swt[kPsMaxT][32];
   float xinv[kPsMaxT];
-  float red[kGuSlices][2][kGuSlices][kPsMaxT][16];  // [group][round parity][slice][column][row]
+  // gate_up partial sums [group][round parity][slice][column][row]; also
+  // the previous layer's y^2 partials during the input phase
+  float red[kGuSlices][2][kGuSlices][kPsMaxT][16];
   uint32_t seq;
 };
 
@@ -420,16 +423,27 @@ __global__ void __launch_bounds__(kPsThreads, 1)
       for (int i = threadIdx.x; i < T * H / 8; i += kPsThreads)
         xp[i] = to_pairs(__ldcg(xg + i));  // also the buffer x_next may name (written at the end)
     } else {
-      if (warp < T) {
-        const float inv = ps_rms_inv(a.y_tag + (size_t)warp * nb * kLine + 4, nb, H, ep - 1, lane, ctrl);
-        if (lane == 0) S.xinv[warp] = inv;
-      }
-      // y of the previous layer: tagged pairs in the activations' layout,
-      // normalised in place once every token's inv is known
+      // y of the previous layer and its y^2 partials in one poll: line g of
+      // token t holds four tagged pairs of y (the activations' layout) and
+      // the partial; y is normalised in place once every token's inv is known
       uint32_t* x32 = reinterpret_cast<uint32_t*>(xp);
+      float* part_s = &S.red[0][0][0][0][0];  // T*nb <= 1024 partials (red is free here)
       const int nw = T * H / 2;
-      poll_block([&](int i) { return a.y_tag + (size_t)(i >> 2) * kLine + (i & 3); }, nw, ep - 1,
-                 ctrl, 2, [&](int i, uint32_t v) { x32[i] = v; });
+      poll_block([&](int i) { return a.y_tag + (size_t)(i / 5) * kLine + (i % 5); }, nw / 4 * 5,
+                 ep - 1, ctrl, 2, [&](int i, uint32_t v) {
+                   const int line = i / 5, w = i - line * 5;
+                   if (w < 4)
+                     x32[line * 4 + w] = v;
+                   else
+                     part_s[line] = __uint_as_float(v);
+                 });
+      __syncthreads();
+      if (warp < T) {  // the partials summed as rms_inv_warp sums them
+        float sq = 0.0f;
+        for (int i = lane; i < nb; i += 32) sq += part_s[warp * nb + i];
+        sq = warp_sum(sq);
+        if (lane == 0) S.xinv[warp] = 1.0f / sqrtf(sq / (float)H + 1e-6f);
+      }
       __syncthreads();
       for (int i = threadIdx.x; i < nw; i += kPsThreads) {
         const float inv = S.xinv[i / (H / 2)];
