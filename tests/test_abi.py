@@ -131,3 +131,17 @@ def test_decode_layers_argument_errors(lib):
                                  None, 0, None) == m.MOE_ERR_INVALID_ARG
     assert lib.moe_decode_layers(C.byref(s), 1, None, None, None, None, None, 0,
                                  None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_of_the_chunked_prefill_fits_two_gib(lib):
+    """The chunked workload reuses one workspace per chunk of 2048 tokens;
+    it stays far below 2 GiB (the plan, h, the plan-ordered activations and
+    the slot outputs at T=2048)."""
+    s = m.make_shape(2048, 2048, 256, 8, 512, 1, 128)
+    n = m.moe_workspace_bytes(s)
+    assert 0 < n <= 2 << 30
+    # and it grows no faster than linearly in T: twice the tokens, at most
+    # twice the bytes plus the fixed part
+    n2 = m.moe_workspace_bytes(m.make_shape(4096, 2048, 256, 8, 512, 1, 128))
+    n1 = m.moe_workspace_bytes(m.make_shape(1, 2048, 256, 8, 512, 1, 128))
+    assert n2 <= 2 * n + n1
