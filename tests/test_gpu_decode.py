@@ -230,3 +230,37 @@ def test_per_layer_decode_kernels_wide_hidden():
     m.moe_decode_layers(cs[0].shape, table, x0, y, ws)
     assert m.moe_query_device_status(ws) == 0
     assert np.array_equal(h16(y), h16(cs[-1].y))
+
+
+SWEEP = [
+    (synth.LayerShape(H=512, E=100, K=4, I=256, n_shared=1), 1),
+    (synth.LayerShape(H=512, E=100, K=4, I=256, n_shared=1), 3),
+    (synth.LayerShape(H=1024, E=64, K=1, I=1024, n_shared=0), 2),
+    (synth.LayerShape(H=256, E=32, K=16, I=128, n_shared=1), 4),
+    (synth.LayerShape(H=2048, E=256, K=8, I=256, n_shared=1), 1),
+]
+
+
+@pytest.mark.parametrize("shape,T", SWEEP, ids=["E100-T1", "E100-T3", "K1-I1024-T2", "K16-T4", "I256-T1"])
+def test_persistent_decode_shape_sweep(shape, T):
+    """The persistent kernel across expert counts that are not a multiple of
+    32, top-1 and top-16, every intermediate size and no shared expert:
+    each layer against the oracle, the stacked call against the chain."""
+    assert m.moe_layer_path(m.make_shape(T, shape.H, shape.E, shape.K, shape.I,
+                                         shape.n_shared, 128)) == 2
+    Ls = [synth.gen_layer(T, shape, seed=120 + i) for i in range(2)]
+    cs = [Case(L, T, shape) for L in Ls]
+    for i, c in enumerate(cs):
+        if i:
+            c.x.copy_(cs[i - 1].x_next)
+        c.run_layer(x_next=True)
+        check_layer(c, Ls[i], h16(c.x))
+    dev = torch.device("cuda")
+    table = m.decode_layer_table([(c.wr, c.bias, c.ex, c.sh) for c in cs])
+    ws = m.alloc_workspace(cs[0].shape, dev)
+    y = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
+    xn = torch.zeros((T, shape.H), dtype=torch.int16, device=dev)
+    m.moe_decode_layers(cs[0].shape, table, d16(Ls[0].x[:T], dev), y, ws, x_next=xn)
+    assert m.moe_query_device_status(ws) == 0
+    assert np.array_equal(h16(y), h16(cs[-1].y))
+    assert np.array_equal(h16(xn), h16(cs[-1].x_next))
