@@ -55,6 +55,8 @@ def lib():
             L.orc_expert_ffn.argtypes = [P] * 6 + [i, i, P, i, P, P]
             L.orc_layer_tokens.argtypes = [P, i, i, i, i, P, P] + [P] * 12 + [P, i, P, P]
             L.orc_rmsnorm_rows.argtypes = [P, i, i, P]
+            L.orc_rmsnorm_gain_rows.argtypes = [P, P, i, i, P]
+            L.orc_residual_add.argtypes = [P, P, C.c_size_t, P]
             L.orc_num_threads.restype = i
             _lib = L
     return _lib
@@ -175,6 +177,38 @@ def rmsnorm_rows(y):
     out = np.empty_like(y)
     lib().orc_rmsnorm_rows(_p(y), T, H, _p(out))
     return out
+
+
+def rmsnorm_gain_rows(h, g):
+    """Pre-norm of the decoder block: bf16(g * h / sqrt(mean(h^2) + 1e-6))."""
+    h = _c(h, np.uint16)
+    g = _c(g, np.uint16)
+    T, H = h.shape
+    out = np.empty_like(h)
+    lib().orc_rmsnorm_gain_rows(_p(h), _p(g), T, H, _p(out))
+    return out
+
+
+def residual_add(h, y):
+    """The block's residual add: bf16(h + y), one rounding."""
+    h = _c(h, np.uint16)
+    y = _c(y, np.uint16)
+    out = np.empty_like(h)
+    lib().orc_residual_add(_p(h), _p(y), C.c_size_t(h.size), _p(out))
+    return out
+
+
+def decode_block(Ls, gains, h0, K):
+    """Stacked decoder blocks: for each layer x = rmsnorm_gain_rows(h, g),
+    y = the MoE layer on x (router, top-K, experts, combine), h = h + y.
+    Returns the last h and the last layer's ids."""
+    h = _c(h0, np.uint16)
+    ids = None
+    for L, g in zip(Ls, gains):
+        x = rmsnorm_gain_rows(h, g)
+        ids, _, w64 = topk(router_logits(x, L.w_router, L.router_bias), K)
+        h = residual_add(h, layer_tokens(L, ids, w64, x=x))
+    return h, ids
 
 
 def route(L, K):

@@ -414,6 +414,33 @@ void orc_rmsnorm_rows(const uint16_t* y, int T, int H, uint16_t* out) {
   }
 }
 
+/* The decoder block around an MoE layer (a reading: the pages name the
+ * model, Qwen3.6-35B-A3B, and its decode loop [P3 "Decode"], not the block
+ * arithmetic; the plainest pre-norm block is taken): the layer's input is
+ * the RMS normalisation of the residual stream h with a learned gain g,
+ *   x[n] = RNE_bf16( g[n] * h[n] / sqrt(mean_n(h[n]^2) + 1e-6) ),
+ * fp64 arithmetic, g and h bf16; the layer's output y is added back,
+ *   h'[n] = RNE_bf16( h[n] + y[n] ),
+ * one rounding of the exact sum. */
+void orc_rmsnorm_gain_rows(const uint16_t* h, const uint16_t* g, int T, int H, uint16_t* out) {
+  for (int t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int n = 0; n < H; ++n) {
+      double v = orc_bf16_value(h[(size_t)t * H + n]);
+      ss += v * v;
+    }
+    double inv = 1.0 / sqrt(ss / H + 1e-6);
+    for (int n = 0; n < H; ++n)
+      out[(size_t)t * H + n] =
+          orc_bf16_rne(orc_bf16_value(g[n]) * orc_bf16_value(h[(size_t)t * H + n]) * inv);
+  }
+}
+
+void orc_residual_add(const uint16_t* h, const uint16_t* y, size_t n, uint16_t* out) {
+  for (size_t i = 0; i < n; ++i)
+    out[i] = orc_bf16_rne(orc_bf16_value(h[i]) + orc_bf16_value(y[i]));
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

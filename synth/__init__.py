@@ -10,6 +10,8 @@ from .gen import (  # noqa: F401
     LayerInputs,
     bf16_bits,
     bf16_bits_to_f32,
+    gen_embed,
+    gen_gain,
     gen_layer,
     gen_tokens,
     zipf_router_bias,

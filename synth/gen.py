@@ -104,3 +104,15 @@ def gen_tokens(T, H, seed) -> np.ndarray:
     """Hidden states alone (a later decode step or prompt chunk)."""
     rng = np.random.default_rng(seed)
     return bf16_bits(rng.standard_normal((T, H)))
+
+
+def gen_gain(H, seed) -> np.ndarray:
+    """A learned RMSNorm gain: bf16 values 1 + 0.1 N(0, 1)."""
+    rng = np.random.default_rng(seed)
+    return bf16_bits(1.0 + 0.1 * rng.standard_normal(H))
+
+
+def gen_embed(V, H, seed) -> np.ndarray:
+    """A token embedding table: V rows of bf16 N(0, 1) values."""
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.standard_normal((V, H)))

@@ -299,3 +299,74 @@ def test_rmsnorm_closed_form():
     r = math.sqrt(25.0 / H + 1e-6)
     assert abs(out[1, 0] - 3 / r) <= 2 ** -8 * 3 / r and abs(out[1, 1] - 4 / r) <= 2 ** -8 * 4 / r
     assert (out[1, 2:] == 0).all()
+
+
+# ----------------------------------------------------- the decoder block --
+def test_rmsnorm_gain_constant_rows_return_the_gain():
+    """h constant c (|c| >> 1e-3): h / rms(h) = sign(c) (1 - ~5e-7 / c^2),
+    which rounds to 1, so each channel's output is its own gain exactly."""
+    H = 256
+    g = synth.gen_gain(H, seed=3)
+    h = np.zeros((2, H)); h[0, :] = 2.0; h[1, :] = -0.75
+    out = oracle.rmsnorm_gain_rows(synth.bf16_bits(h), g)
+    assert np.array_equal(out[0], g)
+    assert np.array_equal(out[1], g ^ np.uint16(0x8000))
+
+
+def test_rmsnorm_gain_of_ones_is_the_unit_normalisation():
+    h = synth.gen_tokens(3, 512, seed=4)
+    ones = synth.bf16_bits(np.ones(512))
+    assert np.array_equal(oracle.rmsnorm_gain_rows(h, ones), oracle.rmsnorm_rows(h))
+
+
+def test_rmsnorm_gain_is_per_channel():
+    """A one-hot gain keeps that channel of the unit normalisation alone; a
+    gain of 2 doubles every output exactly (scaling by 2 is exact in bf16)."""
+    H = 256
+    h = synth.gen_tokens(2, H, seed=5)
+    unit = synth.bf16_bits_to_f32(oracle.rmsnorm_rows(h))
+    onehot = np.zeros(H); onehot[37] = 1.0
+    out = synth.bf16_bits_to_f32(oracle.rmsnorm_gain_rows(h, synth.bf16_bits(onehot)))
+    assert np.array_equal(out[:, 37], unit[:, 37])
+    assert (np.delete(out, 37, axis=1) == 0).all()
+    g = synth.gen_gain(H, seed=6)
+    g2 = synth.bf16_bits(2.0 * synth.bf16_bits_to_f32(g))
+    a = synth.bf16_bits_to_f32(oracle.rmsnorm_gain_rows(h, g))
+    b = synth.bf16_bits_to_f32(oracle.rmsnorm_gain_rows(h, g2))
+    assert np.array_equal(b, 2.0 * a)
+
+
+def test_residual_add_ties_and_torch():
+    """bf16 has spacing 2^-7 at 1.0 and 2^-6 at 3.0: a half-spacing addend
+    is a tie (to the even neighbour), anything above it rounds away; a far
+    smaller addend vanishes; and random pairs match torch's bf16 addition
+    (fp32 sum, one rounding)."""
+    one = 1.0
+    cases = [(one, 2 ** -8, one), (one + 2 ** -7, 2 ** -8, one + 2 ** -6),
+             (one, 2 ** -8 + 2 ** -15, one + 2 ** -7), (one, 2 ** -30, one),
+             (1.5, -1.5, 0.0), (-3.0, 2 ** -7, -3.0),
+             (-3.0, 2 ** -7 + 2 ** -14, -3.0 + 2 ** -6)]
+    h = synth.bf16_bits(np.array([c[0] for c in cases]))
+    y = synth.bf16_bits(np.array([c[1] for c in cases]))
+    out = synth.bf16_bits_to_f32(oracle.residual_add(h, y)).astype(np.float64)
+    assert np.array_equal(out, np.array([c[2] for c in cases]))
+    rng = np.random.default_rng(7)
+    a = synth.bf16_bits(rng.standard_normal(4096) * 10.0 ** rng.integers(-3, 3, 4096))
+    b = synth.bf16_bits(rng.standard_normal(4096))
+    ta = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    tb = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    ref = (ta + tb).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.residual_add(a, b), ref)
+
+
+def test_decode_block_zero_layer_keeps_the_residual_stream():
+    """A layer whose experts rebuild to zero (scale and bias 0) outputs y = 0,
+    so the block returns its input unchanged, whatever the gain."""
+    shape = synth.LayerShape(H=256, E=8, K=2, I=128, n_shared=1)
+    L = synth.gen_layer(3, shape, seed=8)
+    for name in ("s_down", "b_down", "sh_s_down", "sh_b_down"):
+        getattr(L, name)[...] = 0
+    h0 = synth.gen_tokens(3, 256, seed=9)
+    h, ids = oracle.decode_block([L], [synth.gen_gain(256, seed=10)], h0, 2)
+    assert np.array_equal(h, h0)
+    assert ids.shape == (3, 2)
