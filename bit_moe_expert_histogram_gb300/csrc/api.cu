@@ -80,14 +80,16 @@ Layout layout_of(const moe_shape_t* s) {
   L.rpart = route_tc_supported(s->T, s->H, s->E, s->K)
                 ? take(route_tc_partial_floats(s->T, s->H, s->E) * 4)
                 : off;
-  // stacked decode: a second partial buffer and two y buffers (ping-pong)
+  // stacked decode: a second partial buffer and two y buffers (ping-pong;
+  // decoder blocks hand the residual stream between persistent launches
+  // through them too)
   const bool dec = decode_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
+  const bool ps = persist_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
   L.part2 = dec ? take(decode_part_floats(s->T, s->H) * 4) : off;
-  L.ybuf = dec ? take((size_t)2 * T * s->H * 2) : off;
+  L.ybuf = (dec || ps) ? take((size_t)2 * T * s->H * 2) : off;
   // persistent decode: the epoch-tagged block-to-block words, and the
   // normalised input handed from one launch of up to kPersistMaxLayers
   // layers to the next
-  const bool ps = persist_supported(s->T, s->H, s->E, s->K, s->I, s->n_shared);
   L.tags = ps ? take(persist_tags(s->T, s->H, s->E, s->K, s->I, s->n_shared).total * 8) : off;
   L.xmid = ps ? take(T * (size_t)s->H * 2) : off;
   L.total = off;
@@ -324,6 +326,51 @@ moe_status_t decode_persistent(const moe_shape_t* s, int n_layers,
   return MOE_OK;
 }
 
+// Decoder blocks through the persistent kernel, 48 layers per launch; the
+// residual stream passes between launches through the two ybuf halves.
+moe_status_t decode_block_persistent(const moe_shape_t* s, int n_layers,
+                                     const moe_layer_weights_t* layers,
+                                     const void* const* gains, const void* h_in,
+                                     const int32_t* tok, const void* embed, int vocab,
+                                     void* h_out, uint8_t* ws, const Layout& L, int grid,
+                                     size_t smem, cudaStream_t stream) {
+  PersistArgs a{};
+  a.T = s->T;
+  a.H = s->H;
+  a.E = s->E;
+  a.K = s->K;
+  a.I = s->I;
+  a.ns = s->n_shared;
+  a.ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  a.w = reinterpret_cast<float*>(ws + L.w);
+  uint64_t* tags = reinterpret_cast<uint64_t*>(ws + L.tags);
+  const PersistTags tl = persist_tags(s->T, s->H, s->E, s->K, s->I, s->n_shared);
+  a.logits_tag = tags + tl.logits;
+  a.h_tag = tags + tl.h;
+  a.y_tag = tags + tl.y;
+  a.ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  a.block = 1;
+  a.vocab = vocab;
+  a.embed = static_cast<const uint16_t*>(embed);
+  uint16_t* mid[2] = {reinterpret_cast<uint16_t*>(ws + L.ybuf),
+                      reinterpret_cast<uint16_t*>(ws + L.ybuf) + (size_t)s->T * s->H};
+  for (int l0 = 0, c = 0; l0 < n_layers; l0 += kPersistMaxLayers, ++c) {
+    const int n = n_layers - l0 < kPersistMaxLayers ? n_layers - l0 : kPersistMaxLayers;
+    a.n_layers = n;
+    a.tok = l0 == 0 ? tok : nullptr;
+    a.x = l0 == 0 ? static_cast<const uint16_t*>(h_in) : mid[(c - 1) & 1];
+    a.y = l0 + n == n_layers ? static_cast<uint16_t*>(h_out) : mid[c & 1];
+    for (int i = 0; i < n; ++i) {
+      a.layer[i] = layers[l0 + i];
+      if (!s->n_shared) a.layer[i].shared = a.layer[i].experts;
+      a.gain[i] = static_cast<const uint16_t*>(gains[l0 + i]);
+    }
+    cudaError_t e = launch_decode_persist(a, grid, smem, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "persistent decode block launch");
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 namespace moe {
@@ -480,6 +527,39 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
   MOE_TRY(run_ffn(shape, x_dev, experts, shared, &plan, y_slots, ws, st));
   return moe_combine(shape, y_slots, plan.row_pos_dev, w, y_dev, x_next_dev, stream);
+}
+
+moe_status_t moe_decode_block(const moe_shape_t* shape, int32_t n_layers,
+                              const moe_layer_weights_t* layers_host,
+                              const void* const* gains_host, const void* h_in_dev,
+                              const int32_t* token_ids_dev, const void* embed_dev, int32_t vocab,
+                              void* h_out_dev, void* ws_dev, size_t ws_bytes,
+                              moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  int grid = 0;
+  size_t smem = 0;
+  if (!persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid,
+                      &smem, true))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n_layers < 1 || !layers_host || !gains_host || !h_out_dev || !aligned16(h_out_dev))
+    return MOE_ERR_INVALID_ARG;
+  if (token_ids_dev) {
+    if (!embed_dev || !aligned16(embed_dev) || vocab < 1) return MOE_ERR_INVALID_ARG;
+  } else if (!h_in_dev || !aligned16(h_in_dev)) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_layer_weights_t& lw = layers_host[l];
+    if (!lw.w_router_dev || !aligned16(lw.w_router_dev) || !weights_ok(&lw.experts))
+      return MOE_ERR_INVALID_ARG;
+    if (shape->n_shared && !weights_ok(&lw.shared)) return MOE_ERR_INVALID_ARG;
+    if (!gains_host[l] || !aligned16(gains_host[l])) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
+  return decode_block_persistent(shape, n_layers, layers_host, gains_host, h_in_dev,
+                                 token_ids_dev, embed_dev, vocab, h_out_dev,
+                                 static_cast<uint8_t*>(ws_dev), layout_of(shape), grid, smem,
+                                 (cudaStream_t)stream);
 }
 
 moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,

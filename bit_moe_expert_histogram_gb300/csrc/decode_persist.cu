@@ -14,7 +14,10 @@
 //   input    every block forms the layer input x in shared memory: layer 0
 //            the caller's x; layer l > 0 bf16(y * inv), y the previous
 //            layer's output and inv = 1/sqrt(mean(y^2) + 1e-6) from its
-//            y^2 partials
+//            y^2 partials. Decoder blocks (BLOCK): every block keeps the
+//            residual stream h in shared memory (layer 0: the caller's h or
+//            the tokens' embedding rows; later: the previous layer's
+//            h + y) and forms x = bf16(gain * (h * inv)) from it
 //   router   units (t, e): the fixed-order fp32 logit of the prefill router
 //            (so the selected ids are bit-identical with it)
 //   top-K    every block selects each token's experts itself
@@ -27,7 +30,8 @@
 //            for two slots, each times its slot's h, one warp each; the
 //            slots are weighted and summed in slot order (shared expert
 //            weight 1) -> bf16 y, and each row group's y^2 partial for the
-//            next normalisation
+//            next normalisation (BLOCK: y is added to h first, h' =
+//            bf16(h + y), and h' and its square partials go on)
 //
 // The expert GEMVs run on the tensor cores (mma.sync m16n8k16, bf16 in,
 // fp32 accumulate) with the weights rebuilt exactly on the CUDA cores:
@@ -376,7 +380,9 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int I>
+// BLOCK: decoder blocks (PersistArgs::block); a separate instantiation, so
+// the stacked chain keeps its own register allocation
+template <int I, bool BLOCK>
 __global__ void __launch_bounds__(kPsThreads, 1)
     dec_persist_kernel(const __grid_constant__ PersistArgs a) {
   extern __shared__ __align__(128) uint8_t dyn[];
@@ -392,6 +398,9 @@ __global__ void __launch_bounds__(kPsThreads, 1)
   uint4* hp = xp + (size_t)T * (H / 8);                      // [T][slots][I/8]
   float* dsl = reinterpret_cast<float*>(hp + (size_t)T * slots * (I / 8));  // [nud][slots][8]
   uint16_t* yv = reinterpret_cast<uint16_t*>(dsl + (size_t)nud * slots * kPsGroup);
+  // decoder blocks: the residual stream h of this layer, pair layout [T][H/8]
+  uint4* rp = reinterpret_cast<uint4*>(
+      (reinterpret_cast<uintptr_t>(yv + (size_t)nud * kPsGroup) + 15) & ~(uintptr_t)15);
   if (threadIdx.x == 0) S.seq = *reinterpret_cast<volatile unsigned*>(&ctrl->ps_seq);
   __syncthreads();
   const uint32_t base = S.seq * kPsEpochStride + 1u;
@@ -418,7 +427,69 @@ __global__ void __launch_bounds__(kPsThreads, 1)
       ps_router_load(R, wr + (size_t)(u0 % E) * H, H, lane);
       if (Lw.router_bias_dev) rbias = __ldg(Lw.router_bias_dev + u0 % E);
     }
-    if (l == 0) {
+    if (BLOCK) {
+      // decoder block: h_l (pair layout) in rp, then x = bf16(g * (h * inv))
+      uint32_t* r32 = reinterpret_cast<uint32_t*>(rp);
+      float* part_s = &S.red[0][0][0][0][0];
+      const int hv = H / 8;
+      if (l == 0) {  // h_0: the caller's h, or the tokens' embedding rows
+        for (int i = threadIdx.x; i < T * hv; i += kPsThreads) {
+          const int t = i / hv, q = i - t * hv;
+          const uint4* src = nullptr;
+          if (a.tok) {
+            const int id = __ldg(a.tok + t);
+            if (id >= 0 && id < a.vocab)
+              src = reinterpret_cast<const uint4*>(a.embed + (size_t)id * H) + q;
+            else if (q == 0 && blockIdx.x == 0)
+              set_error(ctrl, MOE_ERR_BAD_INPUT, KID_DECODE, id);
+          } else {
+            src = reinterpret_cast<const uint4*>(a.x) + i;
+          }
+          rp[i] = src ? to_pairs(__ldcg(src)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
+        if (warp < T) {  // sum of squares of token warp's h
+          float sq = 0.0f;
+          for (int i = lane; i < H / 2; i += 32) {
+            const uint32_t v = r32[warp * (H / 2) + i];
+            sq += bf_lo(v) * bf_lo(v);
+            sq += bf_hi(v) * bf_hi(v);
+          }
+          sq = warp_sum(sq);
+          if (lane == 0) S.xinv[warp] = 1.0f / sqrtf(sq / (float)H + 1e-6f);
+        }
+      } else {  // h_l and its square partials from the previous layer
+        poll_block([&](int i) { return a.y_tag + (size_t)(i / 5) * kLine + (i % 5); },
+                   T * H / 8 * 5, ep - 1, ctrl, 2, [&](int i, uint32_t v) {
+                     const int line = i / 5, w = i - line * 5;
+                     if (w < 4)
+                       r32[line * 4 + w] = v;
+                     else
+                       part_s[line] = __uint_as_float(v);
+                   });
+        __syncthreads();
+        if (warp < T) {
+          float sq = 0.0f;
+          for (int i = lane; i < nb; i += 32) sq += part_s[warp * nb + i];
+          sq = warp_sum(sq);
+          if (lane == 0) S.xinv[warp] = 1.0f / sqrtf(sq / (float)H + 1e-6f);
+        }
+      }
+      __syncthreads();
+      const uint4* gq = reinterpret_cast<const uint4*>(a.gain[l]);
+      for (int i = threadIdx.x; i < T * hv; i += kPsThreads) {
+        const int t = i / hv;
+        const float inv = S.xinv[t];
+        const uint4 gv = to_pairs(__ldg(gq + (i - t * hv)));
+        const uint4 hq = rp[i];
+        uint4 o;
+        o.x = pack_bf2(bf_lo(gv.x) * (bf_lo(hq.x) * inv), bf_hi(gv.x) * (bf_hi(hq.x) * inv));
+        o.y = pack_bf2(bf_lo(gv.y) * (bf_lo(hq.y) * inv), bf_hi(gv.y) * (bf_hi(hq.y) * inv));
+        o.z = pack_bf2(bf_lo(gv.z) * (bf_lo(hq.z) * inv), bf_hi(gv.z) * (bf_hi(hq.z) * inv));
+        o.w = pack_bf2(bf_lo(gv.w) * (bf_lo(hq.w) * inv), bf_hi(gv.w) * (bf_hi(hq.w) * inv));
+        xp[i] = o;
+      }
+    } else if (l == 0) {
       const uint4* xg = reinterpret_cast<const uint4*>(a.x);
       for (int i = threadIdx.x; i < T * H / 8; i += kPsThreads)
         xp[i] = to_pairs(__ldcg(xg + i));  // also the buffer x_next may name (written at the end)
@@ -668,6 +739,11 @@ __global__ void __launch_bounds__(kPsThreads, 1)
         for (int k = 0; k < K; ++k) acc = __fmaf_rn(S.swt[t][k], dr[k * kPsGroup], acc);
         if (ns) acc += dr[K * kPsGroup];
         yb = f2bf(acc);
+        if (BLOCK) {  // the residual add: h_{l+1} = bf16(h_l + y_l)
+          const uint32_t hw = reinterpret_cast<const uint32_t*>(
+              rp)[(size_t)t * (H / 2) + (size_t)rgp * 4 + (lane & 3)];
+          yb = f2bf(((lane >> 2) ? bf_hi(hw) : bf_lo(hw)) + __uint_as_float(yb << 16));
+        }
         const float yr = __uint_as_float(yb << 16);
         ysq = yr * yr;
         yv[ud * kPsGroup + lane] = (uint16_t)yb;
@@ -714,33 +790,44 @@ constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices];
 bool g_attr[kMaxDevices][4];
 
+template <int I, bool BLOCK>
+cudaError_t prepare_one(int dev, int optin) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, dec_persist_kernel<I, BLOCK>);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dec_persist_kernel<I, BLOCK>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              optin - (int)fa.sharedSizeBytes);
+}
+
 template <int I>
 cudaError_t prepare(int dev) {
   if (g_attr[dev][__builtin_ctz(I / 128)]) return cudaSuccess;
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, dec_persist_kernel<I>);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dec_persist_kernel<I>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           optin - (int)fa.sharedSizeBytes);
+  e = prepare_one<I, false>(dev, optin);
+  if (e == cudaSuccess) e = prepare_one<I, true>(dev, optin);
   if (e == cudaSuccess) g_attr[dev][__builtin_ctz(I / 128)] = true;
   return e;
 }
 
 template <int I>
-bool occupancy_ok(size_t smem) {
+bool occupancy_ok(size_t smem, bool block) {
   int occ = 0;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dec_persist_kernel<I>, kPsThreads,
-                                                       smem) == cudaSuccess &&
-         occ >= 1;
+  const cudaError_t e =
+      block ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dec_persist_kernel<I, true>,
+                                                            kPsThreads, smem)
+            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dec_persist_kernel<I, false>,
+                                                            kPsThreads, smem);
+  return e == cudaSuccess && occ >= 1;
 }
 
-size_t dyn_smem(int T, int H, int K, int I, int ns, int grid) {
+size_t dyn_smem(int T, int H, int K, int I, int ns, int grid, bool block) {
   const int slots = K + ns, nud = (T * (H / kPsGroup) + grid - 1) / grid;
   size_t b = (size_t)T * H * 2 + (size_t)T * slots * I * 2;
   b += (size_t)nud * slots * kPsGroup * 4 + (size_t)nud * kPsGroup * 2;
+  if (block) b = ((b + 15) & ~(size_t)15) + (size_t)T * H * 2;  // the residual stream
   return (b + 127) & ~(size_t)127;
 }
 
@@ -761,7 +848,8 @@ PersistTags persist_tags(int T, int H, int E, int K, int I, int ns) {
   return p;
 }
 
-bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t* smem) {
+bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t* smem,
+                    bool block) {
   if (!persist_supported(T, H, E, K, I, ns)) return false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -779,11 +867,11 @@ bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t
   int G = g_sms[dev];
   G = G < T * (H / kPsGroup) ? G : T * (H / kPsGroup);
   G = G < K * (I / 8) ? G : K * (I / 8);
-  const size_t s = dyn_smem(T, H, K, I, ns, G);
-  const bool ok = I == 128 ? occupancy_ok<128>(s)
-                  : I == 256 ? occupancy_ok<256>(s)
-                  : I == 512 ? occupancy_ok<512>(s)
-                             : occupancy_ok<1024>(s);
+  const size_t s = dyn_smem(T, H, K, I, ns, G, block);
+  const bool ok = I == 128 ? occupancy_ok<128>(s, block)
+                  : I == 256 ? occupancy_ok<256>(s, block)
+                  : I == 512 ? occupancy_ok<512>(s, block)
+                             : occupancy_ok<1024>(s, block);
   if (!ok) return false;
   *grid = G;
   *smem = s;
@@ -802,11 +890,19 @@ cudaError_t launch_decode_persist(const PersistArgs& a, int grid, size_t smem,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (a.block) {
+    switch (a.I) {
+      case 128: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<128, true>, a);
+      case 256: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<256, true>, a);
+      case 512: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<512, true>, a);
+      default: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<1024, true>, a);
+    }
+  }
   switch (a.I) {
-    case 128: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<128>, a);
-    case 256: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<256>, a);
-    case 512: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<512>, a);
-    default: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<1024>, a);
+    case 128: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<128, false>, a);
+    case 256: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<256, false>, a);
+    case 512: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<512, false>, a);
+    default: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<1024, false>, a);
   }
 }
 

@@ -84,6 +84,16 @@ struct PersistArgs {
   uint64_t* h_tag;      // line per gate_up tile: words 4 col + r = bf16 pair (h_r, h_r+4)
   uint64_t* y_tag;      // line t*(H/8)+g: words 0..3 = bf16 pairs (y_r, y_r+4), word 4 = y^2 partial
   Ctrl* ctrl;
+  // decoder blocks (moe_decode_block) when block != 0: layer l's input is
+  // bf16(gain[l] * h_l / rms(h_l)) and its output h_{l+1} = bf16(h_l + y_l)
+  // (y is then h, the residual stream; x_next must be null); h_0 is
+  // embed[tok[t]] when tok is set (ids outside [0, vocab) are recorded and
+  // read as zero rows), else x
+  int block;
+  const int32_t* tok;
+  const uint16_t* embed;
+  int vocab;
+  const uint16_t* gain[kPersistMaxLayers];
   moe_layer_weights_t layer[kPersistMaxLayers];
 };
 bool persist_supported(int T, int H, int E, int K, int I, int ns);
@@ -95,7 +105,9 @@ PersistTags persist_tags(int T, int H, int E, int K, int I, int ns);
 // Grid and dynamic shared memory of a launch on the current device; false
 // when the shape's blocks do not fit on it (the caller takes the per-layer
 // kernels then).
-bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t* smem);
+// block: room for the residual stream too (decoder blocks)
+bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t* smem,
+                    bool block = false);
 cudaError_t launch_decode_persist(const PersistArgs& a, int grid, size_t smem,
                                   cudaStream_t stream);
 

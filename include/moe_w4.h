@@ -230,6 +230,39 @@ moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
                                void* y_dev, void* x_next_dev, void* ws_dev, size_t ws_bytes,
                                moe_stream_t stream);
 
+/* n_layers decoder blocks around the MoE layers, for a few tokens (the
+ * residual stream of a decode step; the pre-norm and residual add are the
+ * plainest reading of the block around a layer of the pages' model, which
+ * they name but do not spell out; the token feed follows [Lily] "Decode":
+ * the chosen token goes straight into the next step's GPU-resident input).
+ * For l = 0 .. n_layers-1:
+ *   x_l     = bf16(gain_l[n] * h_l[n] / sqrt(mean_n(h_l[n]^2) + 1e-6))
+ *   y_l     = layer l on x_l (router, top-K, experts, combine, as
+ *             moe_layer_w4 computes them)
+ *   h_{l+1} = bf16(h_l + y_l)
+ * h_0 = embed_dev[token_ids_dev[t]] when token_ids_dev is not NULL (the
+ * tokens' embedding rows, gathered on the device, so a decode loop feeds
+ * each step's token ids from device memory with no host round trip; an id
+ * outside [0, vocab) is recorded as MOE_ERR_BAD_INPUT and reads as a zero
+ * row), else h_in_dev. Writes h_out_dev = h_{n_layers}.
+ * Runs the persistent decode kernel (one cooperative launch per 48 layers);
+ * a shape it cannot hold returns MOE_ERR_UNSUPPORTED_SHAPE (moe_layer_path
+ * tells which shapes it holds).
+ *  layers_host   n_layers host structs, as for moe_decode_layers
+ *  gains_host    n_layers device pointers, each bf16 [H], 16-byte aligned
+ *  h_in_dev      bf16 [T][H], or NULL when token_ids_dev is given
+ *  token_ids_dev int32 [T] or NULL
+ *  embed_dev     bf16 [vocab][H] (used with token_ids_dev)
+ *  h_out_dev     bf16 [T][H] out; may be h_in_dev
+ * The workspace is the layer's (moe_workspace_bytes), zero-filled by
+ * moe_workspace_init; the last layer's ids and weights are left in it. */
+moe_status_t moe_decode_block(const moe_shape_t* shape, int32_t n_layers,
+                              const moe_layer_weights_t* layers_host,
+                              const void* const* gains_host, const void* h_in_dev,
+                              const int32_t* token_ids_dev, const void* embed_dev, int32_t vocab,
+                              void* h_out_dev, void* ws_dev, size_t ws_bytes,
+                              moe_stream_t stream);
+
 /* moe_plan without a workspace: same inputs, same outputs, bit-identical
  * results. The pages have no counterpart; this entry point exists for
  * callers that cannot allocate device memory where they build the plan (code
