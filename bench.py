@@ -38,6 +38,7 @@ import synth  # noqa: E402
 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM = 6800.0
+BLOCK_VOCAB = 4096  # embedding rows of the decoder-block workload
 FALLBACK_BF16 = 1900.0
 
 
@@ -275,7 +276,7 @@ def job_throughput(tokens_per_rank_step, world, ms_per_step):
 
 # ---------------------------------------------------------- GPU arm --
 class GpuWorkload:
-    def __init__(self, wl, dev, m, tile_rows=128, rank=0):
+    def __init__(self, wl, dev, m, tile_rows=128, rank=0, block=False):
         import torch
         self.wl, self.dev, self.m, self.torch = wl, dev, m, torch
         S = wl.shape
@@ -325,6 +326,22 @@ class GpuWorkload:
         self.fused = self.path in (1, 2)
         self.persistent = self.path == 2
         self.table = m.decode_layer_table(self.layers) if self.fused else None
+        # decoder blocks (moe_decode_block): per-layer gains and the token
+        # feed from an embedding table, the step's token ids in device memory
+        self.block = bool(block)
+        self.h2d_bytes = self.tokens_per_step * S.H * 2
+        if self.block:
+            if not self.persistent:
+                raise ValueError("decoder blocks need the persistent decode kernel")
+            self.vocab = BLOCK_VOCAB
+            self.gains_d = [torch.from_numpy(synth.gen_gain(S.H, seed=l).view(np.int16)).to(dev)
+                            for l in range(nl)]
+            self.gains = m.gain_table(self.gains_d)
+            self.embed = torch.from_numpy(
+                synth.gen_embed(self.vocab, S.H, seed=77).view(np.int16)).to(dev)
+            self.tok_host = (np.arange(T, dtype=np.int32) * 7919 + 11 + rank) % self.vocab
+            self.tok = torch.from_numpy(self.tok_host).to(dev)
+            self.h2d_bytes = T * 4
 
     def launches_per_step(self):
         """Kernel launches of one step: the persistent decode kernel runs up
@@ -340,7 +357,8 @@ class GpuWorkload:
         host's launch rate would otherwise add to a step of well under a
         millisecond: copies, the decode launch, the read-back)."""
         torch = self.torch
-        self.x_pin = torch.from_numpy(self.x_host.view(np.int16)).pin_memory()
+        self.x_pin = (torch.from_numpy(self.tok_host).pin_memory() if self.block else
+                      torch.from_numpy(self.x_host.view(np.int16)).pin_memory())
         self.y_pin = torch.empty((self.tokens_per_step, self.S.H), dtype=torch.int16).pin_memory()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -361,6 +379,10 @@ class GpuWorkload:
         """One pass of the hot path over the step's tokens (device-resident)."""
         m, S, T = self.m, self.S, self.T
         nl = len(self.layers)
+        if self.block:  # every decoder block in one call, h_0 from the token ids
+            m.moe_decode_block(self.shape, self.table, self.gains, self.y_out, self.ws,
+                               token_ids=self.tok, embed=self.embed)
+            return
         if self.fused:  # every layer in one call (moe_decode_layers)
             m.moe_decode_layers(self.shape, self.table, self.x_all[:T], self.y_out, self.ws)
             return
@@ -385,6 +407,12 @@ class GpuWorkload:
         """The same through the public calls with host buffers copied in and out."""
         m, T = self.m, self.T
         nl = len(self.layers)
+        if self.block:
+            self.tok.copy_(x_pin[:T], non_blocking=True)
+            m.moe_decode_block(self.shape, self.table, self.gains, self.y, self.ws,
+                               token_ids=self.tok, embed=self.embed)
+            y_pin[:T].copy_(self.y, non_blocking=True)
+            return
         if self.fused:
             self.xa.copy_(x_pin[:T], non_blocking=True)
             m.moe_decode_layers(self.shape, self.table, self.xa, self.y, self.ws)
@@ -424,7 +452,7 @@ def run_ours(args, wl):
     import bit_moe_expert_histogram_gb300 as m
     m.load()
 
-    G = GpuWorkload(wl, dev, m, tile_rows=args.tile_rows, rank=rank)
+    G = GpuWorkload(wl, dev, m, tile_rows=args.tile_rows, rank=rank, block=args.block)
     counts = G.realised_counts()
     algo_bytes, flops, ffn_bytes, ffn_flops = layer_algo(G.T, wl.shape, counts)
     calls = G.n_chunks * len(G.layers)
@@ -489,7 +517,8 @@ def run_ours(args, wl):
 
     # e2e: host buffers in and out through moe_layer_w4 (decode: the same
     # calls and copies replayed from a CUDA graph; eager calls also reported)
-    x_pin = torch.from_numpy(G.x_host.view(np.int16)).pin_memory()
+    x_pin = (torch.from_numpy(G.tok_host).pin_memory() if G.block else
+             torch.from_numpy(G.x_host.view(np.int16)).pin_memory())
     y_pin = torch.empty((G.tokens_per_step, wl.shape.H), dtype=torch.int16).pin_memory()
     e_steps = max(3, min(args.steps, 50))
 
@@ -532,6 +561,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "T": wl.T, "layers": wl.layers,
                    "chunks": G.n_chunks, "H": wl.shape.H, "E": wl.shape.E, "K": wl.shape.K,
                    "I": wl.shape.I, "n_shared": wl.shape.n_shared, "tile_rows": args.tile_rows,
+                   "block": bool(args.block),
                    "l2": "no flush: weights %.1f MB per layer > 129 MB L2" %
                          (len(G.layers) and (wl.shape.E + wl.shape.n_shared) *
                           expert_bytes(wl.shape.H, wl.shape.I) / 1e6),
@@ -542,8 +572,9 @@ def run_ours(args, wl):
                  "hbm_frac": round(step_bytes / (ms_step / 1e3) / 1e9 / hbm, 4),
                  "tensor_frac": round(step_flops / (ms_step / 1e3) / 1e12 / bf16s, 4),
                  "touched_experts": int((counts > 0).sum()), "max_group": int(counts.max())},
-        "roofline": ({"kernel": "dec_persist_kernel: %d layers in one cooperative launch"
-                                % len(G.layers)} if G.persistent else
+        "roofline": ({"kernel": "dec_persist_kernel: %d %s in one cooperative launch"
+                                % (len(G.layers), "decoder blocks" if G.block else "layers")}
+                     if G.persistent else
                      {"kernel": "moe_decode_layers chain (dec_route, dec_gate_up, dec_down)"
                                 " per layer, CUDA graph of %d layers" % len(G.layers)}
                      if G.fused else
@@ -551,11 +582,13 @@ def run_ours(args, wl):
                                 "grouped GEMMs)"}),
         "e2e": {"value": round(job_throughput(G.tokens_per_step, world, e_ms), 2),
                 "unit": "tokens/s",
-                "h2d_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
+                "h2d_bytes_per_step": int(G.h2d_bytes),
                 "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "steps": e_steps, "ms_per_step": round(e_ms, 5),
-                "mode": "CUDA graph of the moe_decode_layers call and copies" if G.fused
-                        else "moe_layer_w4 calls",
+                "mode": ("CUDA graph of the token-id copy, the moe_decode_block call and the "
+                         "read-back" if G.block else
+                         "CUDA graph of the moe_decode_layers call and copies" if G.fused
+                         else "moe_layer_w4 calls"),
                 "eager_value": round(job_throughput(G.tokens_per_step, world, e_eager_ms), 2)},
         "gpu_launches": G.launches_per_step() * args.steps,
         "launch_mode": ("CUDA graph replay of one cooperative launch per step" if G.persistent
@@ -602,6 +635,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="stacked layers (default: the workload's); a smaller case for profilers")
+    ap.add_argument("--block", action="store_true",
+                    help="decode: decoder blocks (pre-norm with gain, residual add) fed by "
+                         "token ids through an embedding table (moe_decode_block)")
     ap.add_argument("--tile-rows", type=int, default=128,
                     help="most routed rows per block-map tile (1..128): the grouped GEMMs' N")
     args = ap.parse_args()
