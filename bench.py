@@ -326,7 +326,7 @@ class GpuWorkload:
         self.fused = self.path in (1, 2)
         self.persistent = self.path == 2
         self.table = m.decode_layer_table(self.layers) if self.fused else None
-        # decoder blocks (moe_decode_block): per-layer gains and the token
+        # decoder blocks (moe_decoder_blocks): per-layer gains and the token
         # feed from an embedding table, the step's token ids in device memory
         self.block = bool(block)
         self.h2d_bytes = self.tokens_per_step * S.H * 2
@@ -380,7 +380,7 @@ class GpuWorkload:
         m, S, T = self.m, self.S, self.T
         nl = len(self.layers)
         if self.block:  # every decoder block in one call, h_0 from the token ids
-            m.moe_decode_block(self.shape, self.table, self.gains, self.y_out, self.ws,
+            m.moe_decoder_blocks(self.shape, self.table, self.gains, self.y_out, self.ws,
                                token_ids=self.tok, embed=self.embed)
             return
         if self.fused:  # every layer in one call (moe_decode_layers)
@@ -409,7 +409,7 @@ class GpuWorkload:
         nl = len(self.layers)
         if self.block:
             self.tok.copy_(x_pin[:T], non_blocking=True)
-            m.moe_decode_block(self.shape, self.table, self.gains, self.y, self.ws,
+            m.moe_decoder_blocks(self.shape, self.table, self.gains, self.y, self.ws,
                                token_ids=self.tok, embed=self.embed)
             y_pin[:T].copy_(self.y, non_blocking=True)
             return
@@ -585,7 +585,7 @@ def run_ours(args, wl):
                 "h2d_bytes_per_step": int(G.h2d_bytes),
                 "d2h_bytes_per_step": int(G.tokens_per_step * wl.shape.H * 2),
                 "steps": e_steps, "ms_per_step": round(e_ms, 5),
-                "mode": ("CUDA graph of the token-id copy, the moe_decode_block call and the "
+                "mode": ("CUDA graph of the token-id copy, the moe_decoder_blocks call and the "
                          "read-back" if G.block else
                          "CUDA graph of the moe_decode_layers call and copies" if G.fused
                          else "moe_layer_w4 calls"),
@@ -637,7 +637,7 @@ def main():
                     help="stacked layers (default: the workload's); a smaller case for profilers")
     ap.add_argument("--block", action="store_true",
                     help="decode: decoder blocks (pre-norm with gain, residual add) fed by "
-                         "token ids through an embedding table (moe_decode_block)")
+                         "token ids through an embedding table (moe_decoder_blocks)")
     ap.add_argument("--tile-rows", type=int, default=128,
                     help="most routed rows per block-map tile (1..128): the grouped GEMMs' N")
     args = ap.parse_args()

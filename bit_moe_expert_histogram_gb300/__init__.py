@@ -31,7 +31,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_r
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
            "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers",
-           "moe_decode_block")
+           "moe_decoder_blocks")
 
 
 class MoeError(RuntimeError):
@@ -99,7 +99,7 @@ def load():
                     ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P]),
                     ("moe_plan_noalloc", [pS, P, pP, P]),
                     ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P]),
-                    ("moe_decode_block", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P])):
+                    ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -211,17 +211,17 @@ def gain_table(gains):
     return arr
 
 
-def moe_decode_block(shape, layer_table, gains, h_out, ws, h_in=None, token_ids=None,
+def moe_decoder_blocks(shape, layer_table, gains, h_out, ws, h_in=None, token_ids=None,
                      embed=None, stream=None):
     """n decoder blocks (pre-norm with gain, MoE layer, residual add); h_0 is
     h_in, or the rows of embed named by the device token ids."""
     if len(gains) != len(layer_table):
         raise ValueError("one gain table entry per layer")
     vocab = embed.shape[0] if embed is not None else 0
-    _check(load().moe_decode_block(C.byref(shape), len(layer_table),
+    _check(load().moe_decoder_blocks(C.byref(shape), len(layer_table),
                                    C.cast(layer_table, C.c_void_p), C.cast(gains, C.c_void_p),
                                    _p(h_in), _p(token_ids), _p(embed), vocab, _p(h_out),
-                                   _p(ws), ws.numel(), _s(stream)), "moe_decode_block")
+                                   _p(ws), ws.numel(), _s(stream)), "moe_decoder_blocks")
 
 
 def moe_layer_w4(shape, x, w_router, router_bias, experts, shared, y, ws, x_next=None,

@@ -49,7 +49,7 @@ int64_t max_blocks_of(const moe_shape_t* s) {
 
 struct Layout {
   size_t ctrl, hist, logits, h, ids, w, counts, offsets, sorted, rowpos, bmap, nblk, yslots, part,
-      rpart, part2, ybuf, tags, xmid, xs, total;
+      rpart, part2, ybuf, tags, xmid, xs, blk, total;
 };
 
 Layout layout_of(const moe_shape_t* s) {
@@ -92,6 +92,8 @@ Layout layout_of(const moe_shape_t* s) {
   // layers to the next
   L.tags = ps ? take(persist_tags(s->T, s->H, s->E, s->K, s->I, s->n_shared).total * 8) : off;
   L.xmid = ps ? take(T * (size_t)s->H * 2) : off;
+  // decoder blocks through the four calls: two residual buffers and x
+  L.blk = take((size_t)3 * T * s->H * 2);
   L.total = off;
   return L;
 }
@@ -328,7 +330,7 @@ moe_status_t decode_persistent(const moe_shape_t* s, int n_layers,
 
 // Decoder blocks through the persistent kernel, 48 layers per launch; the
 // residual stream passes between launches through the two ybuf halves.
-moe_status_t decode_block_persistent(const moe_shape_t* s, int n_layers,
+moe_status_t decoder_blocks_persistent(const moe_shape_t* s, int n_layers,
                                      const moe_layer_weights_t* layers,
                                      const void* const* gains, const void* h_in,
                                      const int32_t* tok, const void* embed, int vocab,
@@ -529,18 +531,13 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
   return moe_combine(shape, y_slots, plan.row_pos_dev, w, y_dev, x_next_dev, stream);
 }
 
-moe_status_t moe_decode_block(const moe_shape_t* shape, int32_t n_layers,
+moe_status_t moe_decoder_blocks(const moe_shape_t* shape, int32_t n_layers,
                               const moe_layer_weights_t* layers_host,
                               const void* const* gains_host, const void* h_in_dev,
                               const int32_t* token_ids_dev, const void* embed_dev, int32_t vocab,
                               void* h_out_dev, void* ws_dev, size_t ws_bytes,
                               moe_stream_t stream) {
   if (!shape_ok(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  int grid = 0;
-  size_t smem = 0;
-  if (!persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid,
-                      &smem, true))
-    return MOE_ERR_UNSUPPORTED_SHAPE;
   if (n_layers < 1 || !layers_host || !gains_host || !h_out_dev || !aligned16(h_out_dev))
     return MOE_ERR_INVALID_ARG;
   if (token_ids_dev) {
@@ -556,10 +553,55 @@ moe_status_t moe_decode_block(const moe_shape_t* shape, int32_t n_layers,
     if (!gains_host[l] || !aligned16(gains_host[l])) return MOE_ERR_INVALID_ARG;
   }
   MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
-  return decode_block_persistent(shape, n_layers, layers_host, gains_host, h_in_dev,
-                                 token_ids_dev, embed_dev, vocab, h_out_dev,
-                                 static_cast<uint8_t*>(ws_dev), layout_of(shape), grid, smem,
-                                 (cudaStream_t)stream);
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  const Layout L = layout_of(shape);
+  cudaStream_t st = (cudaStream_t)stream;
+  int grid = 0;
+  size_t smem = 0;
+  if (persist_config(shape->T, shape->H, shape->E, shape->K, shape->I, shape->n_shared, &grid,
+                     &smem, true))
+    return decoder_blocks_persistent(shape, n_layers, layers_host, gains_host, h_in_dev,
+                                     token_ids_dev, embed_dev, vocab, h_out_dev, ws, L, grid,
+                                     smem, st);
+  // more tokens: per layer the four calls, the pre-norm of the next layer and
+  // the residual add fused into the combine
+  const size_t TH = (size_t)shape->T * shape->H;
+  uint16_t* hb[2] = {reinterpret_cast<uint16_t*>(ws + L.blk),
+                     reinterpret_cast<uint16_t*>(ws + L.blk) + TH};
+  uint16_t* x = reinterpret_cast<uint16_t*>(ws + L.blk) + 2 * TH;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  const uint16_t* h = token_ids_dev ? hb[0] : static_cast<const uint16_t*>(h_in_dev);
+  cudaError_t e = launch_block_input(
+      static_cast<const uint16_t*>(h_in_dev), token_ids_dev,
+      static_cast<const uint16_t*>(embed_dev), vocab, static_cast<const uint16_t*>(gains_host[0]),
+      shape->T, shape->H, token_ids_dev ? hb[0] : nullptr, x, ctrl, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decoder block input launch");
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  float* w = reinterpret_cast<float*>(ws + L.w);
+  moe_plan_t plan;
+  plan.counts_dev = reinterpret_cast<int32_t*>(ws + L.counts);
+  plan.offsets_dev = reinterpret_cast<int32_t*>(ws + L.offsets);
+  plan.sorted_rows_dev = reinterpret_cast<int32_t*>(ws + L.sorted);
+  plan.row_pos_dev = reinterpret_cast<int32_t*>(ws + L.rowpos);
+  plan.block_map_dev = reinterpret_cast<int32_t*>(ws + L.bmap);
+  plan.num_blocks_dev = reinterpret_cast<int32_t*>(ws + L.nblk);
+  void* y_slots = ws + L.yslots;
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_layer_weights_t& lw = layers_host[l];
+    const bool last = l == n_layers - 1;
+    MOE_TRY(moe_route(shape, x, lw.w_router_dev, lw.router_bias_dev, ids, w, ws_dev, ws_bytes,
+                      stream));
+    MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
+    MOE_TRY(run_ffn(shape, x, &lw.experts, &lw.shared, &plan, y_slots, ws, st));
+    // the next residual buffer: never the one this layer reads
+    uint16_t* hn = last ? static_cast<uint16_t*>(h_out_dev) : (h == hb[0] ? hb[1] : hb[0]);
+    e = launch_combine(static_cast<const uint16_t*>(y_slots), plan.row_pos_dev, w, shape->T,
+                       shape->H, shape->K, shape->n_shared, nullptr, last ? nullptr : x, st, h, hn,
+                       last ? nullptr : static_cast<const uint16_t*>(gains_host[l + 1]));
+    if (e != cudaSuccess) return cuda_fail(e, "decoder block combine launch");
+    h = hn;
+  }
+  return MOE_OK;
 }
 
 moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,

@@ -84,7 +84,7 @@ struct PersistArgs {
   uint64_t* h_tag;      // line per gate_up tile: words 4 col + r = bf16 pair (h_r, h_r+4)
   uint64_t* y_tag;      // line t*(H/8)+g: words 0..3 = bf16 pairs (y_r, y_r+4), word 4 = y^2 partial
   Ctrl* ctrl;
-  // decoder blocks (moe_decode_block) when block != 0: layer l's input is
+  // decoder blocks (moe_decoder_blocks) when block != 0: layer l's input is
   // bf16(gain[l] * h_l / rms(h_l)) and its output h_{l+1} = bf16(h_l + y_l)
   // (y is then h, the residual stream; x_next must be null); h_0 is
   // embed[tok[t]] when tok is set (ids outside [0, vocab) are recorded and
@@ -134,9 +134,17 @@ cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, cons
 // shared expert's rows in token order), S rows of H bf16
 cudaError_t launch_gather_x(const uint16_t* x, const int32_t* sorted_rows, int K, int R, int S,
                             int T, int H, uint16_t* xs, Ctrl* ctrl, int nsm, cudaStream_t stream);
+// h_out set: decoder blocks (h_out = bf16(h_in + y), x_next of h_out with
+// gain); y may then be null
 cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, const float* w, int T,
                            int H, int K, int n_shared, uint16_t* y, uint16_t* x_next,
-                           cudaStream_t stream);
+                           cudaStream_t stream, const uint16_t* h_in = nullptr,
+                           uint16_t* h_out = nullptr, const uint16_t* gain = nullptr);
+// The first decoder block's h_0 (h_in, or the embedding rows of tok copied to
+// h0_out) and its input x = bf16(gain * h_0 / rms(h_0)).
+cudaError_t launch_block_input(const uint16_t* h_in, const int32_t* tok, const uint16_t* embed,
+                               int vocab, const uint16_t* gain, int T, int H, uint16_t* h0_out,
+                               uint16_t* x, Ctrl* ctrl, cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
                            int N, int Kd, cudaStream_t stream);
 // Host helpers shared by the C-ABI translation units (api.cu keeps the state).

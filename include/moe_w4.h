@@ -245,9 +245,10 @@ moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
  * each step's token ids from device memory with no host round trip; an id
  * outside [0, vocab) is recorded as MOE_ERR_BAD_INPUT and reads as a zero
  * row), else h_in_dev. Writes h_out_dev = h_{n_layers}.
- * Runs the persistent decode kernel (one cooperative launch per 48 layers);
- * a shape it cannot hold returns MOE_ERR_UNSUPPORTED_SHAPE (moe_layer_path
- * tells which shapes it holds).
+ * A few tokens (the shapes the persistent decode kernel holds) run in one
+ * cooperative launch per 48 layers; more tokens run the four calls of each
+ * layer, with the residual add and the next layer's pre-norm fused into the
+ * combine.
  *  layers_host   n_layers host structs, as for moe_decode_layers
  *  gains_host    n_layers device pointers, each bf16 [H], 16-byte aligned
  *  h_in_dev      bf16 [T][H], or NULL when token_ids_dev is given
@@ -256,7 +257,7 @@ moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
  *  h_out_dev     bf16 [T][H] out; may be h_in_dev
  * The workspace is the layer's (moe_workspace_bytes), zero-filled by
  * moe_workspace_init; the last layer's ids and weights are left in it. */
-moe_status_t moe_decode_block(const moe_shape_t* shape, int32_t n_layers,
+moe_status_t moe_decoder_blocks(const moe_shape_t* shape, int32_t n_layers,
                               const moe_layer_weights_t* layers_host,
                               const void* const* gains_host, const void* h_in_dev,
                               const int32_t* token_ids_dev, const void* embed_dev, int32_t vocab,

@@ -198,7 +198,7 @@ def residual_add(h, y):
     return out
 
 
-def decode_block(Ls, gains, h0, K):
+def decoder_blocks(Ls, gains, h0, K):
     """Stacked decoder blocks: for each layer x = rmsnorm_gain_rows(h, g),
     y = the MoE layer on x (router, top-K, experts, combine), h = h + y.
     Returns the last h and the last layer's ids."""

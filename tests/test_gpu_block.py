@@ -1,4 +1,4 @@
-"""GPU parity of the decoder blocks around the MoE layers (moe_decode_block):
+"""GPU parity of the decoder blocks around the MoE layers (moe_decoder_blocks):
 the pre-norm with a learned gain, the layer, the residual add, and the token
 feed from device memory ("Perplexity Open Sources Lily: A Rust + Metal
 Inference Engine for Qwen3.6-35B-A3B on Apple Silicon", section "Decode:
@@ -67,21 +67,24 @@ class Stack:
         hi = len(self.Ls) if hi is None else hi
         table, gains = self.sub(lo, hi)
         out = torch.empty((self.T, self.S.H), dtype=torch.int16, device=self.dev) if out is None else out
-        m.moe_decode_block(self.shape, table, gains, out, self.ws, h_in=h_in, **kw)
+        m.moe_decoder_blocks(self.shape, table, gains, out, self.ws, h_in=h_in, **kw)
         return out
 
 
-@pytest.mark.parametrize("shape,T", [(FULL, 1), (FULL, 2), (TINY, 3)])
-def test_block_layers_teacher_forced(shape, T):
+@pytest.mark.parametrize("shape,T,n_layers", [(FULL, 1, 3), (FULL, 2, 3), (TINY, 3, 3),
+                                              (TINY, 40, 3), (FULL, 64, 2)])
+def test_block_layers_teacher_forced(shape, T, n_layers):
     """After each layer the residual stream matches the oracle block applied
-    to the device's stream of the layer before."""
-    st = Stack(shape, T, 3, seed=200)
+    to the device's stream of the layer before (T <= 4: the persistent
+    kernel; more tokens: the four calls with the residual add and the next
+    pre-norm in the combine)."""
+    st = Stack(shape, T, n_layers, seed=200)
     h0 = st.Ls[0].x[:T].copy()
     prev = h0
-    for n in range(1, 4):
+    for n in range(1, n_layers + 1):
         out = st.run(d16(h0, st.dev), 0, n)
         assert m.moe_query_device_status(st.ws) == 0
-        h_o, _ = oracle.decode_block([st.Ls[n - 1]], [st.g[n - 1]], prev, shape.K)
+        h_o, _ = oracle.decoder_blocks([st.Ls[n - 1]], [st.g[n - 1]], prev, shape.K)
         got = h16(out)
         close(f64(got), f64(h_o), "h after %d layers" % n)
         # the layer's own contribution, against the oracle's
@@ -89,9 +92,10 @@ def test_block_layers_teacher_forced(shape, T):
         prev = got
 
 
-def test_block_is_deterministic_and_may_write_its_input():
-    st = Stack(TINY, 2, 4, seed=300)
-    h0 = d16(st.Ls[0].x[:2], st.dev)
+@pytest.mark.parametrize("T", [2, 24])
+def test_block_is_deterministic_and_may_write_its_input(T):
+    st = Stack(TINY, T, 4, seed=300)
+    h0 = d16(st.Ls[0].x[:T], st.dev)
     a = h16(st.run(h0.clone())).copy()
     b = h16(st.run(h0.clone())).copy()
     assert np.array_equal(a, b)
@@ -113,22 +117,27 @@ def test_block_split_over_launches():
     assert np.array_equal(whole, two)
 
 
-def test_block_token_feed_from_the_embedding_table():
+@pytest.mark.parametrize("shape,T", [(FULL, 3), (TINY, 12)])
+def test_block_token_feed_from_the_embedding_table(shape, T):
     """Token ids in device memory: h_0 is the ids' embedding rows, gathered
-    by the kernel; an id outside the table is recorded and reads as zeros."""
-    T, V = 3, 1000
-    st = Stack(FULL, T, 2, seed=500)
-    emb_h = synth.gen_embed(V, FULL.H, seed=501)
+    on the device; an id outside the table is recorded and reads as zeros."""
+    V = 1000
+    st = Stack(shape, T, 2, seed=500)
+    emb_h = synth.gen_embed(V, shape.H, seed=501)
     emb = d16(emb_h, st.dev)
-    ids = torch.tensor([7, 999, 0], dtype=torch.int32, device=st.dev)
+    pick = (np.arange(T) * 397 + 7) % V
+    pick[1] = V - 1
+    ids = torch.tensor(pick, dtype=torch.int32, device=st.dev)
     got = h16(st.run(None, token_ids=ids, embed=emb)).copy()
     assert m.moe_query_device_status(st.ws) == 0
-    ref = h16(st.run(d16(emb_h[[7, 999, 0]], st.dev))).copy()
+    ref = h16(st.run(d16(emb_h[pick], st.dev))).copy()
     assert np.array_equal(got, ref)
-    bad = torch.tensor([7, V, 0], dtype=torch.int32, device=st.dev)
+    bad_pick = pick.copy()
+    bad_pick[1] = V
+    bad = torch.tensor(bad_pick, dtype=torch.int32, device=st.dev)
     got_bad = h16(st.run(None, token_ids=bad, embed=emb)).copy()
     assert m.moe_query_device_status(st.ws) == m.MOE_ERR_BAD_INPUT
-    h_zero = emb_h[[7, 0, 0]].copy()
+    h_zero = emb_h[pick].copy()
     h_zero[1] = 0
     ref_bad = h16(st.run(d16(h_zero, st.dev))).copy()
     assert np.array_equal(got_bad, ref_bad)
@@ -151,7 +160,7 @@ def test_block_decode_loop_captured_in_a_graph():
     def loop():
         tok.copy_(ids0)
         for s in range(steps):
-            m.moe_decode_block(st.shape, table, gains, outs[s], st.ws, token_ids=tok, embed=emb)
+            m.moe_decoder_blocks(st.shape, table, gains, outs[s], st.ws, token_ids=tok, embed=emb)
             h = outs[s].view(torch.bfloat16)[:, :V].float()
             tok.copy_(torch.argmax(h, dim=1).to(torch.int32))
 
@@ -183,9 +192,9 @@ def test_block_rejects_bad_arguments():
     table, gains = st.sub(0, 1)
     out = torch.empty((1, TINY.H), dtype=torch.int16, device=st.dev)
     with pytest.raises(m.MoeError):
-        m.moe_decode_block(st.shape, table, gains, out, st.ws)  # neither h_in nor token ids
+        m.moe_decoder_blocks(st.shape, table, gains, out, st.ws)  # neither h_in nor token ids
     with pytest.raises(ValueError):
-        m.moe_decode_block(st.shape, table, m.gain_table([]), out, st.ws, h_in=out)
+        m.moe_decoder_blocks(st.shape, table, m.gain_table([]), out, st.ws, h_in=out)
     wide = m.make_shape(2, 8192, TINY.E, TINY.K, TINY.I, TINY.n_shared, 128)
-    with pytest.raises(m.MoeError):  # T*H > 8192: no persistent kernel
-        m.moe_decode_block(wide, table, gains, out, st.ws, h_in=out)
+    with pytest.raises(m.MoeError):  # a workspace sized for another shape
+        m.moe_decoder_blocks(wide, table, gains, out, st.ws, h_in=out)

@@ -359,7 +359,7 @@ def test_residual_add_ties_and_torch():
     assert np.array_equal(oracle.residual_add(a, b), ref)
 
 
-def test_decode_block_zero_layer_keeps_the_residual_stream():
+def test_decoder_blocks_zero_layer_keeps_the_residual_stream():
     """A layer whose experts rebuild to zero (scale and bias 0) outputs y = 0,
     so the block returns its input unchanged, whatever the gain."""
     shape = synth.LayerShape(H=256, E=8, K=2, I=128, n_shared=1)
@@ -367,6 +367,6 @@ def test_decode_block_zero_layer_keeps_the_residual_stream():
     for name in ("s_down", "b_down", "sh_s_down", "sh_b_down"):
         getattr(L, name)[...] = 0
     h0 = synth.gen_tokens(3, 256, seed=9)
-    h, ids = oracle.decode_block([L], [synth.gen_gain(256, seed=10)], h0, 2)
+    h, ids = oracle.decoder_blocks([L], [synth.gen_gain(256, seed=10)], h0, 2)
     assert np.array_equal(h, h0)
     assert ids.shape == (3, 2)
