@@ -56,6 +56,8 @@ def lib():
             L.orc_layer_tokens.argtypes = [P, i, i, i, i, P, P] + [P] * 12 + [P, i, P, P]
             L.orc_rmsnorm_rows.argtypes = [P, i, i, P]
             L.orc_rmsnorm_gain_rows.argtypes = [P, P, i, i, P]
+            L.orc_attn_decode.restype = i
+            L.orc_attn_decode.argtypes = [P, P, P, P, i, i, i, i, i, i, i, P]
             L.orc_residual_add.argtypes = [P, P, C.c_size_t, P]
             L.orc_num_threads.restype = i
             _lib = L
@@ -209,6 +211,25 @@ def decoder_blocks(Ls, gains, h0, K):
         ids, _, w64 = topk(router_logits(x, L.w_router, L.router_bias), K)
         h = residual_add(h, layer_tokens(L, ids, w64, x=x))
     return h, ids
+
+
+def attn_decode(q, k_cache, v_cache, table, L):
+    """Grouped-query decode attention over a block-paged key/value cache.
+
+    q [T][n_q][D]; k_cache, v_cache [n_phys][n_kv][B][D] (bf16 bits);
+    table [ceil(L / B)] physical block of each logical block. Query token t
+    is at position L - T + t. Returns o [T][n_q][D] (bf16 bits)."""
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint16)
+    v_cache = _c(v_cache, np.uint16)
+    table = _c(table, np.int32)
+    T, n_q, D = q.shape
+    n_phys, n_kv, B, _ = k_cache.shape
+    o = np.empty_like(q)
+    if lib().orc_attn_decode(_p(q), _p(k_cache), _p(v_cache), _p(table), n_phys, T, n_q, n_kv,
+                             D, int(L), B, _p(o)) != 0:
+        raise ValueError("oracle attention: block table entry out of range")
+    return o
 
 
 def route(L, K):

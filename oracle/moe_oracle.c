@@ -441,6 +441,56 @@ void orc_residual_add(const uint16_t* h, const uint16_t* y, size_t n, uint16_t* 
     out[i] = orc_bf16_rne(orc_bf16_value(h[i]) + orc_bf16_value(y[i]));
 }
 
+/* Decode attention of a grouped-query layer (the model's full-attention
+ * layers: 16 query heads share 2 key/value heads [P3 "Three Workload
+ * Shapes"]; at decode the queries of a few new tokens attend to a growing
+ * key/value cache kept in fixed-size blocks [P3 "Decode"]). Plain softmax
+ * attention, fp64:
+ *   query token t sits at position L - T + t and sees positions 0..L-T+t;
+ *   head h reads key/value head h / (n_q / n_kv);
+ *   s_j = (q . k_j) / sqrt(D),  o = sum_j softmax(s)_j v_j,  RNE to bf16.
+ * Position j of head g is row j % B of physical block table[j / B]:
+ * k_cache[((table[j / B] * n_kv + g) * B + j % B) * D + d], v likewise.
+ * q, o: [T][n_q][D] bf16 bits. Returns -1 for a table entry outside
+ * [0, n_phys), else 0. */
+int orc_attn_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                    const int32_t* table, int n_phys, int T, int n_q, int n_kv, int D, int L,
+                    int B, uint16_t* o) {
+  const int nblk = (L + B - 1) / B;
+  for (int i = 0; i < nblk; ++i)
+    if (table[i] < 0 || table[i] >= n_phys) return -1;
+  const int group = n_q / n_kv;
+  double* s = (double*)malloc(sizeof(double) * (size_t)L);
+  double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+  for (int t = 0; t < T; ++t) {
+    const int last = L - T + t;  /* the token's own position */
+    for (int h = 0; h < n_q; ++h) {
+      const int g = h / group;
+      const uint16_t* qv = q + ((size_t)t * n_q + h) * D;
+      double mx = -INFINITY;
+      for (int j = 0; j <= last; ++j) {
+        const size_t row = (((size_t)table[j / B] * n_kv + g) * B + j % B) * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += orc_bf16_value(qv[d]) * orc_bf16_value(k_cache[row + d]);
+        s[j] = dot / sqrt((double)D);
+        if (s[j] > mx) mx = s[j];
+      }
+      double z = 0.0;
+      for (int d = 0; d < D; ++d) acc[d] = 0.0;
+      for (int j = 0; j <= last; ++j) {
+        const double p = exp(s[j] - mx);
+        z += p;
+        const size_t row = (((size_t)table[j / B] * n_kv + g) * B + j % B) * D;
+        for (int d = 0; d < D; ++d) acc[d] += p * orc_bf16_value(v_cache[row + d]);
+      }
+      for (int d = 0; d < D; ++d) o[((size_t)t * n_q + h) * D + d] = orc_bf16_rne(acc[d] / z);
+    }
+  }
+  free(s);
+  free(acc);
+  return 0;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

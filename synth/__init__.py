@@ -10,6 +10,7 @@ from .gen import (  # noqa: F401
     LayerInputs,
     bf16_bits,
     bf16_bits_to_f32,
+    gen_attn,
     gen_embed,
     gen_gain,
     gen_layer,

@@ -116,3 +116,18 @@ def gen_embed(V, H, seed) -> np.ndarray:
     """A token embedding table: V rows of bf16 N(0, 1) values."""
     rng = np.random.default_rng(seed)
     return bf16_bits(rng.standard_normal((V, H)))
+
+
+def gen_attn(T, n_q, n_kv, D, L, B=64, seed=0, spare=3):
+    """Decode-attention inputs: q [T][n_q][D], a key/value cache of
+    ceil(L / B) + spare physical blocks [n_phys][n_kv][B][D] (bf16 N(0, 1)),
+    and a block table mapping the logical blocks to a random permutation of
+    them."""
+    rng = np.random.default_rng(seed)
+    nblk = (L + B - 1) // B
+    n_phys = nblk + spare
+    q = bf16_bits(rng.standard_normal((T, n_q, D)))
+    k = bf16_bits(rng.standard_normal((n_phys, n_kv, B, D)))
+    v = bf16_bits(rng.standard_normal((n_phys, n_kv, B, D)))
+    table = rng.permutation(n_phys)[:nblk].astype(np.int32)
+    return q, k, v, table

@@ -370,3 +370,76 @@ def test_decoder_blocks_zero_layer_keeps_the_residual_stream():
     h, ids = oracle.decoder_blocks([L], [synth.gen_gain(256, seed=10)], h0, 2)
     assert np.array_equal(h, h0)
     assert ids.shape == (3, 2)
+
+
+# ------------------------------------------------- decode attention (GQA) --
+def _dense_kv(k, v, table, L):
+    """The cache as contiguous [n_kv][L][D] arrays (positions in order)."""
+    B = k.shape[2]
+    idx = [(table[j // B], j % B) for j in range(L)]
+    kk = np.stack([k[p, :, r] for p, r in idx], axis=1)
+    vv = np.stack([v[p, :, r] for p, r in idx], axis=1)
+    return kk, vv
+
+
+def test_attn_matches_torch_sdpa():
+    """Against torch's scaled_dot_product_attention in float64 on the same
+    numbers (contiguous K/V, each query head given its group's K/V, the
+    causal window of each new token as an explicit mask)."""
+    T, n_q, n_kv, D, L = 2, 16, 2, 64, 150
+    q, k, v, table = synth.gen_attn(T, n_q, n_kv, D, L, seed=11)
+    o = synth.bf16_bits_to_f32(oracle.attn_decode(q, k, v, table, L)).astype(np.float64)
+    kk, vv = _dense_kv(k, v, table, L)
+    qf = torch.from_numpy(synth.bf16_bits_to_f32(q).astype(np.float64)).permute(1, 0, 2)
+    kf = torch.from_numpy(synth.bf16_bits_to_f32(kk).astype(np.float64))
+    vf = torch.from_numpy(synth.bf16_bits_to_f32(vv).astype(np.float64))
+    kf = kf.repeat_interleave(n_q // n_kv, dim=0)
+    vf = vf.repeat_interleave(n_q // n_kv, dim=0)
+    mask = torch.tensor([[j <= L - T + t for j in range(L)] for t in range(T)])
+    ref = torch.nn.functional.scaled_dot_product_attention(qf, kf, vf, attn_mask=mask)
+    ref = ref.permute(1, 0, 2).numpy()
+    assert np.abs(o - ref).max() <= 2 ** -8 * np.abs(ref).max()
+    assert np.abs(o - ref).mean() <= 2 ** -9 * np.abs(ref).mean()
+
+
+def test_attn_closed_forms():
+    """One position: o = v_0. Equal keys: o = the mean of the visible
+    values. A dominant key: o = its value. Head h reads group h / 8."""
+    T, n_q, n_kv, D = 1, 16, 2, 64
+    q, k, v, table = synth.gen_attn(T, n_q, n_kv, D, 1, seed=12)
+    o = oracle.attn_decode(q, k, v, table, 1)
+    for h in range(n_q):
+        assert np.array_equal(o[0, h], v[table[0], h // 8, 0])
+    L = 100
+    q, k, v, table = synth.gen_attn(T, n_q, n_kv, D, L, seed=13)
+    k[...] = k[0:1, :, 0:1]  # every key equal within a head group
+    o = synth.bf16_bits_to_f32(oracle.attn_decode(q, k, v, table, L)).astype(np.float64)
+    _, vv = _dense_kv(k, v, table, L)
+    mean = synth.bf16_bits_to_f32(vv).astype(np.float64).mean(axis=1)  # [n_kv][D]
+    for h in range(n_q):
+        assert np.abs(o[0, h] - mean[h // 8]).max() <= 2 ** -8 * np.abs(mean[h // 8]).max()
+    q, k, v, table = synth.gen_attn(T, n_q, n_kv, D, L, seed=14)
+    j = 37
+    k[table[j // 64], 1, j % 64] = synth.bf16_bits(
+        40.0 * synth.bf16_bits_to_f32(q[0, 8]))  # head 8's query, scaled up
+    o = oracle.attn_decode(q, k, v, table, L)
+    assert np.array_equal(o[0, 8], v[table[j // 64], 1, j % 64])
+    v[:, 1] = 0  # group 1 silenced: heads 8..15 output zero, heads 0..7 do not
+    o = synth.bf16_bits_to_f32(oracle.attn_decode(q, k, v, table, L))
+    assert (o[0, 8:] == 0).all() and (np.abs(o[0, :8]) > 0).any()
+
+
+def test_attn_causal_window_and_paging():
+    """With two new tokens the first does not see the last position; moving
+    the blocks to other physical slots changes nothing."""
+    n_q, n_kv, D, L = 16, 2, 64, 130
+    q, k, v, table = synth.gen_attn(2, n_q, n_kv, D, L, seed=15)
+    o2 = oracle.attn_decode(q, k, v, table, L)
+    o1 = oracle.attn_decode(q[:1], k, v, table, L - 1)
+    assert np.array_equal(o2[0], o1[0])
+    perm = np.random.default_rng(16).permutation(k.shape[0])
+    k2 = np.empty_like(k); v2 = np.empty_like(v)
+    k2[perm] = k; v2[perm] = v
+    assert np.array_equal(oracle.attn_decode(q, k2, v2, perm[table], L), o2)
+    with pytest.raises(ValueError):
+        oracle.attn_decode(q, k, v, np.full_like(table, k.shape[0]), L)
