@@ -31,7 +31,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_r
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
            "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers",
-           "moe_decoder_blocks")
+           "moe_decoder_blocks", "moe_attn_workspace_bytes", "moe_attn_decode")
 
 
 class MoeError(RuntimeError):
@@ -50,6 +50,11 @@ class Shape(C.Structure):
     def __repr__(self):
         return "Shape(T=%d, H=%d, E=%d, K=%d, I=%d, n_shared=%d, tile_rows=%d)" % (
             self.T, self.H, self.E, self.K, self.I, self.n_shared, self.tile_rows)
+
+
+class AttnShape(C.Structure):
+    _fields_ = [("T", C.c_int32), ("n_q", C.c_int32), ("n_kv", C.c_int32), ("D", C.c_int32),
+                ("L", C.c_int32), ("block", C.c_int32)]
 
 
 class W4Weights(C.Structure):
@@ -88,6 +93,8 @@ def load():
             L.moe_max_blocks.argtypes = [pS]
             L.moe_layer_path.restype = I32
             L.moe_layer_path.argtypes = [pS]
+            L.moe_attn_workspace_bytes.restype = SZ
+            L.moe_attn_workspace_bytes.argtypes = [C.POINTER(AttnShape)]
             for name, args in (
                     ("moe_workspace_init", [P, SZ, P]),
                     ("moe_route", [pS, P, P, P, P, P, P, SZ, P]),
@@ -99,7 +106,8 @@ def load():
                     ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P]),
                     ("moe_plan_noalloc", [pS, P, pP, P]),
                     ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P]),
-                    ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P])):
+                    ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P]),
+                    ("moe_attn_decode", [C.POINTER(AttnShape), P, P, P, P, I32, P, P, SZ, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -200,6 +208,26 @@ def moe_decode_layers(shape, layer_table, x, y, ws, x_next=None, stream=None):
     _check(load().moe_decode_layers(C.byref(shape), len(layer_table),
                                     C.cast(layer_table, C.c_void_p), _p(x), _p(y), _p(x_next),
                                     _p(ws), ws.numel(), _s(stream)), "moe_decode_layers")
+
+
+def make_attn_shape(T, n_q, n_kv, D, L, block=64):
+    return AttnShape(T, n_q, n_kv, D, L, block)
+
+
+def alloc_attn_workspace(shape, device="cuda", stream=None):
+    n = load().moe_attn_workspace_bytes(C.byref(shape))
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "alloc_attn_workspace")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_workspace_init(ws, stream)
+    return ws
+
+
+def moe_attn_decode(shape, q, k_cache, v_cache, table, o, ws, stream=None):
+    """Grouped-query decode attention over a block-paged key/value cache."""
+    _check(load().moe_attn_decode(C.byref(shape), _p(q), _p(k_cache), _p(v_cache), _p(table),
+                                  k_cache.shape[0], _p(o), _p(ws), ws.numel(), _s(stream)),
+           "moe_attn_decode")
 
 
 def gain_table(gains):

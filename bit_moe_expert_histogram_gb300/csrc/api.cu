@@ -604,6 +604,32 @@ moe_status_t moe_decoder_blocks(const moe_shape_t* shape, int32_t n_layers,
   return MOE_OK;
 }
 
+size_t moe_attn_workspace_bytes(const moe_attn_shape_t* shape) {
+  if (!attn_supported(shape)) return 0;
+  return 256 + attn_part_floats(shape) * 4;
+}
+
+moe_status_t moe_attn_decode(const moe_attn_shape_t* shape, const void* q_dev,
+                             const void* k_cache_dev, const void* v_cache_dev,
+                             const int32_t* table_dev, int32_t n_phys, void* o_dev, void* ws_dev,
+                             size_t ws_bytes, moe_stream_t stream) {
+  if (!attn_supported(shape)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!q_dev || !k_cache_dev || !v_cache_dev || !table_dev || !o_dev || n_phys < 1 ||
+      !aligned16(q_dev) || !aligned16(k_cache_dev) || !aligned16(v_cache_dev) ||
+      !aligned16(o_dev))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws_dev || ws_bytes < moe_attn_workspace_bytes(shape)) return MOE_ERR_WORKSPACE;
+  int nsm = 0;
+  MOE_TRY(sm_count(&nsm));
+  uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  cudaError_t e = launch_attn_decode(
+      shape, static_cast<const uint16_t*>(q_dev), static_cast<const uint16_t*>(k_cache_dev),
+      static_cast<const uint16_t*>(v_cache_dev), table_dev, n_phys, static_cast<uint16_t*>(o_dev),
+      reinterpret_cast<float*>(ws + 256), reinterpret_cast<Ctrl*>(ws), nsm,
+      (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "attention launch");
+}
+
 moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
                                const moe_layer_weights_t* layers_host, const void* x_dev,
                                void* y_dev, void* x_next_dev, void* ws_dev, size_t ws_bytes,

@@ -28,7 +28,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
-enum : int { KID_PLAN = 1, KID_FFN = 2, KID_DECODE = 3, KID_ROUTE = 4 };
+enum : int { KID_PLAN = 1, KID_FFN = 2, KID_DECODE = 3, KID_ROUTE = 4, KID_ATTN = 5 };
 
 __device__ __forceinline__ void set_error(Ctrl* c, int code, int kid, int detail) {
   if (atomicCAS(&c->err, 0, code) == 0) {

@@ -147,6 +147,12 @@ cudaError_t launch_block_input(const uint16_t* h_in, const int32_t* tok, const u
                                uint16_t* x, Ctrl* ctrl, cudaStream_t stream);
 cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
                            int N, int Kd, cudaStream_t stream);
+// Grouped-query decode attention over a block-paged cache (attn_decode.cu).
+bool attn_supported(const moe_attn_shape_t* s);
+size_t attn_part_floats(const moe_attn_shape_t* s);
+cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const uint16_t* q, const uint16_t* kc,
+                               const uint16_t* vc, const int32_t* table, int n_phys, uint16_t* o,
+                               float* part, Ctrl* ctrl, int nsm, cudaStream_t stream);
 // Host helpers shared by the C-ABI translation units (api.cu keeps the state).
 bool shape_supported(const moe_shape_t* shape);
 void set_last_error(const char* text);

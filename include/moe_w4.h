@@ -299,6 +299,45 @@ moe_status_t moe_debug_dequant_w4(const uint32_t* q_dev, const uint16_t* s_dev,
 const char* moe_status_string(moe_status_t status);
 const char* moe_last_error(void);
 
+/* ----------------------------------------------------------------------
+ * Grouped-query decode attention ([Lily] "Three Workload Shapes": the
+ * model's full-attention layers have 16 query heads sharing 2 key/value
+ * heads; [Lily] "Decode": the query heads of a key/value head are packed so
+ * each cache row is loaded once, and the cache is kept in fixed-size
+ * blocks). For query token t (at position L - T + t) and head h, with
+ * g = h / (n_q / n_kv):
+ *   o[t][h] = sum_j softmax_j( q[t][h] . k_j / sqrt(D) ) v_j,  j <= L - T + t,
+ * fp32 scores and sums, P rounded to bf16 before it multiplies V, o bf16.
+ * Position j of group g is row j % block of physical block table[j / block].
+ * ---------------------------------------------------------------------- */
+typedef struct moe_attn_shape {
+  int32_t T;      /* query tokens (1 or 2), the last T positions */
+  int32_t n_q;    /* query heads */
+  int32_t n_kv;   /* key/value heads; (n_q / n_kv) * T <= 16 */
+  int32_t D;      /* head dimension: 64 or 128 */
+  int32_t L;      /* sequence length, the T query tokens included (T <= L <= 2^24) */
+  int32_t block;  /* positions per cache block: 64 */
+} moe_attn_shape_t;
+
+/* Workspace bytes of moe_attn_decode (a status word and the per-chunk
+ * partials), 0 for an unsupported shape. Zero-fill it once with
+ * moe_workspace_init; moe_query_device_status reads its status. */
+size_t moe_attn_workspace_bytes(const moe_attn_shape_t* shape);
+
+/* o = attention of q over the cache (definition above). Device pointers:
+ *  q_dev        bf16 [T][n_q][D]
+ *  k_cache_dev  bf16 [n_phys][n_kv][block][D]; v_cache_dev likewise
+ *  table_dev    int32 [ceil(L / block)]: the physical block of each logical
+ *               block; an entry outside [0, n_phys) is recorded as
+ *               MOE_ERR_BAD_INPUT and its positions are left out
+ *  o_dev        bf16 [T][n_q][D] out
+ * All bf16 pointers 16-byte aligned. Errors: MOE_ERR_UNSUPPORTED_SHAPE,
+ * MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE (too small), MOE_ERR_CUDA. */
+moe_status_t moe_attn_decode(const moe_attn_shape_t* shape, const void* q_dev,
+                             const void* k_cache_dev, const void* v_cache_dev,
+                             const int32_t* table_dev, int32_t n_phys, void* o_dev, void* ws_dev,
+                             size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
