@@ -624,12 +624,198 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------- decode attention leg --
+# The model's full-attention layers at decode: 16 query heads on 2 key/value
+# heads, head dimension H / 16 = 128, a 32K context in 64-position blocks;
+# a step is one token through the 10 attention layers (distinct caches,
+# 320 MB, more than the 129 MB L2).
+ATTN_WORKLOADS = {"attn_decode": dict(T=1, n_q=16, n_kv=2, D=128, L=32768, layers=10)}
+ATTN_METRIC = "GQA decode attention tokens/s over a 32K block-paged KV cache; % of HBM roofline"
+
+
+def attn_bytes(c):
+    """Algorithmic bytes of one layer's call: the visible keys and values,
+    the block table, q read and o written."""
+    nblk = (c["L"] + 63) // 64
+    return (c["L"] * c["n_kv"] * c["D"] * 2 * 2 + nblk * 4 + 2 * c["T"] * c["n_q"] * c["D"] * 2)
+
+
+def attn_oracle(c, budget_s=12.0, steps=0):
+    """Seconds per step of the oracle on one layer's call (scaled to the
+    step's layers by the caller); at least one call, more within budget."""
+    import oracle
+    q, k, v, tab = synth.gen_attn(c["T"], c["n_q"], c["n_kv"], c["D"], c["L"], seed=1)
+    times = []
+    while not times or (sum(times) < budget_s and len(times) < max(3, steps)):
+        t0 = time.time()
+        oracle.attn_decode(q, k, v, tab, c["L"])
+        times.append(time.time() - t0)
+    return times, oracle.num_threads()
+
+
+def run_attn(args):
+    import torch
+    name = args.workload
+    c = ATTN_WORKLOADS[name]
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times, thr = attn_oracle(c, budget_s=60.0, steps=args.warmup + args.steps)
+        times = times[args.warmup:] or times
+        v = 1.0 / (statistics.mean(times) * c["layers"])
+        cb = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+              "sample": "one layer's call per step, tokens/s divided by %d layers" % c["layers"]}
+        print(json.dumps({"impl": "reference", "metric": ATTN_METRIC, "value": v,
+                          "unit": "tokens/s", "n_gpus": args.gpus, "steps": len(times),
+                          "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "config": dict(workload=name, **c),
+                          "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_moe_expert_histogram_gb300 as m
+    m.load()
+    shape = m.make_attn_shape(c["T"], c["n_q"], c["n_kv"], c["D"], c["L"])
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa
+    layers = []
+    for l in range(c["layers"]):
+        q, k, v, tab = synth.gen_attn(c["T"], c["n_q"], c["n_kv"], c["D"], c["L"],
+                                      seed=1000 * rank + l)
+        layers.append((d(q), d(k), d(v), torch.from_numpy(tab).to(dev)))
+    ws = m.alloc_attn_workspace(shape, dev)
+    o = torch.empty((c["T"], c["n_q"], c["D"]), dtype=torch.int16, device=dev)
+
+    def step():
+        for (q, k, v, tab) in layers:
+            m.moe_attn_decode(shape, q, k, v, tab, o, ws)
+
+    q_pin = layers[0][0].cpu().pin_memory()
+    o_pin = torch.empty_like(o, device="cpu").pin_memory()
+    q_dev = torch.empty_like(layers[0][0])
+
+    def step_e2e():
+        q_dev.copy_(q_pin, non_blocking=True)
+        for (_, k, v, tab) in layers:
+            m.moe_attn_decode(shape, q_dev, k, v, tab, o, ws)
+        o_pin.copy_(o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    if m.moe_query_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+        step_e2e()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_step, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    with torch.cuda.graph(g_e2e):
+        step_e2e()
+    for _ in range(args.warmup):
+        g_step.replay()
+    stream = torch.cuda.current_stream()
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus) if rank == 0 else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0.record(stream)
+    for _ in range(args.steps):
+        g_step.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        ms = max_over_ranks(ms, dist, dev)
+    if m.moe_query_device_status(ws) != 0:
+        raise RuntimeError("device status after the timed region")
+    e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        g_e2e.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        e_ms = max_over_ranks(e_ms, dist, dev)
+    hbm, _, _, src = peaks()
+    ms_step = ms / args.steps
+    per_launch_ms = ms_step / c["layers"]
+    ub = attn_bytes(c)
+    gbs = ub / (per_launch_ms / 1e3) / 1e9
+    nblk = (c["L"] + 63) // 64
+    line = {
+        "metric": ATTN_METRIC, "value": round(job_throughput(c["T"], world, ms_step), 2),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 q/k/v -> fp32 scores and sums",
+        "data": "synthetic (seeded numpy: q, k, v N(0,1); block table a random permutation)",
+        "config": dict(workload=name, l2="no flush: %d layers' caches, %.0f MB > 129 MB L2" % (
+            c["layers"], c["layers"] * ub / 1e6), parallelism="replicas x%d" % world, **c),
+        "roofline": {"kernel": "attn_split_kernel<%d> + attn_merge_kernel, one layer's call"
+                               % c["D"],
+                     "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "peak_source": src,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4), "traffic": None,
+                     "ms_per_launch": round(per_launch_ms, 5),
+                     "algorithmic_bytes_per_launch": ub},
+        "e2e": {"value": round(job_throughput(c["T"], world, e_ms), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(q_pin.numel() * 2),
+                "d2h_bytes_per_step": int(o_pin.numel() * 2), "steps": e_steps,
+                "ms_per_step": round(e_ms, 5),
+                "mode": "CUDA graph of the q copy, the 10 moe_attn_decode calls and the read-back"},
+        "gpu_launches": 2 * c["layers"] * args.steps,
+        "launch_mode": "CUDA graph replay (split and merge kernels per layer)",
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, thr = attn_oracle(c, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": 1.0 / (statistics.mean(times) * c["layers"]),
+                                "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": "%d call(s) of one layer, scaled to %d layers"
+                                          % (len(times), c["layers"]),
+                                "seconds": round(sum(times), 3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="prefill", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="prefill",
+                    choices=sorted(synth.CONFIGS) + sorted(ATTN_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -643,6 +829,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload in ATTN_WORKLOADS:
+        run_attn(args)
+        return
     wl = synth.CONFIGS[args.workload]
     if args.layers > 0:
         wl = dataclasses.replace(wl, layers=args.layers)

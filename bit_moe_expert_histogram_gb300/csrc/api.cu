@@ -619,14 +619,21 @@ moe_status_t moe_attn_decode(const moe_attn_shape_t* shape, const void* q_dev,
       !aligned16(o_dev))
     return MOE_ERR_INVALID_ARG;
   if (!ws_dev || ws_bytes < moe_attn_workspace_bytes(shape)) return MOE_ERR_WORKSPACE;
+  if ((int64_t)n_phys * shape->n_kv * shape->block >= INT32_MAX) return MOE_ERR_INVALID_ARG;
   int nsm = 0;
   MOE_TRY(sm_count(&nsm));
   uint8_t* ws = static_cast<uint8_t*>(ws_dev);
+  // the caches as [n_phys * n_kv * block rows][D]: boxes of 64 rows x 64 elements
+  const uint64_t rows = (uint64_t)n_phys * shape->n_kv * shape->block;
+  CUtensorMap tk, tv;
+  MOE_TRY(map_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_cache_dev, shape->D, rows, 64, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B));
+  MOE_TRY(map_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, v_cache_dev, shape->D, rows, 64, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B));
   cudaError_t e = launch_attn_decode(
-      shape, static_cast<const uint16_t*>(q_dev), static_cast<const uint16_t*>(k_cache_dev),
-      static_cast<const uint16_t*>(v_cache_dev), table_dev, n_phys, static_cast<uint16_t*>(o_dev),
-      reinterpret_cast<float*>(ws + 256), reinterpret_cast<Ctrl*>(ws), nsm,
-      (cudaStream_t)stream);
+      shape, tk, tv, static_cast<const uint16_t*>(q_dev), table_dev, n_phys,
+      static_cast<uint16_t*>(o_dev), reinterpret_cast<float*>(ws + 256),
+      reinterpret_cast<Ctrl*>(ws), nsm, (cudaStream_t)stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "attention launch");
 }
 

@@ -10,13 +10,16 @@
 // j <= L - T + t, head h reading key/value head h / (n_q / n_kv).
 //
 // Split along the sequence: CTA (chunk c, group g) takes cb consecutive
-// 64-position blocks of head group g. All the group's query rows (its
-// n_q / n_kv heads times the T tokens, at most 16) form the M = 16 rows of
-// mma.sync m16n8k16 tiles, so every key and value row is read once per
-// group. A block's keys and values are copied into shared memory with
-// cp.async (two stages, 16-byte chunks XOR-swizzled by row so ldmatrix
-// reads are conflict-free); warp w takes positions 16w..16w+15 of each
-// block: S = Q K^T (fp32), an online softmax per row (exp2 of log2e-scaled
+// 64-position blocks of head group g, cb chosen so that the CTAs of all
+// groups fill the SMs once. All the group's query rows (its n_q / n_kv
+// heads times the T tokens, at most 16) form the M = 16 rows of mma.sync
+// m16n8k16 tiles, so every key and value row is read once per group. The
+// blocks' keys and values stream into shared memory by TMA through a ring
+// of six stages (boxes of 64 rows x 64 elements with the 128-byte
+// swizzle, so ldmatrix reads are conflict-free; one mbarrier per stage,
+// bounded waits); warp w takes positions 16w..16w+15 of each block
+// while the next five blocks are in flight: S = Q K^T (fp32), an online
+// softmax per row (exp2 of log2e-scaled
 // scores), P = bf16(exp2(S - m)) reused in registers as the A operand of
 // O += P V. The four warps' (max, sum, O) meet in shared memory at the end
 // of the chunk; with one chunk the output is written directly, otherwise a
@@ -31,15 +34,9 @@ constexpr int kAB = 64;       // positions per cache block
 constexpr int kAWarps = 4;    // warps per CTA; warp w: positions 16w..16w+15 of a block
 constexpr int kAThreads = 32 * kAWarps;
 constexpr int kARows = 16;    // query rows of a group (heads x tokens), the MMA's M
+constexpr int kAStages = 6;   // cache blocks in shared memory per CTA (one CTA per SM)
+constexpr int kMThreads = 256;  // merge kernel: 8 warps over the chunks
 
-__device__ __forceinline__ void cp16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -59,10 +56,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// byte offset of 16-byte chunk ch of row p in a [64][D] bf16 tile
+// byte offset of 16-byte chunk ch (elements 8ch..8ch+7) of row p in a
+// [64][D] bf16 tile stored as D/64 TMA boxes of 64 rows x 128 bytes with
+// the 128-byte swizzle (chunk c of row p at c ^ (p % 8))
 template <int D>
 __device__ __forceinline__ uint32_t swz(int p, int ch) {
-  return (uint32_t)(p * D * 2 + ((ch ^ (p & 7)) << 4));
+  return (uint32_t)((ch >> 3) * (kAB * 128) + p * 128 + (((ch & 7) ^ (p & 7)) << 4));
 }
 }  // namespace
 
@@ -70,21 +69,28 @@ __device__ __forceinline__ uint32_t swz(int p, int ch) {
 // O[row][D], fp32, at part + ((g * n_chunks + c) * 16 * (D + 2)).
 template <int D>
 __global__ void __launch_bounds__(kAThreads)
-    attn_split_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc,
-                      const uint16_t* __restrict__ vc, const int32_t* __restrict__ table,
+    attn_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const uint16_t* __restrict__ q,
+                      const int32_t* __restrict__ table,
                       int n_phys, int T, int n_q, int n_kv, int L, int cb, int n_chunks,
                       float* __restrict__ part, uint16_t* __restrict__ o, Ctrl* ctrl) {
   constexpr int kTile = kAB * D * 2;  // bytes of one block's keys (or values)
   constexpr int kKS = D / 16;         // k-steps of Q K^T
   constexpr int kDT = D / 8;          // n-tiles of O
-  extern __shared__ __align__(128) uint8_t sm[];
-  const uint32_t sbase = smem_u32(sm);  // [stage][K | V][kTile]
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  __shared__ __align__(8) uint64_t full[kAStages];  // stage landed (TMA bytes)
+  __shared__ int s_abort;
+  // [kAStages][K | V][kTile], 1024-byte aligned for the swizzle
+  const uint32_t sbase = (smem_u32(sm_raw) + 1023u) & ~1023u;
+  uint8_t* sm = sm_raw + (sbase - smem_u32(sm_raw));
   const int c = blockIdx.x, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, cq = lane & 3;
+  const int wq = warp;  // quarter of the block
   const int group = n_q / n_kv, rows = group * T;
   const int nblk = (L + kAB - 1) / kAB;
   const int b0 = c * cb, b1 = min(b0 + cb, nblk);
+  pdl_trigger();  // the merge kernel may launch now; it waits for this grid to finish
   // Q fragments (rows r = t * group + head in group; rows >= rows are zero)
   uint32_t qa[kKS][4];
   {
@@ -105,20 +111,31 @@ __global__ void __launch_bounds__(kAThreads)
   const int lim1 = gq + 8 < rows ? L - T + (gq + 8) / group : -1;
   const float sl2 = 1.4426950408889634f / sqrtf((float)D);  // log2(e) / sqrt(D)
 
-  // block b of this group into stage st (every thread its share of chunks)
+  const uint32_t fb = smem_u32(&full[0]);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAStages; ++i) mbar_init(fb + 8u * i, 1);
+    s_abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  __syncthreads();
+  const uint64_t pol = policy_evict_first();  // the cache is streamed once
+  // block b of this group into stage st (thread 0)
   auto issue = [&](int b, int st) {
     int phys = __ldg(table + b);
     if (phys < 0 || phys >= n_phys) {
-      if (threadIdx.x == 0) set_error(ctrl, MOE_ERR_BAD_INPUT, KID_ATTN, b);
+      set_error(ctrl, MOE_ERR_BAD_INPUT, KID_ATTN, b);
       phys = 0;  // read in bounds; the block's scores are masked below
     }
-    const size_t row0 = ((size_t)phys * n_kv + g) * kAB;
+    const int row0 = (phys * n_kv + g) * kAB;
     const uint32_t sk = sbase + (uint32_t)(st * 2 * kTile), sv = sk + kTile;
+    const uint32_t bar = fb + 8u * st;
+    mbar_arrive_expect_tx(bar, 2u * kTile);
 #pragma unroll
-    for (int i = threadIdx.x; i < kAB * (D / 8); i += kAThreads) {
-      const int p = i / (D / 8), ch = i - p * (D / 8);
-      cp16(sk + swz<D>(p, ch), kc + (row0 + p) * D + ch * 8);
-      cp16(sv + swz<D>(p, ch), vc + (row0 + p) * D + ch * 8);
+    for (int bx = 0; bx < D / 64; ++bx) {
+      tma_load_2d(sk + bx * (kAB * 128), &tm_k, bx * 64, row0, bar, pol);
+      tma_load_2d(sv + bx * (kAB * 128), &tm_v, bx * 64, row0, bar, pol);
     }
   };
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
@@ -126,14 +143,27 @@ __global__ void __launch_bounds__(kAThreads)
 #pragma unroll
   for (int j = 0; j < kDT; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.0f;
 
-  if (b0 < b1) issue(b0, 0);
-  cp_commit();
-  for (int b = b0; b < b1; ++b) {
-    const int st = (b - b0) & 1;
-    if (b + 1 < b1) issue(b + 1, st ^ 1);
-    cp_commit();
-    cp_wait<1>();
+  // blocks b0 .. b0 + kAStages - 2 first
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kAStages - 1 && b0 + i < b1; ++i) issue(b0 + i, i);
+  int issued = min(kAStages - 1, b1 - b0);  // blocks issued so far (thread 0's count)
+  int b = b0;
+  for (; b < b1; ++b) {
+    // this thread's reads of block b - 1 are ordered before the TMA refill
+    // of its stage, which thread 0 issues after the barrier
+    fence_proxy_async_smem();
     __syncthreads();
+    if (s_abort) break;
+    if (b + kAStages - 1 < b1) {
+      if (threadIdx.x == 0) issue(b + kAStages - 1, (b - b0 + kAStages - 1) % kAStages);
+      ++issued;
+    }
+    const int st = (b - b0) % kAStages;
+    if (!mbar_wait(fb + 8u * st, (uint32_t)((b - b0) / kAStages) & 1u, &s_abort)) {
+      // recorded once; every thread leaves at the next barrier
+      if (atomicCAS(&s_abort, 0, 1) == 0) set_error(ctrl, MOE_ERR_TIMEOUT, KID_ATTN, b);
+      continue;
+    }
     const uint32_t sk = sbase + (uint32_t)(st * 2 * kTile), sv = sk + kTile;
     int phys = __ldg(table + b);
     const bool bad = phys < 0 || phys >= n_phys;
@@ -141,7 +171,7 @@ __global__ void __launch_bounds__(kAThreads)
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
       const int mi = lane >> 3, rr = lane & 7;
-      const int p = 16 * warp + ((mi & 2) ? 8 : 0) + rr;
+      const int p = 16 * wq + ((mi & 2) ? 8 : 0) + rr;
 #pragma unroll
       for (int ks = 0; ks < kKS; ++ks) {
         uint32_t k0, k1, k2, k3;
@@ -156,7 +186,7 @@ __global__ void __launch_bounds__(kAThreads)
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int pos = b * kAB + 16 * warp + 8 * j + 2 * cq + h;
+        const int pos = b * kAB + 16 * wq + 8 * j + 2 * cq + h;
         s[j][h] = (!bad && pos <= lim0) ? s[j][h] * sl2 : -INFINITY;
         s[j][2 + h] = (!bad && pos <= lim1) ? s[j][2 + h] * sl2 : -INFINITY;
         mx0 = fmaxf(mx0, s[j][h]);
@@ -188,7 +218,7 @@ __global__ void __launch_bounds__(kAThreads)
     l1 = l1 * f1 + (bf_lo(pa1) + bf_hi(pa1)) + (bf_lo(pa3) + bf_hi(pa3));
     {
       const int mi = lane >> 3, rr = lane & 7;
-      const int pv = 16 * warp + ((mi & 1) ? 8 : 0) + rr;
+      const int pv = 16 * wq + ((mi & 1) ? 8 : 0) + rr;
 #pragma unroll
       for (int j = 0; j < kDT; j += 2) {
         oacc[j][0] *= f0; oacc[j][1] *= f0; oacc[j][2] *= f1; oacc[j][3] *= f1;
@@ -199,9 +229,18 @@ __global__ void __launch_bounds__(kAThreads)
         mma16816(oacc[j + 1], pa0, pa1, pa2, pa3, v2, v3);
       }
     }
-    __syncthreads();  // the stage is refilled by the next iteration's issue
   }
-  cp_wait<0>();
+  __syncthreads();
+  if (s_abort) {
+    // a wait ran out: wait (again bounded) for the copies that may still be
+    // in flight so none lands after the CTA exits, and leave no result
+    if (threadIdx.x == 0) {
+      volatile int never = 0;
+      for (int i = issued > kAStages ? issued - kAStages : 0; i < issued; ++i)
+        mbar_wait(fb + 8u * (i % kAStages), (uint32_t)(i / kAStages) & 1u, &never);
+    }
+    return;
+  }
   // row sums over the quad
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
   l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
@@ -256,28 +295,63 @@ __global__ void __launch_bounds__(kAThreads)
   }
 }
 
-// o from the chunks' partials, merged in chunk order: one block per
-// (group, row), thread d per output element.
+// o from the chunks' partials: one block per (group, row), one pass. Warp w
+// takes chunks w, w + 8, .. (lane: D/32 consecutive elements of O) with a
+// running maximum, loading each chunk's m, l and O slice together; the
+// eight warps' (max, sum, O) are then combined in warp order.
 template <int D>
-__global__ void __launch_bounds__(D)
+__global__ void __launch_bounds__(kMThreads)
     attn_merge_kernel(const float* __restrict__ part, int T, int n_q, int n_kv, int n_chunks,
                       uint16_t* __restrict__ o) {
-  const int g = blockIdx.x / kARows, r = blockIdx.x - g * kARows, d = threadIdx.x;
+  constexpr int kE = D / 32;  // elements per lane
+  constexpr int kW = kMThreads / 32;
+  __shared__ float wm[kW], wl[kW], wo[kW][D];
+  const int g = blockIdx.x / kARows, r = blockIdx.x - g * kARows;
   const int group = n_q / n_kv;
   if (r >= group * T) return;
-  const float* pg = part + (size_t)g * n_chunks * kARows * (D + 2);
-  float M = -INFINITY;
-  for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, pg[(size_t)c * kARows * (D + 2) + r]);
-  const float U = M == -INFINITY ? 0.0f : M;
-  float Ls = 0.0f, Os = 0.0f;
-  for (int c = 0; c < n_chunks; ++c) {
-    const float* pc = pg + (size_t)c * kARows * (D + 2);
-    const float f = exp2f(pc[r] - U);
-    Ls += pc[kARows + r] * f;
-    Os += pc[2 * kARows + (size_t)r * D + d] * f;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t stride = (size_t)kARows * (D + 2);
+  pdl_wait();  // the split kernel's partials are complete and visible
+  const float* pg = part + (size_t)g * n_chunks * stride;
+  float M = -INFINITY, Ls = 0.0f, acc[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) acc[e] = 0.0f;
+#pragma unroll 4
+  for (int c = warp; c < n_chunks; c += kW) {
+    const float* pc = pg + c * stride;
+    const float mc = __ldcg(pc + r), lc = __ldcg(pc + kARows + r);
+    float oc[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) oc[e] = __ldcg(pc + 2 * kARows + (size_t)r * D + lane * kE + e);
+    const float nM = fmaxf(M, mc);
+    const float U = nM == -INFINITY ? 0.0f : nM;
+    const float fo = exp2f(M - U), fc = exp2f(mc - U);
+    Ls = Ls * fo + lc * fc;
+#pragma unroll
+    for (int e = 0; e < kE; ++e) acc[e] = acc[e] * fo + oc[e] * fc;
+    M = nM;
   }
-  o[((size_t)(r / group) * n_q + g * group + r % group) * D + d] =
-      (uint16_t)f2bf(Ls > 0.0f ? Os / Ls : 0.0f);
+  if (lane == 0) {
+    wm[warp] = M;
+    wl[warp] = Ls;
+  }
+#pragma unroll
+  for (int e = 0; e < kE; ++e) wo[warp][lane * kE + e] = acc[e];
+  __syncthreads();
+  float MM = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) MM = fmaxf(MM, wm[w]);
+  const float U = MM == -INFINITY ? 0.0f : MM;
+  float L = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) L += wl[w] * exp2f(wm[w] - U);
+  for (int d = threadIdx.x; d < D; d += kMThreads) {
+    float Os = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) Os += wo[w][d] * exp2f(wm[w] - U);
+    o[((size_t)(r / group) * n_q + g * group + r % group) * D + d] =
+        (uint16_t)f2bf(L > 0.0f ? Os / L : 0.0f);
+  }
 }
 
 bool attn_supported(const moe_attn_shape_t* s) {
@@ -290,9 +364,9 @@ bool attn_supported(const moe_attn_shape_t* s) {
 }
 
 size_t attn_smem(int D) {
-  const size_t stages = (size_t)2 * 2 * kAB * D * 2;
+  const size_t stages = (size_t)kAStages * 2 * kAB * D * 2;
   const size_t merge = (size_t)kAWarps * kARows * (2 + D) * 4;
-  return stages > merge ? stages : merge;
+  return (stages > merge ? stages : merge) + 1024;  // + the alignment of the stages
 }
 
 size_t attn_part_floats(const moe_attn_shape_t* s) {
@@ -300,16 +374,36 @@ size_t attn_part_floats(const moe_attn_shape_t* s) {
   return (size_t)s->n_kv * nblk * kARows * (s->D + 2);
 }
 
-cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const uint16_t* q, const uint16_t* kc,
-                               const uint16_t* vc, const int32_t* table, int n_phys, uint16_t* o,
-                               float* part, Ctrl* ctrl, int nsm, cudaStream_t stream) {
+// The merge kernel with programmatic stream serialisation: it is scheduled
+// while the split kernel runs and waits in pdl_wait for its results.
+template <int D>
+cudaError_t launch_merge(const float* part, const moe_attn_shape_t* s, int n_chunks, uint16_t* o,
+                         size_t msmem, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s->n_kv * kARows);
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = msmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<D>, part, s->T, s->n_q, s->n_kv, n_chunks, o);
+}
+
+cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const uint16_t* q, const int32_t* table,
+                               int n_phys, uint16_t* o, float* part, Ctrl* ctrl, int nsm,
+                               cudaStream_t stream) {
   const int nblk = (s->L + kAB - 1) / kAB;
-  // chunks of whole blocks, about two CTAs per SM over both groups
-  const int want = 2 * nsm;
+  // chunks of whole blocks, one CTA per SM over all groups
+  const int want = nsm;
   int cb = (nblk * s->n_kv + want - 1) / want;
   cb = cb < 1 ? 1 : cb;
   const int n_chunks = (nblk + cb - 1) / cb;
   const size_t smem = attn_smem(s->D);
+  const size_t msmem = 0;
   dim3 grid(n_chunks, s->n_kv);
   cudaError_t e;
   if (s->D == 64) {
@@ -317,19 +411,17 @@ cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const uint16_t* q, con
                              (int)smem);
     if (e != cudaSuccess) return e;
     attn_split_kernel<64><<<grid, kAThreads, smem, stream>>>(
-        q, kc, vc, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
-    if (n_chunks > 1)
-      attn_merge_kernel<64><<<s->n_kv * kARows, 64, 0, stream>>>(part, s->T, s->n_q, s->n_kv,
-                                                                  n_chunks, o);
+        tm_k, tm_v, q, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
+    if (n_chunks > 1) e = launch_merge<64>(part, s, n_chunks, o, msmem, stream);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
     if (e != cudaSuccess) return e;
     attn_split_kernel<128><<<grid, kAThreads, smem, stream>>>(
-        q, kc, vc, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
-    if (n_chunks > 1)
-      attn_merge_kernel<128><<<s->n_kv * kARows, 128, 0, stream>>>(part, s->T, s->n_q, s->n_kv,
-                                                                    n_chunks, o);
+        tm_k, tm_v, q, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
+    if (n_chunks > 1) e = launch_merge<128>(part, s, n_chunks, o, msmem, stream);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -150,9 +150,12 @@ cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t*
 // Grouped-query decode attention over a block-paged cache (attn_decode.cu).
 bool attn_supported(const moe_attn_shape_t* s);
 size_t attn_part_floats(const moe_attn_shape_t* s);
-cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const uint16_t* q, const uint16_t* kc,
-                               const uint16_t* vc, const int32_t* table, int n_phys, uint16_t* o,
-                               float* part, Ctrl* ctrl, int nsm, cudaStream_t stream);
+// tm_k / tm_v: the caches as [n_phys * n_kv * 64 rows][D] bf16, boxes of
+// 64 rows x 64 elements, 128-byte swizzle
+cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const uint16_t* q, const int32_t* table,
+                               int n_phys, uint16_t* o, float* part, Ctrl* ctrl, int nsm,
+                               cudaStream_t stream);
 // Host helpers shared by the C-ABI translation units (api.cu keeps the state).
 bool shape_supported(const moe_shape_t* shape);
 void set_last_error(const char* text);
