@@ -22,8 +22,11 @@
 // softmax per row (exp2 of log2e-scaled
 // scores), P = bf16(exp2(S - m)) reused in registers as the A operand of
 // O += P V. The four warps' (max, sum, O) meet in shared memory at the end
-// of the chunk; with one chunk the output is written directly, otherwise a
-// second kernel merges the chunks' partials in chunk order.
+// of the chunk; with one chunk the output is written directly. Otherwise
+// the chunks (at most one CTA per SM over all groups, every CTA resident:
+// a cooperative launch) write partials, meet at a grid barrier, and merge
+// them: each CTA takes 32 output elements of one query row, its four warps
+// a quarter of the chunks each.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -35,7 +38,6 @@ constexpr int kAWarps = 4;    // warps per CTA; warp w: positions 16w..16w+15 of
 constexpr int kAThreads = 32 * kAWarps;
 constexpr int kARows = 16;    // query rows of a group (heads x tokens), the MMA's M
 constexpr int kAStages = 6;   // cache blocks in shared memory per CTA (one CTA per SM)
-constexpr int kMThreads = 256;  // merge kernel: 8 warps over the chunks
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -90,7 +92,6 @@ __global__ void __launch_bounds__(kAThreads)
   const int group = n_q / n_kv, rows = group * T;
   const int nblk = (L + kAB - 1) / kAB;
   const int b0 = c * cb, b1 = min(b0 + cb, nblk);
-  pdl_trigger();  // the merge kernel may launch now; it waits for this grid to finish
   // Q fragments (rows r = t * group + head in group; rows >= rows are zero)
   uint32_t qa[kKS][4];
   {
@@ -293,64 +294,79 @@ __global__ void __launch_bounds__(kAThreads)
       pc[2 * kARows + (size_t)r * D + d] = Os;
     }
   }
-}
-
-// o from the chunks' partials: one block per (group, row), one pass. Warp w
-// takes chunks w, w + 8, .. (lane: D/32 consecutive elements of O) with a
-// running maximum, loading each chunk's m, l and O slice together; the
-// eight warps' (max, sum, O) are then combined in warp order.
-template <int D>
-__global__ void __launch_bounds__(kMThreads)
-    attn_merge_kernel(const float* __restrict__ part, int T, int n_q, int n_kv, int n_chunks,
-                      uint16_t* __restrict__ o) {
-  constexpr int kE = D / 32;  // elements per lane
-  constexpr int kW = kMThreads / 32;
-  __shared__ float wm[kW], wl[kW], wo[kW][D];
-  const int g = blockIdx.x / kARows, r = blockIdx.x - g * kARows;
-  const int group = n_q / n_kv;
-  if (r >= group * T) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t stride = (size_t)kARows * (D + 2);
-  pdl_wait();  // the split kernel's partials are complete and visible
-  const float* pg = part + (size_t)g * n_chunks * stride;
-  float M = -INFINITY, Ls = 0.0f, acc[kE];
-#pragma unroll
-  for (int e = 0; e < kE; ++e) acc[e] = 0.0f;
-#pragma unroll 4
-  for (int c = warp; c < n_chunks; c += kW) {
-    const float* pc = pg + c * stride;
-    const float mc = __ldcg(pc + r), lc = __ldcg(pc + kARows + r);
-    float oc[kE];
-#pragma unroll
-    for (int e = 0; e < kE; ++e) oc[e] = __ldcg(pc + 2 * kARows + (size_t)r * D + lane * kE + e);
-    const float nM = fmaxf(M, mc);
-    const float U = nM == -INFINITY ? 0.0f : nM;
-    const float fo = exp2f(M - U), fc = exp2f(mc - U);
-    Ls = Ls * fo + lc * fc;
-#pragma unroll
-    for (int e = 0; e < kE; ++e) acc[e] = acc[e] * fo + oc[e] * fc;
-    M = nM;
-  }
-  if (lane == 0) {
-    wm[warp] = M;
-    wl[warp] = Ls;
-  }
-#pragma unroll
-  for (int e = 0; e < kE; ++e) wo[warp][lane * kE + e] = acc[e];
+  if (n_chunks == 1) return;
+  // ---- grid barrier: every CTA's partials are written and visible
+  __threadfence();
   __syncthreads();
-  float MM = -INFINITY;
+  if (threadIdx.x == 0) {
+    volatile unsigned* gen = &ctrl->attn_gen;
+    const unsigned g0 = *gen;
+    const unsigned G = gridDim.x * gridDim.y;
+    if (atomicAdd(&ctrl->attn_arrive, 1u) == G - 1u) {
+      ctrl->attn_arrive = 0u;
+      __threadfence();
+      atomicAdd(&ctrl->attn_gen, 1u);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      while (*gen == g0) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_error(ctrl, MOE_ERR_TIMEOUT, KID_ATTN, -1);
+          s_abort = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  if (s_abort) return;
+  // ---- merge: task = (group, row, 32 elements); warp w takes chunks w, w+4, ..
+  // with a running maximum, then warp 0 combines the four in warp order
+  float* mm = reinterpret_cast<float*>(sm);  // [warp]: max, sum; then [warp][32] O
+  float* ml = mm + kAWarps;
+  float* mo = ml + kAWarps;
+  const int tasks = n_kv * rows * (D / 32);
+  const int cid = blockIdx.y * gridDim.x + blockIdx.x, G = gridDim.x * gridDim.y;
+  const size_t stride = (size_t)kARows * (D + 2);
+  for (int task = cid; task < tasks; task += G) {
+    const int pr = task / (D / 32), dsl = task - pr * (D / 32);
+    const int gg = pr / rows, r = pr - gg * rows, d = dsl * 32 + lane;
+    const float* pg = part + (size_t)gg * n_chunks * stride;
+    float M = -INFINITY, Ls = 0.0f, Os = 0.0f;
+#pragma unroll 8
+    for (int cc = warp; cc < n_chunks; cc += kAWarps) {
+      const float* pc = pg + cc * stride;
+      const float mc = __ldcg(pc + r), lc = __ldcg(pc + kARows + r);
+      const float oc = __ldcg(pc + 2 * kARows + (size_t)r * D + d);
+      const float nM = fmaxf(M, mc);
+      const float U = nM == -INFINITY ? 0.0f : nM;
+      const float fo = exp2f(M - U), fc = exp2f(mc - U);
+      Ls = Ls * fo + lc * fc;
+      Os = Os * fo + oc * fc;
+      M = nM;
+    }
+    if (lane == 0) {
+      mm[warp] = M;
+      ml[warp] = Ls;
+    }
+    mo[warp * 32 + lane] = Os;
+    __syncthreads();
+    if (warp == 0) {
+      float MM = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kW; ++w) MM = fmaxf(MM, wm[w]);
-  const float U = MM == -INFINITY ? 0.0f : MM;
-  float L = 0.0f;
+      for (int w = 0; w < kAWarps; ++w) MM = fmaxf(MM, mm[w]);
+      const float U = MM == -INFINITY ? 0.0f : MM;
+      float L = 0.0f, O = 0.0f;
 #pragma unroll
-  for (int w = 0; w < kW; ++w) L += wl[w] * exp2f(wm[w] - U);
-  for (int d = threadIdx.x; d < D; d += kMThreads) {
-    float Os = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) Os += wo[w][d] * exp2f(wm[w] - U);
-    o[((size_t)(r / group) * n_q + g * group + r % group) * D + d] =
-        (uint16_t)f2bf(L > 0.0f ? Os / L : 0.0f);
+      for (int w = 0; w < kAWarps; ++w) {
+        const float f = exp2f(mm[w] - U);
+        L += ml[w] * f;
+        O += mo[w * 32 + lane] * f;
+      }
+      o[((size_t)(r / group) * n_q + gg * group + r % group) * D + d] =
+          (uint16_t)f2bf(L > 0.0f ? O / L : 0.0f);
+    }
+    __syncthreads();
   }
 }
 
@@ -374,56 +390,41 @@ size_t attn_part_floats(const moe_attn_shape_t* s) {
   return (size_t)s->n_kv * nblk * kARows * (s->D + 2);
 }
 
-// The merge kernel with programmatic stream serialisation: it is scheduled
-// while the split kernel runs and waits in pdl_wait for its results.
-template <int D>
-cudaError_t launch_merge(const float* part, const moe_attn_shape_t* s, int n_chunks, uint16_t* o,
-                         size_t msmem, cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(s->n_kv * kARows);
-  cfg.blockDim = dim3(kMThreads);
-  cfg.dynamicSmemBytes = msmem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_merge_kernel<D>, part, s->T, s->n_q, s->n_kv, n_chunks, o);
-}
-
 cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const CUtensorMap& tm_k,
                                const CUtensorMap& tm_v, const uint16_t* q, const int32_t* table,
                                int n_phys, uint16_t* o, float* part, Ctrl* ctrl, int nsm,
                                cudaStream_t stream) {
   const int nblk = (s->L + kAB - 1) / kAB;
-  // chunks of whole blocks, one CTA per SM over all groups
-  const int want = nsm;
-  int cb = (nblk * s->n_kv + want - 1) / want;
-  cb = cb < 1 ? 1 : cb;
+  // chunks of whole blocks, at most one CTA per SM over all groups
+  const int per_group = nsm / s->n_kv > 1 ? nsm / s->n_kv : 1;
+  const int cb = (nblk + per_group - 1) / per_group;
   const int n_chunks = (nblk + cb - 1) / cb;
   const size_t smem = attn_smem(s->D);
-  const size_t msmem = 0;
-  dim3 grid(n_chunks, s->n_kv);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_chunks, s->n_kv);
+  cfg.blockDim = dim3(kAThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n_chunks > 1 ? 1 : 0;  // the grid barrier needs every CTA resident
   cudaError_t e;
   if (s->D == 64) {
     e = cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-    if (e != cudaSuccess) return e;
-    attn_split_kernel<64><<<grid, kAThreads, smem, stream>>>(
-        tm_k, tm_v, q, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
-    if (n_chunks > 1) e = launch_merge<64>(part, s, n_chunks, o, msmem, stream);
-    if (e != cudaSuccess) return e;
+    if (e == cudaSuccess)
+      e = cudaLaunchKernelEx(&cfg, attn_split_kernel<64>, tm_k, tm_v, q, table, n_phys, s->T,
+                             s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
   } else {
     e = cudaFuncSetAttribute(attn_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-    if (e != cudaSuccess) return e;
-    attn_split_kernel<128><<<grid, kAThreads, smem, stream>>>(
-        tm_k, tm_v, q, table, n_phys, s->T, s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
-    if (n_chunks > 1) e = launch_merge<128>(part, s, n_chunks, o, msmem, stream);
-    if (e != cudaSuccess) return e;
+    if (e == cudaSuccess)
+      e = cudaLaunchKernelEx(&cfg, attn_split_kernel<128>, tm_k, tm_v, q, table, n_phys, s->T,
+                             s->n_q, s->n_kv, s->L, cb, n_chunks, part, o, ctrl);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

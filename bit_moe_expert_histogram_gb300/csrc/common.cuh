@@ -24,7 +24,9 @@ struct Ctrl {
   unsigned ps_seq;   // persistent decode: launches so far (epoch base of the next one)
   unsigned ps_exit;  // persistent decode: blocks finished (reset by the last one)
   unsigned ps_abort; // persistent decode: a wait ran out; every block stops waiting
-  int pad[52];
+  unsigned attn_arrive;  // attention: CTAs at the grid barrier (reset by the last)
+  unsigned attn_gen;     // attention: grid barriers passed
+  int pad[50];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
