@@ -784,7 +784,8 @@ def run_attn(args):
         "roofline": {"kernel": "attn_split_kernel<%d> + attn_merge_kernel, one layer's call"
                                % c["D"],
                      "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "peak_source": src,
-                     "unit": "GB/s", "frac": round(gbs / hbm, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "traffic": measured_traffic(name),
                      "ms_per_launch": round(per_launch_ms, 5),
                      "algorithmic_bytes_per_launch": ub},
         "e2e": {"value": round(job_throughput(c["T"], world, e_ms), 2), "unit": "tokens/s",
