@@ -56,6 +56,7 @@ def lib():
             L.orc_layer_tokens.argtypes = [P, i, i, i, i, P, P] + [P] * 12 + [P, i, P, P]
             L.orc_rmsnorm_rows.argtypes = [P, i, i, P]
             L.orc_rmsnorm_gain_rows.argtypes = [P, P, i, i, P]
+            L.orc_gdn_scan.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, P]
             L.orc_attn_decode.restype = i
             L.orc_attn_decode.argtypes = [P, P, P, P, i, i, i, i, i, i, i, P]
             L.orc_residual_add.argtypes = [P, P, C.c_size_t, P]
@@ -230,6 +231,25 @@ def attn_decode(q, k_cache, v_cache, table, L):
                              D, int(L), B, _p(o)) != 0:
         raise ValueError("oracle attention: block table entry out of range")
     return o
+
+
+def gdn_scan(q, k, v, alpha, beta, state):
+    """Gated delta rule over T tokens: returns (o [T][n_v][dv] bf16 bits,
+    the final state [n_v][dv][dk] fp32). q, k [T][n_k][dk], v [T][n_v][dv]
+    bf16 bits; alpha, beta [T][n_v] fp32; state [n_v][dv][dk] fp32."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    alpha = _c(alpha, np.float32)
+    beta = _c(beta, np.float32)
+    state = _c(state, np.float32)
+    T, n_k, dk = q.shape
+    n_v, dv = v.shape[1], v.shape[2]
+    o = np.empty((T, n_v, dv), np.uint16)
+    s_out = np.empty_like(state)
+    lib().orc_gdn_scan(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(state), T, n_k, n_v, dk, dv,
+                       _p(s_out), _p(o))
+    return o, s_out
 
 
 def route(L, K):

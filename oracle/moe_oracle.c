@@ -491,6 +491,53 @@ int orc_attn_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
   return 0;
 }
 
+/* The fixed-size recurrence of the model's 30 Gated DeltaNet layers [P3
+ * "Three Workload Shapes"; the pages name a register-resident scan, P3
+ * "Prefill"] in the published gated delta rule (Yang, Kautz, Hatamizadeh,
+ * "Gated Delta Networks: Improving Mamba2 with Delta Rule"), fp64: per
+ * value head h (key head h / (n_v / n_k)), state S [dv][dk], and token t
+ *   S <- alpha_t S (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *   o_t = S q_t   (RNE to bf16).
+ * q, k [T][n_k][dk] and v [T][n_v][dv] are bf16 bits; alpha, beta [T][n_v]
+ * and the states [n_v][dv][dk] are fp32 (s_out may equal s_in). */
+void orc_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                  const float* beta, const float* s_in, int T, int n_k, int n_v, int dk, int dv,
+                  float* s_out, uint16_t* o) {
+  const int group = n_v / n_k;
+  double* S = (double*)malloc(sizeof(double) * (size_t)dv * dk);
+  double* Sk = (double*)malloc(sizeof(double) * (size_t)dv);
+  for (int h = 0; h < n_v; ++h) {
+    const int hk = h / group;
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) S[i] = s_in[(size_t)h * dv * dk + i];
+    for (int t = 0; t < T; ++t) {
+      const uint16_t* kt = k + ((size_t)t * n_k + hk) * dk;
+      const uint16_t* qt = q + ((size_t)t * n_k + hk) * dk;
+      const uint16_t* vt = v + ((size_t)t * n_v + h) * dv;
+      const double a = alpha[(size_t)t * n_v + h], b = beta[(size_t)t * n_v + h];
+      /* S k, then S <- a S - a b (S k) k^T + b v k^T */
+      for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * orc_bf16_value(kt[j]);
+        Sk[i] = acc;
+      }
+      for (int i = 0; i < dv; ++i)
+        for (int j = 0; j < dk; ++j) {
+          const double kj = orc_bf16_value(kt[j]);
+          S[(size_t)i * dk + j] =
+              a * S[(size_t)i * dk + j] - a * b * Sk[i] * kj + b * orc_bf16_value(vt[i]) * kj;
+        }
+      for (int i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * orc_bf16_value(qt[j]);
+        o[((size_t)t * n_v + h) * dv + i] = orc_bf16_rne(acc);
+      }
+    }
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) s_out[(size_t)h * dv * dk + i] = (float)S[i];
+  }
+  free(S);
+  free(Sk);
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

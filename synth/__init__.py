@@ -12,6 +12,7 @@ from .gen import (  # noqa: F401
     bf16_bits_to_f32,
     gen_attn,
     gen_embed,
+    gen_gdn,
     gen_gain,
     gen_layer,
     gen_tokens,

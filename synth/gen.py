@@ -131,3 +131,22 @@ def gen_attn(T, n_q, n_kv, D, L, B=64, seed=0, spare=3):
     v = bf16_bits(rng.standard_normal((n_phys, n_kv, B, D)))
     table = rng.permutation(n_phys)[:nblk].astype(np.int32)
     return q, k, v, table
+
+
+def gen_gdn(T, n_k, n_v, dk, dv, seed=0):
+    """Gated-DeltaNet scan inputs: q, k unit vectors per head (bf16 of a
+    normalised N(0, 1) draw), v ~ N(0, 1) bf16, decay alpha ~ U[0.9, 1),
+    write strength beta ~ U[0, 1) (fp32), and a starting state
+    ~ N(0, 0.1^2) fp32 [n_v][dv][dk]."""
+    rng = np.random.default_rng(seed)
+
+    def unit(shape):
+        a = rng.standard_normal(shape)
+        return bf16_bits(a / np.linalg.norm(a, axis=-1, keepdims=True))
+    q = unit((T, n_k, dk))
+    k = unit((T, n_k, dk))
+    v = bf16_bits(rng.standard_normal((T, n_v, dv)))
+    alpha = rng.uniform(0.9, 1.0, (T, n_v)).astype(np.float32)
+    beta = rng.uniform(0.0, 1.0, (T, n_v)).astype(np.float32)
+    state = (0.1 * rng.standard_normal((n_v, dv, dk))).astype(np.float32)
+    return q, k, v, alpha, beta, state

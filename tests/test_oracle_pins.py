@@ -443,3 +443,51 @@ def test_attn_causal_window_and_paging():
     assert np.array_equal(oracle.attn_decode(q, k2, v2, perm[table], L), o2)
     with pytest.raises(ValueError):
         oracle.attn_decode(q, k, v, np.full_like(table, k.shape[0]), L)
+
+
+# ------------------------------------------ Gated DeltaNet recurrence --
+def test_gdn_pure_decay_and_exact_write():
+    """beta = 0 leaves alpha-scaled states (o = the decayed state times q);
+    alpha = beta = 1 with k a basis vector e_j replaces column j of the
+    state by v and keeps the others (the delta rule's exact write)."""
+    T, n_k, n_v, dk, dv = 3, 2, 4, 16, 8
+    q, k, v, alpha, beta, s0 = synth.gen_gdn(T, n_k, n_v, dk, dv, seed=21)
+    beta0 = np.zeros_like(beta)
+    o, s1 = oracle.gdn_scan(q, k, v, alpha, beta0, s0)
+    decay = np.prod(alpha.astype(np.float64), axis=0)  # [n_v]
+    assert np.allclose(s1, s0 * decay[:, None, None], rtol=1e-6)
+    qf = synth.bf16_bits_to_f32(q).astype(np.float64)
+    exp_o = np.einsum("hij,hj->hi", s0 * decay[:, None, None], qf[-1][np.arange(n_v) // 2])
+    got = synth.bf16_bits_to_f32(o[-1]).astype(np.float64)
+    assert np.abs(got - exp_o).max() <= 2 ** -8 * np.abs(exp_o).max()
+    j = 5
+    kb = np.zeros((1, n_k, dk)); kb[..., j] = 1.0
+    ones = np.ones((1, n_v), np.float32)
+    _, s2 = oracle.gdn_scan(q[:1], synth.bf16_bits(kb), v[:1], ones, ones, s0)
+    vf = synth.bf16_bits_to_f32(v[0]).astype(np.float32)
+    assert np.array_equal(s2[:, :, j], vf)
+    keep = [c for c in range(dk) if c != j]
+    assert np.array_equal(s2[:, :, keep], s0[:, :, keep])
+
+
+def test_gdn_matches_the_matrix_form_in_torch():
+    """The recurrence as matrices in torch float64, S (alpha (I - beta k k^T))
+    + beta v k^T, token by token, with each value head reading key head
+    h // (n_v / n_k)."""
+    T, n_k, n_v, dk, dv = 5, 2, 4, 16, 12
+    q, k, v, alpha, beta, s0 = synth.gen_gdn(T, n_k, n_v, dk, dv, seed=22)
+    o, s_end = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    S = torch.from_numpy(s0.astype(np.float64))
+    qf = torch.from_numpy(synth.bf16_bits_to_f32(q).astype(np.float64))
+    kf = torch.from_numpy(synth.bf16_bits_to_f32(k).astype(np.float64))
+    vf = torch.from_numpy(synth.bf16_bits_to_f32(v).astype(np.float64))
+    eye = torch.eye(dk, dtype=torch.float64)
+    for t in range(T):
+        for h in range(n_v):
+            kk = kf[t, h // 2]
+            a, b = float(alpha[t, h]), float(beta[t, h])
+            S[h] = S[h] @ (a * (eye - b * torch.outer(kk, kk))) + b * torch.outer(vf[t, h], kk)
+        ref = torch.einsum("hij,hj->hi", S, qf[t][torch.arange(n_v) // 2]).numpy()
+        got = synth.bf16_bits_to_f32(o[t]).astype(np.float64)
+        assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max()
+    assert np.allclose(s_end, S.numpy(), rtol=1e-5, atol=1e-6)
