@@ -31,7 +31,8 @@ EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_r
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
            "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
            "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers",
-           "moe_decoder_blocks", "moe_attn_workspace_bytes", "moe_attn_decode")
+           "moe_decoder_blocks", "moe_attn_workspace_bytes", "moe_attn_decode",
+           "moe_gdn_scan")
 
 
 class MoeError(RuntimeError):
@@ -55,6 +56,11 @@ class Shape(C.Structure):
 class AttnShape(C.Structure):
     _fields_ = [("T", C.c_int32), ("n_q", C.c_int32), ("n_kv", C.c_int32), ("D", C.c_int32),
                 ("L", C.c_int32), ("block", C.c_int32)]
+
+
+class GdnShape(C.Structure):
+    _fields_ = [("T", C.c_int32), ("n_k", C.c_int32), ("n_v", C.c_int32), ("dk", C.c_int32),
+                ("dv", C.c_int32)]
 
 
 class W4Weights(C.Structure):
@@ -107,7 +113,8 @@ def load():
                     ("moe_plan_noalloc", [pS, P, pP, P]),
                     ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P]),
                     ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P]),
-                    ("moe_attn_decode", [C.POINTER(AttnShape), P, P, P, P, I32, P, P, SZ, P])):
+                    ("moe_attn_decode", [C.POINTER(AttnShape), P, P, P, P, I32, P, P, SZ, P]),
+                    ("moe_gdn_scan", [C.POINTER(GdnShape), P, P, P, P, P, P, P, P, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -228,6 +235,16 @@ def moe_attn_decode(shape, q, k_cache, v_cache, table, o, ws, stream=None):
     _check(load().moe_attn_decode(C.byref(shape), _p(q), _p(k_cache), _p(v_cache), _p(table),
                                   k_cache.shape[0], _p(o), _p(ws), ws.numel(), _s(stream)),
            "moe_attn_decode")
+
+
+def make_gdn_shape(T, n_k, n_v, dk, dv):
+    return GdnShape(T, n_k, n_v, dk, dv)
+
+
+def moe_gdn_scan(shape, q, k, v, alpha, beta, state_in, state_out, o, stream=None):
+    """Gated delta rule over shape.T tokens (state_out may be state_in)."""
+    _check(load().moe_gdn_scan(C.byref(shape), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
+                               _p(state_in), _p(state_out), _p(o), _s(stream)), "moe_gdn_scan")
 
 
 def gain_table(gains):

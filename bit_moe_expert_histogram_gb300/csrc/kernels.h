@@ -156,6 +156,11 @@ cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const CUtensorMap& tm_
                                const CUtensorMap& tm_v, const uint16_t* q, const int32_t* table,
                                int n_phys, uint16_t* o, float* part, Ctrl* ctrl, int nsm,
                                cudaStream_t stream);
+// Gated delta rule scan (gdn_scan.cu).
+bool gdn_supported(const moe_gdn_shape_t* s);
+cudaError_t launch_gdn_scan(const moe_gdn_shape_t* s, const uint16_t* q, const uint16_t* k,
+                            const uint16_t* v, const float* alpha, const float* beta,
+                            const float* s_in, float* s_out, uint16_t* o, cudaStream_t stream);
 // Host helpers shared by the C-ABI translation units (api.cu keeps the state).
 bool shape_supported(const moe_shape_t* shape);
 void set_last_error(const char* text);

@@ -338,6 +338,38 @@ moe_status_t moe_attn_decode(const moe_attn_shape_t* shape, const void* q_dev,
                              const int32_t* table_dev, int32_t n_phys, void* o_dev, void* ws_dev,
                              size_t ws_bytes, moe_stream_t stream);
 
+/* ----------------------------------------------------------------------
+ * The Gated DeltaNet recurrence ([Lily] "Three Workload Shapes": 30 of the
+ * 40 layers are Gated DeltaNet, a fixed-size recurrence; [Lily] "Prefill":
+ * a register-resident scan), in the published gated delta rule: for value
+ * head h (key head h / (n_v / n_k)), state S [dv][dk] and t = 0 .. T-1
+ *   S <- alpha_t S (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *   o_t = S q_t,
+ * fp32 state and arithmetic, o bf16. The q/k projections, their
+ * normalisation and the gates are the caller's (inputs here).
+ * ---------------------------------------------------------------------- */
+typedef struct moe_gdn_shape {
+  int32_t T;    /* tokens, scanned in order */
+  int32_t n_k;  /* key heads */
+  int32_t n_v;  /* value heads, a multiple of n_k */
+  int32_t dk;   /* key dimension: 128 */
+  int32_t dv;   /* value dimension: a multiple of 16 */
+} moe_gdn_shape_t;
+
+/* Device pointers:
+ *  q_dev, k_dev       bf16 [T][n_k][dk]
+ *  v_dev              bf16 [T][n_v][dv]
+ *  alpha_dev, beta_dev fp32 [T][n_v]
+ *  state_in_dev       fp32 [n_v][dv][dk]; state_out_dev likewise, may be
+ *                     state_in_dev (updated in place)
+ *  o_dev              bf16 [T][n_v][dv] out
+ * All 16-byte aligned. Errors: MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_INVALID_ARG,
+ * MOE_ERR_CUDA. */
+moe_status_t moe_gdn_scan(const moe_gdn_shape_t* shape, const void* q_dev, const void* k_dev,
+                          const void* v_dev, const float* alpha_dev, const float* beta_dev,
+                          const float* state_in_dev, float* state_out_dev, void* o_dev,
+                          moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
