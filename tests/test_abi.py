@@ -145,3 +145,62 @@ def test_workspace_of_the_chunked_prefill_fits_two_gib(lib):
     n2 = m.moe_workspace_bytes(m.make_shape(4096, 2048, 256, 8, 512, 1, 128))
     n1 = m.moe_workspace_bytes(m.make_shape(1, 2048, 256, 8, 512, 1, 128))
     assert n2 <= 2 * n + n1
+
+
+def test_attention_workspace_and_argument_errors(lib):
+    """Host checks of moe_attn_decode, in order: the shape, the pointers,
+    the workspace size; none reaches the device."""
+    ok = m.make_attn_shape(1, 16, 2, 128, 32768)
+    n = lib.moe_attn_workspace_bytes(C.byref(ok))
+    # the status word and the partials of at most one chunk per cache block
+    assert n == 256 + 2 * 512 * 16 * (128 + 2) * 4
+    for bad in [(3, 16, 2, 128, 100), (1, 16, 3, 128, 100), (1, 16, 2, 96, 100),
+                (2, 16, 1, 128, 100), (1, 16, 2, 128, 0), (1, 16, 2, 128, 100, 32)]:
+        s = m.make_attn_shape(*bad)
+        assert lib.moe_attn_workspace_bytes(C.byref(s)) == 0
+        assert lib.moe_attn_decode(C.byref(s), None, None, None, None, 1, None, None, 0,
+                                   None) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    p = C.c_void_p(0x10000)
+    assert lib.moe_attn_decode(C.byref(ok), None, p, p, p, 1, p, p, n,
+                               None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_attn_decode(C.byref(ok), C.c_void_p(0x10008), p, p, p, 1, p, p, n,
+                               None) == m.MOE_ERR_INVALID_ARG  # q not 16-byte aligned
+    assert lib.moe_attn_decode(C.byref(ok), p, p, p, p, 0, p, p, n,
+                               None) == m.MOE_ERR_INVALID_ARG  # an empty block pool
+    assert lib.moe_attn_decode(C.byref(ok), p, p, p, p, 1, p, p, n - 1,
+                               None) == m.MOE_ERR_WORKSPACE
+
+
+def test_gdn_scan_argument_errors(lib):
+    p = C.c_void_p(0x10000)
+    for bad in [(1, 16, 32, 64, 128), (1, 16, 24, 128, 128), (1, 16, 32, 128, 40),
+                (0, 16, 32, 128, 128), (1, 0, 32, 128, 128)]:
+        s = m.make_gdn_shape(*bad)
+        assert lib.moe_gdn_scan(C.byref(s), p, p, p, p, p, p, p, p,
+                                None) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    ok = m.make_gdn_shape(4, 16, 32, 128, 128)
+    assert lib.moe_gdn_scan(C.byref(ok), p, p, p, p, None, p, p, p,
+                            None) == m.MOE_ERR_INVALID_ARG
+    assert lib.moe_gdn_scan(C.byref(ok), p, p, p, p, p, C.c_void_p(0x10004), p, p,
+                            None) == m.MOE_ERR_INVALID_ARG  # the state not 16-byte aligned
+
+
+def test_decoder_blocks_argument_errors(lib):
+    s = m.make_shape(1, 256, 16, 2, 128, 1, 128)
+    table = (m.LayerWeights * 1)()
+    gains = (C.c_void_p * 1)(0x10000)
+    out = C.c_void_p(0x20000)
+    call = lambda shape, n, tab, g, h_in, tok, emb, vocab, h_out, wsb=0: lib.moe_decoder_blocks(
+        C.byref(shape), n, tab, g, h_in, tok, emb, vocab, h_out, None, wsb, None)
+    T = C.cast(table, C.c_void_p)
+    G = C.cast(gains, C.c_void_p)
+    bad_shape = m.make_shape(1, 100, 16, 2, 128, 1, 128)  # H not a multiple of 256
+    assert call(bad_shape, 1, T, G, out, None, None, 0, out) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert call(s, 0, T, G, out, None, None, 0, out) == m.MOE_ERR_INVALID_ARG     # no layers
+    assert call(s, 1, T, None, out, None, None, 0, out) == m.MOE_ERR_INVALID_ARG  # no gains
+    assert call(s, 1, T, G, None, None, None, 0, out) == m.MOE_ERR_INVALID_ARG   # no h_0
+    tok = C.c_void_p(0x30000)
+    assert call(s, 1, T, G, None, tok, None, 10, out) == m.MOE_ERR_INVALID_ARG   # ids, no table
+    assert call(s, 1, T, G, None, tok, out, 0, out) == m.MOE_ERR_INVALID_ARG     # empty table
+    # the layer table itself: a router pointer is required
+    assert call(s, 1, T, G, out, None, None, 0, out) == m.MOE_ERR_INVALID_ARG
