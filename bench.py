@@ -12,13 +12,20 @@ synthetic tokens with all weights resident in HBM. Workloads (synth.CONFIGS):
   tiny     T=16, H=256, 16 experts top-2 + 1 shared, I=128
 Weights of every layer (455.8 MB for the full shape) exceed the 129 MB L2,
 so no L2 flush is needed between steps; config says so.
+  attn_decode  one token through the 10 full-attention layers: 16 query
+               heads on 2 KV heads, D=128, a 32K block-paged cache each
+               (moe_attn_decode; 336 MB of caches, more than L2)
+Options: --block (decode: decoder blocks fed token ids, moe_decoder_blocks),
+--tile-rows N (the grouped GEMMs' most tokens per tile), --layers N.
 
 Prints one JSON line (rank 0). value = tokens/s of the whole job; e2e =
-the same through moe_layer_w4 with the step's hidden states copied from
+the same through the public calls with the step's inputs copied from
 pinned host memory and the output copied back inside the timed region;
-roofline = the expert-FFN call (both grouped GEMMs) against the measured
-HBM copy bandwidth; cpu_baseline = the CPU oracle on a bounded sample.
---impl reference times the CPU oracle itself on the same workload.
+roofline = the dominant launch (the expert-FFN call, the persistent decode
+launch, or one attention call) against the measured HBM copy bandwidth or,
+past the ridge, the measured bf16 tensor peak; cpu_baseline = the CPU
+oracle on a bounded sample. --impl reference times the CPU oracle itself
+on the same workload.
 """
 import argparse
 import dataclasses
