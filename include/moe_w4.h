@@ -332,7 +332,10 @@ size_t moe_attn_workspace_bytes(const moe_attn_shape_t* shape);
  *               MOE_ERR_BAD_INPUT and its positions are left out
  *  o_dev        bf16 [T][n_q][D] out
  * All bf16 pointers 16-byte aligned. Errors: MOE_ERR_UNSUPPORTED_SHAPE,
- * MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE (too small), MOE_ERR_CUDA. */
+ * MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE (too small), MOE_ERR_CUDA. A wait
+ * that runs out on the device (MOE_ERR_TIMEOUT from moe_query_device_status)
+ * can leave the workspace's grid-barrier counter mid-count: re-initialise
+ * the workspace (moe_workspace_init) before the next call. */
 moe_status_t moe_attn_decode(const moe_attn_shape_t* shape, const void* q_dev,
                              const void* k_cache_dev, const void* v_cache_dev,
                              const int32_t* table_dev, int32_t n_phys, void* o_dev, void* ws_dev,
