@@ -1,0 +1,76 @@
+"""The bench's CPU-side contract: the reference arm (the oracle timed on the
+host) prints one JSON line with the keys the driver reads, for a MoE
+workload and for the attention leg; the roofline bound follows the ridge of
+the measured peaks; the workload table covers every leg."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+import bench
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+        "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+        "cpu_baseline", "e2e"}
+
+
+def run_reference(workload):
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          workload, "--steps", "1", "--warmup", "1"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line_for_a_moe_workload():
+    d = run_reference("tiny")
+    assert KEYS <= set(d)
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+    assert d["config"]["workload"] == "tiny"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_line_for_the_attention_leg():
+    d = run_reference("attn_decode")
+    assert KEYS <= set(d)
+    assert d["config"]["workload"] == "attn_decode" and d["config"]["L"] == 32768
+    assert d["value"] > 0 and d["higher_is_better"] is True
+
+
+def test_algorithmic_counts():
+    """Bytes of an expert, the layer's bytes and FLOPs from a histogram, and
+    the attention call's bytes, from their definitions."""
+    H, I = 2048, 512
+    # packed nibbles (0.5 B per weight) and two bf16 per 64-weight group
+    assert bench.expert_bytes(H, I) == 3 * H * I // 2 + 2 * 2 * (3 * H * I // 64)
+    S = synth.CONFIGS["prefill"].shape
+    counts = np.zeros(S.E, np.int64)
+    counts[:3] = [10, 5, 1]
+    algo, flops, ffn_bytes, ffn_flops = bench.layer_algo(16, S, counts)
+    assert ffn_bytes == 4 * bench.expert_bytes(S.H, S.I) + 16 * S.H * 2 * 2
+    assert ffn_flops == 2 * 3 * S.I * S.H * (16 * S.K + 16)
+    assert flops == ffn_flops + 2 * S.E * S.H * 16
+    c = bench.ATTN_WORKLOADS["attn_decode"]
+    assert bench.attn_bytes(c) == c["L"] * 2 * 128 * 4 + 512 * 4 + 2 * 16 * 128 * 2
+
+
+def test_tensor_or_hbm_bound_by_the_ridge():
+    """At T=512 the grouped GEMMs sit below the ridge of the measured peaks
+    (HBM-bound); a Zipf T=2048 layer with about 140 touched experts sits
+    above it (tensor-bound)."""
+    hbm, bf16, _, _ = bench.peaks()
+    ridge = bf16 * 1e3 / hbm
+    S = synth.CONFIGS["prefill"].shape
+    uniform = np.full(S.E, 16)
+    _, _, b512, f512 = bench.layer_algo(512, S, uniform)
+    assert f512 / b512 < ridge
+    skew = np.zeros(S.E, np.int64)
+    skew[:140] = 2048 * S.K // 140
+    _, _, b2k, f2k = bench.layer_algo(2048, S, skew)
+    assert f2k / b2k > ridge
