@@ -42,7 +42,9 @@
 // accumulator pair (freed by the epilogue). Roles that mostly wait sleep in their barrier waits. Every
 // wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains what
 // it started, frees TMEM and returns. Before exit the MMA thread waits for
-// the arrival of every commit it issued.
+// the arrival of every commit it issued; if that wait itself runs out, the
+// tensor pipe has stopped, and the CTA records MOE_ERR_TIMEOUT and leaves
+// its TMEM columns allocated rather than free columns MMAs may still write.
 #include <atomic>
 
 #include "common.cuh"
@@ -90,7 +92,7 @@ __host__ __device__ constexpr int b_uempty(int q) { return 2 * kNW + 2 * kNS + k
 constexpr int kBarAccFull = 2 * kNW + 2 * kNS + 2 * kNU;
 constexpr int kBarAccEmpty = kBarAccFull + 1;
 constexpr int kNumBars = kBarAccEmpty + 1;
-constexpr int kRingOff = kNumBars * 8 + 8;  // unit queue (ints) after the barriers
+constexpr int kRingOff = kNumBars * 8 + 16;  // unit queue (ints) after the barrier words
 static_assert(kRingOff + 4 * kNU <= 512, "barrier area");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sW = sbase + kSmemW, sB = sbase + kSmemB, sBar = sbase + kSmemBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kSmemBar + kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kSmemBar + kNumBars * 8 + 4);
+  volatile int* tmem_keep = abort_flag + 1;  // set when the MMA drain timed out
   volatile int* ring = reinterpret_cast<volatile int*>(gbase + kSmemBar + kRingOff);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarAccFull), 1);
     mbar_init(bar(kBarAccEmpty), kEpiWarps);
     *abort_flag = 0;
+    *tmem_keep = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -369,9 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // commit targets, so no arrive can land after this CTA has exited (and
       // all MMAs are complete before TMEM is released).
       volatile int never = 0;
+      bool drained = true;
       for (uint32_t i = it > (uint32_t)kNS ? it - kNS : 0u; i < it; ++i)
-        mbar_wait(bar(b_sfree(i % kNS)), (i / kNS) & 1u, &never);
-      if (committed > 0) mbar_wait(bar(kBarAccFull), (committed - 1) & 1u, &never);
+        drained &= mbar_wait(bar(b_sfree(i % kNS)), (i / kNS) & 1u, &never);
+      if (committed > 0) drained &= mbar_wait(bar(kBarAccFull), (committed - 1) & 1u, &never);
+      if (!drained) {
+        // an MMA commit is still pending after the wait limit: the tensor
+        // pipe has stopped. Its MMAs may still write TMEM, so the columns
+        // are not released (the context is unusable after this anyway).
+        set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 6);
+        *tmem_keep = 1;
+      }
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue --
@@ -518,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 2 && !*tmem_keep) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -2,9 +2,10 @@
 // scatter of (token, slot) rows into expert-contiguous order, and the tile
 // block map ("Perplexity Open Sources Lily: A Rust + Metal Inference Engine
 // for Qwen3.6-35B-A3B on Apple Silicon", section "Prefill: Keep Weights
-// Packed, Keep Routing on the GPU": the routing histogram, prefix scan,
-// scatter and block map stay on the GPU, with no CPU synchronisation inside
-// the layer). Integer work only: results are unique and deterministic.
+// Packed, Keep Routing on the GPU": every step that turns expert ids into
+// the grouped GEMM's schedule runs as device kernels, and the host never
+// waits on the device between them). Integer work only: results are unique
+// and deterministic.
 //
 // Two launches. plan_hist: block c counts the experts of items
 // [c*CH, (c+1)*CH) into hist[c][E]. plan_scatter: block c derives the

@@ -11,7 +11,10 @@
 //
 // The array's name in host code is only a host-side handle; its device
 // address is looked up once per device with cudaGetSymbolAddress, with that
-// device current, on the first call made on that device.
+// device current, on the first call made on that device, and cached for the
+// life of the process. A cudaDeviceReset unloads the module, so the array
+// may come back at another address: the cached one is then stale, and this
+// entry point must not be called on that device again in the process.
 #include <mutex>
 
 #include "common.cuh"

@@ -234,7 +234,7 @@ moe_status_t moe_decode_layers(const moe_shape_t* shape, int32_t n_layers,
  * residual stream of a decode step; the pre-norm and residual add are the
  * plainest reading of the block around a layer of the pages' model, which
  * they name but do not spell out; the token feed follows [Lily] "Decode":
- * the chosen token goes straight into the next step's GPU-resident input).
+ * the sampled token id stays on the device and feeds the next step).
  * For l = 0 .. n_layers-1:
  *   x_l     = bf16(gain_l[n] * h_l[n] / sqrt(mean_n(h_l[n]^2) + 1e-6))
  *   y_l     = layer l on x_l (router, top-K, experts, combine, as
@@ -275,8 +275,10 @@ moe_status_t moe_decoder_blocks(const moe_shape_t* shape, int32_t n_layers,
  * ceil(T*K/2048) * E <= 65472, else MOE_ERR_UNSUPPORTED_SHAPE (text in
  * moe_last_error()) before anything is enqueued. The first call on a device
  * looks up that array's device address (cudaGetSymbolAddress, with the
- * device current), so make it before any stream capture. It allocates and
- * frees nothing. All calls share the one array: calls that can overlap on
+ * device current) and caches it for the life of the process, so make that
+ * call before any stream capture, and do not call this entry point on a
+ * device after cudaDeviceReset there (the cached address may be stale). It
+ * allocates and frees nothing. All calls share the one array: calls that can overlap on
  * the GPU (other streams, other host threads) race and must be ordered by
  * the caller. Expert ids outside [0, E) are skipped, as in moe_plan, but are
  * not reported. */

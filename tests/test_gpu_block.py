@@ -2,8 +2,8 @@
 the pre-norm with a learned gain, the layer, the residual add, and the token
 feed from device memory ("Perplexity Open Sources Lily: A Rust + Metal
 Inference Engine for Qwen3.6-35B-A3B on Apple Silicon", section "Decode:
-Minimize Bytes Moved Per Token": the chosen token goes straight into the
-next step's GPU-resident input). Each layer is checked against the oracle
+Minimize Bytes Moved Per Token": the sampled token id stays on the device
+and feeds the next step). Each layer is checked against the oracle
 teacher-forced on the device's residual stream; launches, aliasing, the
 embedding gather and a captured decode loop are checked bit for bit."""
 import numpy as np

@@ -45,6 +45,8 @@ def test_noalloc_plan_equals_workspace_plan_on_two_calls(lib):
                                   C.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == m.MOE_OK, lib.moe_last_error()
         torch.cuda.synchronize()
+        # the reference plan (moe_plan, through its workspace) saw no error;
+        # moe_plan_noalloc reports none by design
         assert m.moe_query_device_status(ws) == 0
         nb = int(ref.num_blocks.item())
         assert int(got.num_blocks.item()) == nb
@@ -60,3 +62,38 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
     st = lib.moe_plan_noalloc(C.byref(shape), C.c_void_p(16), C.byref(plan), None)
     assert st == m.MOE_ERR_UNSUPPORTED_SHAPE
     assert b"static scratch" in lib.moe_last_error()
+
+
+def test_noalloc_skips_bad_ids_like_moe_plan(lib):
+    """Ids outside [0, E) (here -1 and E) are left out of the plan by both
+    calls: counts, offsets, the sorted rows that exist, row_pos of every
+    valid item and the block map must still agree bit for bit."""
+    dev = torch.device("cuda")
+    T, E, K, bm = 200, 32, 4, 16
+    shape = m.make_shape(T, 256, E, K, 128, 1, bm)
+    ids_np = _ids(T, E, K, 5)
+    ids_np[3, 1] = -1
+    ids_np[77, 0] = E
+    ids_np[199, 3] = -1
+    ids = torch.from_numpy(ids_np).to(dev)
+    ws = m.alloc_workspace(shape, dev)
+    ref = m.PlanBuffers(shape, dev)
+    m.moe_plan(shape, ids, ref, ws)
+    got = m.PlanBuffers(shape, dev)
+    st = lib.moe_plan_noalloc(C.byref(shape), C.c_void_p(ids.data_ptr()), C.byref(got.ptrs),
+                              C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == m.MOE_OK, lib.moe_last_error()
+    torch.cuda.synchronize()
+    # the workspace plan records the bad ids in its status word
+    assert m.moe_query_device_status(ws) == m.MOE_ERR_BAD_INPUT
+    valid = ((ids_np >= 0) & (ids_np < E)).reshape(-1)
+    n_valid = int(valid.sum())
+    assert torch.equal(got.counts, ref.counts)
+    assert torch.equal(got.offsets, ref.offsets)
+    assert int(ref.offsets[E].item()) == n_valid
+    assert torch.equal(got.sorted_rows[:n_valid], ref.sorted_rows[:n_valid])
+    vi = torch.from_numpy(np.nonzero(valid)[0]).to(dev)
+    assert torch.equal(got.row_pos[vi], ref.row_pos[vi])
+    nb = int(ref.num_blocks.item())
+    assert int(got.num_blocks.item()) == nb
+    assert torch.equal(got.block_map[:3 * nb], ref.block_map[:3 * nb])
