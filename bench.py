@@ -18,6 +18,11 @@ so no L2 flush is needed between steps; config says so.
 Options: --block (decode: decoder blocks fed token ids, moe_decoder_blocks),
 --tile-rows N (the grouped GEMMs' most tokens per tile), --layers N.
 
+The default run (prefill) also times the decode and skewed workloads after
+the headline, with the same --steps/--warmup, and reports each under
+"legs" with its own value, per-step spread, roofline, e2e and clocks
+(--no-legs skips them).
+
 Prints one JSON line (rank 0). value = tokens/s of the whole job; e2e =
 the same through the public calls with the step's inputs copied from
 pinned host memory and the output copied back inside the timed region;
@@ -353,11 +358,12 @@ class GpuWorkload:
     def launches_per_step(self):
         """Kernel launches of one step: the persistent decode kernel runs up
         to 48 layers per launch; the per-layer decode path launches route,
-        gate_up, down per layer; otherwise route 2, plan 2, ffn 2, combine 1."""
+        gate_up, down per layer; otherwise route 2, plan 2, activation
+        gather 1, ffn 2, combine 1."""
         calls = self.n_chunks * len(self.layers)
         if self.persistent:
             return -(-len(self.layers) // 48)
-        return (3 if self.fused else 7) * calls
+        return (3 if self.fused else 8) * calls
 
     def capture(self):
         """CUDA graphs of the device step and of the host-buffer step (the
@@ -444,21 +450,24 @@ class GpuWorkload:
         return self.plan.counts.cpu().numpy()
 
 
-def run_ours(args, wl):
+def step_spread(times_ms):
+    """Median, quartiles and extremes of per-step CUDA-event times (ms)."""
+    if not times_ms:
+        return None
+    q = np.percentile(np.asarray(times_ms, dtype=np.float64), [25, 50, 75])
+    return {"median": round(float(q[1]), 5), "p25": round(float(q[0]), 5),
+            "p75": round(float(q[2]), 5), "iqr": round(float(q[2] - q[0]), 5),
+            "min": round(float(min(times_ms)), 5), "max": round(float(max(times_ms)), 5),
+            "n": len(times_ms)}
+
+
+def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
+    """Time one workload on this rank: warm-up, exactly args.steps timed steps
+    (CUDA events on the launching stream, one pair per step and one around
+    all of them), the end-to-end copy-in/copy-out variant, the dominant
+    launch's roofline, and (rank 0 at N=1) the oracle on a bounded sample.
+    Returns the JSON fields of the workload."""
     import torch
-    import torch.distributed as dist
-
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import bit_moe_expert_histogram_gb300 as m
-    m.load()
-
     G = GpuWorkload(wl, dev, m, tile_rows=args.tile_rows, rank=rank, block=args.block)
     counts = G.realised_counts()
     algo_bytes, flops, ffn_bytes, ffn_flops = layer_algo(G.T, wl.shape, counts)
@@ -482,40 +491,40 @@ def run_ours(args, wl):
     sampler = ClockSampler(bus) if rank == 0 else None
     ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    if G.fused:
+        G.capture()
+        for _ in range(args.warmup):
+            G.g_step.replay()
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    if G.fused:
-        G.capture()
-        for _ in range(args.warmup):
-            G.g_step.replay()
-        torch.cuda.synchronize()
-    t0.record(stream)
+    step_ev[0].record(stream)
     for i in range(args.steps):
         if G.fused:
             G.g_step.replay()
         else:
             G.step(ffn_ev[i])
-    t1.record(stream)
+        step_ev[i + 1].record(stream)
     torch.cuda.synchronize()
-    if sampler:
-        clocks = sampler.stop()
-    else:
-        clocks = None
+    clocks = sampler.stop() if sampler else None
     if world > 1:
         dist.barrier()
-    ms = t0.elapsed_time(t1)
+    ms = step_ev[0].elapsed_time(step_ev[-1])
+    per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     if G.persistent:  # the unit is one launch of the persistent kernel (all layers)
         ffn_ms = ms / args.steps / G.launches_per_step()
+        ffn_each = [t / G.launches_per_step() for t in per_step]
     elif G.fused:  # the unit is one layer call of the graph (3 kernels)
         ffn_ms = ms / args.steps / len(G.layers)
+        ffn_each = [t / len(G.layers) for t in per_step]
     else:
-        ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
+        ffn_each = [a.elapsed_time(b) for a, b in ffn_ev]
+        ffn_ms = statistics.mean(ffn_each)
     if world > 1:
         ms = max_over_ranks(ms, dist, dev)
     st = m.moe_query_device_status(G.ws)
@@ -552,23 +561,14 @@ def run_ours(args, wl):
     ms_step = ms / args.steps
     value = job_throughput(G.tokens_per_step, world, ms_step)
     line = {
-        "metric": METRIC,
         "value": round(value, 2),
         "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 x u4 -> fp32 accumulate",
-        "data": "synthetic (seeded numpy: hidden N(0,1), router N(0,1/H), nibbles U{0..15}, "
-                "scales U[0.002,0.02], bias -8*scale)",
+        "step_ms": step_spread(per_step),
         "config": {"workload": wl.name, "T": wl.T, "layers": wl.layers,
                    "chunks": G.n_chunks, "H": wl.shape.H, "E": wl.shape.E, "K": wl.shape.K,
                    "I": wl.shape.I, "n_shared": wl.shape.n_shared, "tile_rows": args.tile_rows,
-                   "block": bool(args.block),
+                   "block": bool(args.block), "zipf_s": wl.zipf_s,
                    "l2": "no flush: weights %.1f MB per layer > 129 MB L2" %
                          (len(G.layers) and (wl.shape.E + wl.shape.n_shared) *
                           expert_bytes(wl.shape.H, wl.shape.I) / 1e6),
@@ -622,9 +622,65 @@ def run_ours(args, wl):
     full = wl.layers == synth.CONFIGS[wl.name].layers and args.tile_rows == 128
     line["roofline"].update({"traffic": measured_traffic(wl.name if full else ""),
                              "ms_per_launch": round(ffn_ms, 5),
+                             "launch_ms": step_spread(ffn_each),
                              "algorithmic_bytes_per_launch": unit_bytes})
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_budget)
+    if rank == 0 and world == 1 and cpu_budget > 0:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=cpu_budget)
+    del G
+    torch.cuda.empty_cache()
+    return line
+
+
+# The graded workloads timed beside the headline in one default run: the
+# headline (prefill T=512) plus decode (T=1 through 40 layers) and the
+# Zipf-skewed T=2048 layer.
+LEGS = ("decode", "skewed")
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_moe_expert_histogram_gb300 as m
+    m.load()
+
+    budget = 0.0 if args.no_cpu_baseline else args.cpu_budget
+    head = measure_workload(args, wl, dev, m, rank, world, dist, budget)
+    line = {
+        "metric": METRIC,
+        "value": head.pop("value"),
+        "unit": head.pop("unit"),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head.pop("ms_per_step"),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 x u4 -> fp32 accumulate",
+        "data": "synthetic (seeded numpy: hidden N(0,1), router N(0,1/H), nibbles U{0..15}, "
+                "scales U[0.002,0.02], bias -8*scale)",
+    }
+    line.update(head)
+    run_legs = (not args.no_legs and wl.name == "prefill" and args.layers == 0
+                and not args.block and args.tile_rows == 128)
+    if run_legs:
+        legs = {}
+        for name in LEGS:
+            lw = synth.CONFIGS[name]
+            legs[name] = measure_workload(args, lw, dev, m, rank, world, dist,
+                                          min(budget, 6.0))
+            legs[name]["steps"] = args.steps
+            legs[name]["warmup"] = args.warmup
+        line["legs"] = legs
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -826,6 +882,8 @@ def main():
                     choices=sorted(synth.CONFIGS) + sorted(ATTN_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="prefill: skip the decode and skewed legs timed after the headline")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="stacked layers (default: the workload's); a smaller case for profilers")

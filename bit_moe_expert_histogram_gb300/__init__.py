@@ -8,7 +8,8 @@ library has not been built, load() raises.
 
 Names follow the C ABI: moe_route, moe_plan, moe_expert_ffn_w4,
 moe_combine, moe_layer_w4, moe_workspace_bytes, moe_max_blocks,
-moe_workspace_init, moe_query_device_status, moe_debug_dequant_w4.
+moe_workspace_init, moe_query_device_status, moe_debug_dequant_w4,
+moe_debug_dequant_w4_decode.
 """
 import ctypes as C
 import os
@@ -29,7 +30,8 @@ MOE_ERR_TIMEOUT = 6
 
 EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_route",
            "moe_plan", "moe_expert_ffn_w4", "moe_combine", "moe_layer_w4",
-           "moe_query_device_status", "moe_debug_dequant_w4", "moe_status_string",
+           "moe_query_device_status", "moe_debug_dequant_w4", "moe_debug_dequant_w4_decode",
+           "moe_status_string",
            "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers",
            "moe_decoder_blocks", "moe_attn_workspace_bytes", "moe_attn_decode",
            "moe_gdn_scan")
@@ -110,6 +112,7 @@ def load():
                     ("moe_layer_w4", [pS, P, P, P, pW, pW, P, P, P, P, P, SZ, P]),
                     ("moe_query_device_status", [P, SZ, P]),
                     ("moe_debug_dequant_w4", [P, P, P, P, I32, I32, P]),
+                    ("moe_debug_dequant_w4_decode", [P, P, P, P, I32, I32, P]),
                     ("moe_plan_noalloc", [pS, P, pP, P]),
                     ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P]),
                     ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P]),
@@ -287,6 +290,13 @@ def moe_debug_dequant_w4(q, s, b, out, stream=None):
     N, K8 = q.shape
     _check(load().moe_debug_dequant_w4(_p(q), _p(s), _p(b), _p(out), N, K8 * 8, _s(stream)),
            "moe_debug_dequant_w4")
+
+
+def moe_debug_dequant_w4_decode(q, s, b, out, stream=None):
+    N, K8 = q.shape
+    _check(load().moe_debug_dequant_w4_decode(_p(q), _p(s), _p(b), _p(out), N, K8 * 8,
+                                              _s(stream)),
+           "moe_debug_dequant_w4_decode")
 
 
 # ----------------------------------------------------- device-side holders --

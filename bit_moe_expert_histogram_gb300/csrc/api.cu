@@ -728,8 +728,18 @@ moe_status_t moe_debug_dequant_w4(const uint32_t* q_dev, const uint16_t* s_dev,
   if (!q_dev || !s_dev || !b_dev || !out_dev || N < 1 || Kd < 64 || Kd % 64 != 0)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(out_dev) || (int64_t)N * Kd >= INT32_MAX) return MOE_ERR_INVALID_ARG;
-  cudaError_t e = launch_dequant(q_dev, s_dev, b_dev, out_dev, N, Kd, (cudaStream_t)stream);
+  cudaError_t e = launch_dequant(q_dev, s_dev, b_dev, out_dev, N, Kd, false, (cudaStream_t)stream);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_debug_dequant_w4 launch");
+}
+
+moe_status_t moe_debug_dequant_w4_decode(const uint32_t* q_dev, const uint16_t* s_dev,
+                                         const uint16_t* b_dev, uint16_t* out_dev, int32_t N,
+                                         int32_t Kd, moe_stream_t stream) {
+  if (!q_dev || !s_dev || !b_dev || !out_dev || N < 1 || Kd < 64 || Kd % 64 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(out_dev) || (int64_t)N * Kd >= INT32_MAX) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_dequant(q_dev, s_dev, b_dev, out_dev, N, Kd, true, (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_debug_dequant_w4_decode launch");
 }
 
 const char* moe_status_string(moe_status_t status) {

@@ -173,11 +173,36 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ q, const uint16_t* _
   }
 }
 
+// Debug: the same with the decode kernels' routine (dequant_word_i4), its
+// (i, i+4) pairs put back into natural element order.
+__global__ void dequant_i4_kernel(const uint32_t* __restrict__ q, const uint16_t* __restrict__ s,
+                                  const uint16_t* __restrict__ b, uint16_t* __restrict__ out,
+                                  int N, int Kd) {
+  const size_t words = (size_t)N * (Kd / 8);
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < words;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t n = i / (Kd / 8), wi = i % (Kd / 8);
+    const size_t g = n * (Kd / 64) + wi / 8;
+    const uint32_t s2 = s[g] | ((uint32_t)s[g] << 16);
+    const uint32_t b2 = b[g] | ((uint32_t)b[g] << 16);
+    uint32_t p[4];
+    dequant_word_i4(q[i], s2, b2, p);
+    // p[j] = (e_j, e_j+4): natural pairs (e0,e1), (e2,e3) from the low
+    // halves, (e4,e5), (e6,e7) from the high halves
+    reinterpret_cast<uint4*>(out)[i] =
+        make_uint4(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410),
+                   __byte_perm(p[0], p[1], 0x7632), __byte_perm(p[2], p[3], 0x7632));
+  }
+}
+
 cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
-                           int N, int Kd, cudaStream_t stream) {
+                           int N, int Kd, bool decode_routine, cudaStream_t stream) {
   const size_t words = (size_t)N * (Kd / 8);
   const int grid = (int)((words + 255) / 256 < 4096 ? (words + 255) / 256 : 4096);
-  dequant_kernel<<<grid, 256, 0, stream>>>(q, s, b, out, N, Kd);
+  if (decode_routine)
+    dequant_i4_kernel<<<grid, 256, 0, stream>>>(q, s, b, out, N, Kd);
+  else
+    dequant_kernel<<<grid, 256, 0, stream>>>(q, s, b, out, N, Kd);
   return cudaGetLastError();
 }
 

@@ -53,28 +53,46 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 __device__ __forceinline__ uint32_t f2bf(float f) { return pack_bf2(f, 0.0f) & 0xFFFFu; }
 
 // ------------------------------------------------------------- dequant --
-// Groupwise-affine 4-bit dequantisation of one packed word: 8 nibbles
-// (element i = bits 4i..4i+3) -> 4 bf16x2 words holding elements (0,1),
-// (2,3), (4,5), (6,7), each bf16(s*q + b) with one rounding ("Perplexity
-// Open Sources Lily: A Rust + Metal Inference Engine for Qwen3.6-35B-A3B on
-// Apple Silicon", section "Prefill: Keep Weights Packed, Keep Routing on the
-// GPU": 64 weights per group share a bf16 scale and bias).
-// s2 / b2 hold the group's scale / bias in both halves.
-// Step 1: byte-permute nibble i into the low bits of a half and OR the
-// exponent pattern of 128.0 -> the bf16 value 128 + q (exact). Step 2:
-// fma(., 1, -128) -> q exactly. Step 3: fma(q, s, b): exact product and
-// sum, one round-to-nearest-even to bf16.
+// Groupwise-affine 4-bit dequantisation ("Perplexity Open Sources Lily: A
+// Rust + Metal Inference Engine for Qwen3.6-35B-A3B on Apple Silicon",
+// section "Prefill: Keep Weights Packed, Keep Routing on the GPU": 64
+// weights per group share a bf16 scale and bias; w = scale*q + bias).
+//
+// affine_pair: two nibbles already placed in bits 0..3 of each 16-bit half
+// of m (every other bit zero) -> the bf16x2 pair (s*q_lo + b, s*q_hi + b),
+// each with one rounding. s2 / b2 hold the group's scale / bias in both
+// halves. Step 1: OR the exponent pattern of 128.0 -> the bf16 value 128 + q
+// (exact). Step 2: fma(., 1, -128) -> q exactly. Step 3: fma(q, s, b): exact
+// product and sum, one round-to-nearest-even to bf16. Every routine below
+// differs from the others only in which two nibbles it places in m.
+__device__ __forceinline__ uint32_t affine_pair(uint32_t m, uint32_t s2, uint32_t b2) {
+  uint32_t q, r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;"
+      : "=r"(q)
+      : "r"(m | 0x43004300u), "r"(0x3F803F80u), "r"(0xC300C300u));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(s2), "r"(b2));
+  return r;
+}
+
+// One packed word (element i = bits 4i..4i+3) -> 4 bf16x2 words holding the
+// natural pairs (0,1), (2,3), (4,5), (6,7): a byte permute brings nibbles
+// 2i and 2i+1 into the low bits of the two halves.
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2,
                                              uint32_t out[4]) {
   const uint32_t w4 = w >> 4;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t p = __byte_perm(w, w4, 0x0400u + 0x0101u * i);
-    uint32_t m = (p & 0x000F000Fu) | 0x43004300u;
-    uint32_t q;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(m), "r"(0x3F803F80u), "r"(0xC300C300u));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out[i]) : "r"(q), "r"(s2), "r"(b2));
+    const uint32_t p = __byte_perm(w, w4, 0x0400u + 0x0101u * i);
+    out[i] = affine_pair(p & 0x000F000Fu, s2, b2);
   }
+}
+
+// The same word -> 4 bf16x2 words where word i holds elements i (low half)
+// and i+4 (high half): one shift and one mask place both nibbles.
+__device__ __forceinline__ void dequant_word_i4(uint32_t w, uint32_t s2, uint32_t b2,
+                                                uint32_t out[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = affine_pair((w >> (4 * i)) & 0x000F000Fu, s2, b2);
 }
 
 __device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }

@@ -12,21 +12,6 @@
 
 namespace moe {
 
-// 8 nibbles -> 4 bf16x2 words; word i holds elements i (low half) and i+4
-// (high half), each bf16(s*q + b) with one rounding: the arithmetic of
-// dequant_word, paired (i, i+4) so that one shift and one mask place both
-// nibbles.
-__device__ __forceinline__ void dequant_word_i4(uint32_t w, uint32_t s2, uint32_t b2,
-                                                uint32_t out[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t m = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-    uint32_t q;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(m), "r"(0x3F803F80u), "r"(0xC300C300u));
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out[i]) : "r"(q), "r"(s2), "r"(b2));
-  }
-}
-
 // acc + lo(p)*half(xa) + hi(p)*half(xb), half = low (HI=0) or high (HI=1):
 // fp32 fma with bf16 operands (the product is exact, one rounding per fma,
 // the same result as converting both operands to fp32 first).

@@ -145,8 +145,10 @@ cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, cons
 cudaError_t launch_block_input(const uint16_t* h_in, const int32_t* tok, const uint16_t* embed,
                                int vocab, const uint16_t* gain, int T, int H, uint16_t* h0_out,
                                uint16_t* x, Ctrl* ctrl, cudaStream_t stream);
+// decode_routine: the decode kernels' dequant_word_i4 (pairs put back into
+// natural order) instead of the grouped GEMMs' dequant_word
 cudaError_t launch_dequant(const uint32_t* q, const uint16_t* s, const uint16_t* b, uint16_t* out,
-                           int N, int Kd, cudaStream_t stream);
+                           int N, int Kd, bool decode_routine, cudaStream_t stream);
 // Grouped-query decode attention over a block-paged cache (attn_decode.cu).
 bool attn_supported(const moe_attn_shape_t* s);
 size_t attn_part_floats(const moe_attn_shape_t* s);

@@ -296,6 +296,14 @@ moe_status_t moe_debug_dequant_w4(const uint32_t* q_dev, const uint16_t* s_dev,
                                   const uint16_t* b_dev, uint16_t* out_dev, int32_t N,
                                   int32_t Kd, moe_stream_t stream);
 
+/* The same with the decode kernels' routine, which rebuilds elements i and
+ * i+4 of each packed word as one pair; the output is put back into natural
+ * element order, so it must equal moe_debug_dequant_w4's bit for bit. Same
+ * arguments and errors. Test use. */
+moe_status_t moe_debug_dequant_w4_decode(const uint32_t* q_dev, const uint16_t* s_dev,
+                                         const uint16_t* b_dev, uint16_t* out_dev, int32_t N,
+                                         int32_t Kd, moe_stream_t stream);
+
 /* Static text of a status code; text of the last CUDA error seen by this
  * thread's calls ("" if none). */
 const char* moe_status_string(moe_status_t status);

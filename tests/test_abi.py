@@ -113,6 +113,10 @@ def test_argument_errors_before_any_launch(lib):
         m.MOE_ERR_INVALID_ARG
     assert lib.moe_debug_dequant_w4(P(16), P(16), P(16), P(16), 4, 100, None) == \
         m.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_dequant_w4_decode(P(16), P(16), P(16), P(16), 4, 100, None) == \
+        m.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_dequant_w4_decode(P(16), P(16), P(16), P(24), 4, 64, None) == \
+        m.MOE_ERR_INVALID_ARG
 
 
 def test_status_strings(lib):

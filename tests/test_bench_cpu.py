@@ -74,3 +74,20 @@ def test_tensor_or_hbm_bound_by_the_ridge():
     skew[:140] = 2048 * S.K // 140
     _, _, b2k, f2k = bench.layer_algo(2048, S, skew)
     assert f2k / b2k > ridge
+
+
+def test_step_spread_quartiles():
+    """Per-step event times are summarised by their median and quartiles."""
+    d = bench.step_spread([1.0, 2.0, 3.0, 4.0, 5.0])
+    assert d["median"] == 3.0 and d["p25"] == 2.0 and d["p75"] == 4.0 and d["iqr"] == 2.0
+    assert d["min"] == 1.0 and d["max"] == 5.0 and d["n"] == 5
+    assert bench.step_spread([]) is None
+
+
+def test_default_run_times_every_graded_workload():
+    """The headline plus its legs cover T=1 (decode, 40 layers), T=512 and the
+    skewed T=2048 layer."""
+    names = {"prefill", *bench.LEGS}
+    Ts = {synth.CONFIGS[n].T for n in names}
+    assert Ts == {1, 512, 2048}
+    assert synth.CONFIGS["decode"].layers == 40 and synth.CONFIGS["skewed"].zipf_s > 0

@@ -42,7 +42,10 @@ def layer(T, shape, seed=0, zipf=0.0):
 
 
 # ---------------------------------------------------------------- dequant --
-def test_dequant_bitexact():
+def _dequant_inputs():
+    """Random words, every nibble value in every position (rows 0..1), scales
+    of both signs over five decades with general biases, and the configs'
+    scale / -8*scale pairs (rows 2..3)."""
     rng = np.random.default_rng(11)
     N, Kd = 512, 256
     q = rng.integers(0, 1 << 32, (N, Kd // 8), dtype=np.uint64).astype(np.uint32)
@@ -52,10 +55,20 @@ def test_dequant_bitexact():
     b = synth.bf16_bits(rng.uniform(-100, 100, (N, Kd // 64)))
     s[2:4] = synth.bf16_bits(rng.uniform(0.002, 0.02, (2, Kd // 64)))
     b[2:4] = synth.bf16_bits(-8 * f64(s[2:4]))
+    return q, s, b
+
+
+@pytest.mark.parametrize("routine", ["grouped_gemm", "decode"])
+def test_dequant_bitexact(routine):
+    """Both device rebuild routines (the grouped GEMMs' natural pairs and
+    the decode kernels' (i, i+4) pairs) against the oracle, bit for bit."""
+    q, s, b = _dequant_inputs()
+    N, Kd = q.shape[0], q.shape[1] * 8
     dev = torch.device("cuda")
     qd = torch.from_numpy(q.view(np.int32)).to(dev)
     out = torch.empty((N, Kd), dtype=torch.int16, device=dev)
-    m.moe_debug_dequant_w4(qd, d16(s, dev), d16(b, dev), out)
+    fn = m.moe_debug_dequant_w4 if routine == "grouped_gemm" else m.moe_debug_dequant_w4_decode
+    fn(qd, d16(s, dev), d16(b, dev), out)
     torch.cuda.synchronize()
     assert np.array_equal(h16(out), oracle.dequant(q, s, b))
 
