@@ -58,18 +58,22 @@ __device__ __forceinline__ uint32_t f2bf(float f) { return pack_bf2(f, 0.0f) & 0
 // section "Prefill: Keep Weights Packed, Keep Routing on the GPU": 64
 // weights per group share a bf16 scale and bias; w = scale*q + bias).
 //
-// affine_pair: two nibbles already placed in bits 0..3 of each 16-bit half
-// of m (every other bit zero) -> the bf16x2 pair (s*q_lo + b, s*q_hi + b),
-// each with one rounding. s2 / b2 hold the group's scale / bias in both
-// halves. Step 1: OR the exponent pattern of 128.0 -> the bf16 value 128 + q
-// (exact). Step 2: fma(., 1, -128) -> q exactly. Step 3: fma(q, s, b): exact
-// product and sum, one round-to-nearest-even to bf16. Every routine below
-// differs from the others only in which two nibbles it places in m.
+// nibble_pair_128: the low nibble of each 16-bit half of x, with the
+// exponent pattern of 128.0 set above it -> the bf16 pair (128 + q_lo,
+// 128 + q_hi), exact. One lop3: (x & 0x000F000F) | 0x43004300.
+__device__ __forceinline__ uint32_t nibble_pair_128(uint32_t x) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(0x000F000Fu), "r"(0x43004300u));
+  return d;
+}
+// affine_pair: m from nibble_pair_128 -> the bf16x2 pair (s*q_lo + b,
+// s*q_hi + b), each with one rounding. s2 / b2 hold the group's scale /
+// bias in both halves. fma(m, 1, -128) gives q exactly; fma(q, s, b) forms
+// the exact product and sum and rounds once to nearest even. The two
+// routines below differ only in which two nibbles they place.
 __device__ __forceinline__ uint32_t affine_pair(uint32_t m, uint32_t s2, uint32_t b2) {
   uint32_t q, r;
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;"
-      : "=r"(q)
-      : "r"(m | 0x43004300u), "r"(0x3F803F80u), "r"(0xC300C300u));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(q) : "r"(m), "r"(0x3F803F80u), "r"(0xC300C300u));
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(s2), "r"(b2));
   return r;
 }
@@ -81,18 +85,30 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b
                                              uint32_t out[4]) {
   const uint32_t w4 = w >> 4;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t p = __byte_perm(w, w4, 0x0400u + 0x0101u * i);
-    out[i] = affine_pair(p & 0x000F000Fu, s2, b2);
-  }
+  for (int i = 0; i < 4; ++i)
+    out[i] = affine_pair(nibble_pair_128(__byte_perm(w, w4, 0x0400u + 0x0101u * i)), s2, b2);
 }
 
 // The same word -> 4 bf16x2 words where word i holds elements i (low half)
-// and i+4 (high half): one shift and one mask place both nibbles.
+// and i+4 (high half): a shift by 4i and one lop3 place both nibbles, the
+// cheapest placement (7 integer instructions per word). Consumers see the
+// elements of each group of 8 in the order 0, 4, 1, 5, 2, 6, 3, 7.
 __device__ __forceinline__ void dequant_word_i4(uint32_t w, uint32_t s2, uint32_t b2,
                                                 uint32_t out[4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) out[i] = affine_pair((w >> (4 * i)) & 0x000F000Fu, s2, b2);
+  for (int i = 0; i < 4; ++i) out[i] = affine_pair(nibble_pair_128(w >> (4 * i)), s2, b2);
+}
+
+// Position of reduction element k in the (i, i+4)-paired order of
+// dequant_word_i4: element k of its group of 8 sits at 2*(k%4) + (k%8)/4.
+__host__ __device__ __forceinline__ int i4_pos(int k) {
+  return (k & ~7) | ((k & 3) << 1) | ((k >> 2) & 1);
+}
+// 8 bf16 in natural order (v.x = (e0,e1), ..., v.w = (e6,e7)) -> the
+// (i, i+4)-paired order ((e0,e4), (e1,e5), (e2,e6), (e3,e7)).
+__device__ __forceinline__ uint4 to_i4_order(const uint4& v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632),
+                    __byte_perm(v.y, v.w, 0x5410), __byte_perm(v.y, v.w, 0x7632));
 }
 
 __device__ __forceinline__ uint32_t dup_lo(uint32_t v) { return __byte_perm(v, 0, 0x1010); }

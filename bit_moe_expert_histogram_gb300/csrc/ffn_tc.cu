@@ -33,7 +33,13 @@
 //   warps 4..7    epilogue: tcgen05.ld of the fp32 accumulators, released as
 //                 soon as they are in registers, then SwiGLU (or plain) -> bf16
 //   warps 8..23   dequantisation of the nibble tiles into TMEM (tcgen05.st);
-//                 each thread rebuilds half of one row's 64-element slice
+//                 each thread rebuilds half of one row's 64-element slice.
+//                 Each packed word is rebuilt as the pairs (i, i+4), the
+//                 cheapest nibble placement, so along the reduction every
+//                 group of 8 elements sits in the order 0,4,1,5,2,6,3,7; the
+//                 activations are stored in the same order (gather_x_kernel
+//                 for x, the gate_up epilogue for h), which leaves each dot
+//                 product's terms unchanged
 // Rings: kNW shared-memory W stages (freed by the dequant warps once read,
 // behind a proxy fence); kNS slots of kKS reduction elements, each a
 // shared-memory B stage plus a TMEM A stage, filled under one barrier (the
@@ -92,8 +98,8 @@ __host__ __device__ constexpr int b_uempty(int q) { return 2 * kNW + 2 * kNS + k
 constexpr int kBarAccFull = 2 * kNW + 2 * kNS + 2 * kNU;
 constexpr int kBarAccEmpty = kBarAccFull + 1;
 constexpr int kNumBars = kBarAccEmpty + 1;
-constexpr int kRingOff = kNumBars * 8 + 16;  // unit queue (ints) after the barrier words
-static_assert(kRingOff + 4 * kNU <= 512, "barrier area");
+constexpr int kRingOff = kNumBars * 8 + 16;  // unit queue after the barrier words
+static_assert(kRingOff + 16 * kNU <= 512, "barrier area");
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -122,27 +128,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "memory");
 }
 
+// One unit as published in the CTA's queue: its index (-1 = no more units)
+// and its block-map entry, decoded once by the W producer so that no other
+// role waits on a global load when a unit starts.
 struct Unit {
-  int e, row0, nrows, mt;
+  int u, e, row0, nrows;
 };
-__device__ __forceinline__ Unit load_unit(const FfnArgs& a, int u) {
-  const int blk = u / a.mtiles;
-  Unit t;
-  t.mt = u - blk * a.mtiles;
-  t.e = a.block_map[3 * blk];
-  t.row0 = a.block_map[3 * blk + 1];
-  t.nrows = a.block_map[3 * blk + 2];
-  return t;
-}
 
-// Next unit from the CTA's queue (published by the W producer); -1 = no more.
-// Every lane of the calling warp waits; one arrival per warp frees the slot.
+// Next unit from the CTA's queue (4 ints per slot). Every lane of the
+// calling warp waits; one arrival per warp frees the slot.
 __device__ __forceinline__ bool next_unit(uint32_t ufull, uint32_t uempty, const volatile int* ring,
-                                          uint32_t uc, volatile int* abort, int lane, int* u) {
+                                          uint32_t uc, volatile int* abort, int lane, Unit* t) {
   const int q = uc % kNU;
   if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(ufull + 8u * q, (uc / kNU) & 1u, abort)))
     return false;
-  *u = ring[q];
+  t->u = ring[4 * q];
+  t->e = ring[4 * q + 1];
+  t->row0 = ring[4 * q + 2];
+  t->nrows = ring[4 * q + 3];
   __syncwarp();
   if (lane == 0) mbar_arrive(uempty + 8u * q);
   return true;
@@ -227,12 +230,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned v = atomicAdd(&a.ctrl->unit_next, 1u);
         const int u = (v >= (unsigned)units) ? -1
                       : ((int)v < shared_units ? routed_units + (int)v : (int)v - shared_units);
-        ring[q] = u;
+        int e = 0, row0 = 0, nrows = 0, mt = 0;
+        if (u >= 0) {
+          const int blk = u / a.mtiles;
+          mt = u - blk * a.mtiles;
+          e = a.block_map[3 * blk];
+          row0 = a.block_map[3 * blk + 1];
+          nrows = a.block_map[3 * blk + 2];
+        }
+        ring[4 * q] = u;
+        ring[4 * q + 1] = e;
+        ring[4 * q + 2] = row0;
+        ring[4 * q + 3] = nrows;
         mbar_arrive(bar(b_ufull(q)));
         if (u < 0) break;
-        const Unit t = load_unit(a, u);
-        const CUtensorMap* tw = (t.e < a.E) ? &tm_w : &tm_wsh;
-        const int wrow = (t.e < a.E ? t.e : 0) * a.rows_per_expert + t.mt * kMtRows;
+        const CUtensorMap* tw = (e < a.E) ? &tm_w : &tm_wsh;
+        const int wrow = (e < a.E ? e : 0) * a.rows_per_expert + mt * kMtRows;
+        {
+          // the unit's scales and biases (128 rows x kgroups bf16 per matrix,
+          // contiguous) into L2 ahead of the dequant warps' loads
+          const size_t ebase = e < a.E ? (size_t)e * a.rows_per_expert * a.kgroups : 0;
+          const uint16_t* sx = e < a.E ? a.s_exp : a.s_sh;
+          const uint16_t* bx = e < a.E ? a.b_exp : a.b_sh;
+          const uint32_t bytes = (uint32_t)(kTileM * a.kgroups * 2);
+#pragma unroll
+          for (int m = 0; m < kMats; ++m) {
+            const size_t off = ebase + (size_t)(m * a.half_rows + mt * kMtRows) * a.kgroups;
+            bulk_prefetch_l2(sx + off, bytes);
+            bulk_prefetch_l2(bx + off, bytes);
+          }
+        }
         for (int st = 0; st < wstages; ++st, ++it) {
           const int s = it % kNW;
           if (!mbar_wait_sleep(bar(b_wfree(s)), ((it / kNW) & 1u) ^ 1u, abort_flag)) {
@@ -265,14 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // activation rows are read again by the unit's other weight tiles
     const uint64_t bpol = policy_evict_last();
     uint32_t it = 0, uc = 0;
-    int u = -1;
+    Unit t;
     while (ok) {
-      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &t)) {
         ok = false;
         break;
       }
-      if (u < 0) break;
-      const Unit t = load_unit(a, u);
+      if (t.u < 0) break;
       // the unit's rows are consecutive rows of the plan-ordered operand:
       // boxes of 16 rows, one per lane and 64-wide atom (rows past the
       // unit's are other units' or zero past the end; their columns are
@@ -306,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 2) {
     // -------------------------------------------------------- MMA issuer --
     uint32_t it = 0, uc = 0, committed = 0;
-    int u = -1;
+    Unit t;
     // every operand address of a slot's 16 MMAs, computed once: B descriptor
     // per 16-element step (+32 B inside an atom, next atom every 4 steps)
     // and A columns (matrix m at +kKS/2), for both slots
@@ -320,16 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ak[ss][kk] = tmem + kABase + ss * kACols + kk * 8;
       }
     while (ok) {
-      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &t)) {
         ok = false;
         break;
       }
-      if (u < 0) break;
+      if (t.u < 0) break;
       if (lane == 0) {
-        const Unit t = load_unit(a, u);
         const int n_mma = max(16, (t.nrows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(kTileM, n_mma);
-        if (!mbar_wait_sleep(bar(kBarAccEmpty), (committed & 1u) ^ 1u, abort_flag)) ok = false;
+        if (!mbar_wait(bar(kBarAccEmpty), (committed & 1u) ^ 1u, abort_flag)) ok = false;
         tc_fence_after();
         for (int st = 0; st < bstages && ok; ++st, ++it) {
           const int s = it % kNS;
@@ -341,13 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t acc = st != 0 ? 1u : 0u;
           const uint32_t d1 = tmem + kTileN;
+// one accumulator's 8 MMAs, then the other's: runs of MMAs into the same
+// accumulator issue faster than alternating ones
 #define MOE_SLOT_MMAS(SS)                                                  \
   mma_bf16_ts(tmem, ak[SS][0], bdk[SS][0], idesc, acc);                    \
-  mma_bf16_ts(d1, ak[SS][0] + kKS / 2, bdk[SS][0], idesc, acc);            \
-  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk) {                \
+  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk)                  \
     mma_bf16_ts_acc(tmem, ak[SS][kk], bdk[SS][kk], idesc);                 \
-    mma_bf16_ts_acc(d1, ak[SS][kk] + kKS / 2, bdk[SS][kk], idesc);         \
-  }
+  mma_bf16_ts(d1, ak[SS][0] + kKS / 2, bdk[SS][0], idesc, acc);            \
+  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk)                  \
+    mma_bf16_ts_acc(d1, ak[SS][kk] + kKS / 2, bdk[SS][kk], idesc);
           if (s == 0) {
             MOE_SLOT_MMAS(0)
           } else {
@@ -391,14 +418,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // accumulator row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     uint32_t uc = 0, done = 0;
-    int u = -1;
+    Unit t;
     while (ok) {
-      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
+      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &t)) {
         ok = false;
         break;
       }
-      if (u < 0) break;
-      const Unit t = load_unit(a, u);
+      if (t.u < 0) break;
+      const int mt = t.u % a.mtiles;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(kBarAccFull), done & 1u, abort_flag))) {
         ok = false;
         break;
@@ -407,7 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t dbase = tmem + lane_off;
       const int nch = (t.nrows + 15) >> 4;  // >= 1
-      uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + t.mt * kMtRows + r;
+      // gate_up writes h in the (i, i+4)-paired order the down GEMM's
+      // rebuilt weights use along its reduction; down writes y_slots in
+      // natural order
+      const int ocol = GATED ? i4_pos(mt * kMtRows + r) : mt * kMtRows + r;
+      uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + ocol;
       for (int ci = 0; ci < nch; ++ci) {
         uint32_t g[16], uu[16];
         tmem_ld16(dbase + ci * 16, g);
@@ -449,27 +480,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t sw = (uint32_t)(r & 7);
     uint32_t wit = 0, ait = 0, uc = 0;
-    int u = -1;
-    while (ok) {
-      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &u)) {
-        ok = false;
-        break;
-      }
-      if (u < 0) break;
-      const Unit t = load_unit(a, u);
-      const int wr = mat * a.half_rows + t.mt * kMtRows + r;
+    // this thread's scale / bias row of a unit's matrix `mat`
+    auto group_rows = [&](const Unit& t, const uint16_t** sp, const uint16_t** bp) {
+      const int wr = mat * a.half_rows + (t.u % a.mtiles) * kMtRows + r;
       const size_t goff = (size_t)wr * a.kgroups;
-      const uint16_t* sp =
-          (t.e < a.E ? a.s_exp + (size_t)t.e * a.rows_per_expert * a.kgroups : a.s_sh) + goff;
-      const uint16_t* bp =
-          (t.e < a.E ? a.b_exp + (size_t)t.e * a.rows_per_expert * a.kgroups : a.b_sh) + goff;
-      uint2 s_next = load_groups(sp, 0, a.kgroups), b_next = load_groups(bp, 0, a.kgroups);
+      const size_t ebase = t.e < a.E ? (size_t)t.e * a.rows_per_expert * a.kgroups : 0;
+      *sp = (t.e < a.E ? a.s_exp : a.s_sh) + ebase + goff;
+      *bp = (t.e < a.E ? a.b_exp : a.b_sh) + ebase + goff;
+    };
+    Unit t;
+    if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &t)) ok = false;
+    uint2 s_next = make_uint2(0u, 0u), b_next = make_uint2(0u, 0u);
+    if (ok && t.u >= 0) {
+      const uint16_t *sp, *bp;
+      group_rows(t, &sp, &bp);
+      s_next = load_groups(sp, 0, a.kgroups);
+      b_next = load_groups(bp, 0, a.kgroups);
+    }
+    while (ok && t.u >= 0) {
+      const uint16_t *sp, *bp;
+      group_rows(t, &sp, &bp);
+      Unit nt;
+      nt.u = -1;
       for (int st = 0; st < wstages && ok; ++st, ++wit) {
         const int s = wit % kNW;
         const uint2 s_cur = s_next, b_cur = b_next;
         if (st + 1 < wstages) {
           s_next = load_groups(sp, 4 * (st + 1), a.kgroups);
           b_next = load_groups(bp, 4 * (st + 1), a.kgroups);
+        } else {
+          // last stage of the unit: take the next unit now and start the
+          // loads of its first scales, so they land while this stage runs
+          if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &nt)) {
+            ok = false;
+            break;
+          }
+          if (nt.u >= 0) {
+            const uint16_t *sp2, *bp2;
+            group_rows(nt, &sp2, &bp2);
+            s_next = load_groups(sp2, 0, a.kgroups);
+            b_next = load_groups(bp2, 0, a.kgroups);
+          }
         }
         if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(b_wfull(s)), (wit / kNW) & 1u, abort_flag))) {
           ok = false;
@@ -507,10 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t s2 = (j & 1) ? dup_hi(sv) : dup_lo(sv);
             const uint32_t b2 = (j & 1) ? dup_hi(bv) : dup_lo(bv);
             uint32_t v[16];
-            dequant_word(wv[j].x, s2, b2, &v[0]);
-            dequant_word(wv[j].y, s2, b2, &v[4]);
-            dequant_word(wv[j].z, s2, b2, &v[8]);
-            dequant_word(wv[j].w, s2, b2, &v[12]);
+            dequant_word_i4(wv[j].x, s2, b2, &v[0]);
+            dequant_word_i4(wv[j].y, s2, b2, &v[4]);
+            dequant_word_i4(wv[j].z, s2, b2, &v[8]);
+            dequant_word_i4(wv[j].w, s2, b2, &v[12]);
             tmem_st16(tmem + lane_off + kABase + as * kACols + mat * (kKS / 2) + jj * (kKA / 2) +
                           kh * 16,
                       v);
@@ -521,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar(b_sfull(as)));
         }
       }
+      t = nt;
     }
     if (!ok && lane == 0) {
       set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 5);
@@ -568,7 +620,9 @@ cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, cons
 // The grouped GEMM's activations in plan order: xs[p] = x[t(p)] for the
 // routed rows p < R (t = sorted_rows[p] / K) and x[p - R] for the shared
 // expert's rows, so a unit's rows are consecutive and load as plain TMA
-// tiles. A row index outside [0, T) is recorded and copied as zeros.
+// tiles; each group of 8 elements is stored in the (i, i+4)-paired order of
+// the rebuilt weights. A row index outside [0, T) is recorded and copied as
+// zeros.
 __global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__ x,
                                                        const int32_t* __restrict__ sorted_rows,
                                                        int K, int R, int S, int T, int hv,
@@ -579,7 +633,7 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__
     const int src = p < R ? __ldg(sorted_rows + p) / K : p - R;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (src >= 0 && src < T)
-      v = __ldg(x + (size_t)src * hv + c);
+      v = to_i4_order(__ldg(x + (size_t)src * hv + c));
     else if (c == 0)
       set_error(ctrl, MOE_ERR_BAD_INPUT, KID_FFN, p);
     xs[i] = v;
