@@ -163,6 +163,29 @@ moe_status_t map_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const 
   return MOE_OK;
 }
 
+// 3-D tensor [d2][d1][d0] of elements of `esize` bytes, dense.
+moe_status_t map_3d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base,
+                    uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2,
+                    CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) {
+    g_last_error = "cuTensorMapEncodeTiled unavailable";
+    return MOE_ERR_CUDA;
+  }
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_error = "cuTensorMapEncodeTiled (3-D) failed: " + std::to_string((int)r);
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 bool weights_ok(const moe_w4_weights_t* w) {
   return w && w->q_gate_up_dev && w->s_gate_up_dev && w->b_gate_up_dev && w->q_down_dev &&
          w->s_down_dev && w->b_down_dev && aligned16(w->q_gate_up_dev) &&
@@ -201,14 +224,14 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
 
   CUtensorMap tw, twsh, tx, th;
-  // packed weights: boxes of 128 rows x 32 words (256 reduction elements);
-  // a reduction length that is not a multiple of 256 reads zero-filled
-  // columns past the row end in its last box
+  // packed gate_up weights as (word, row of the half, 2*expert + half):
+  // boxes of 32 words (256 reduction elements) x 16 rows x both halves, so
+  // one box brings 16 gate rows and the matching 16 up rows
   const uint32_t wbox = (uint32_t)ffn_stage_k() / 8;
-  MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_gate_up_dev, H / 8,
-                 (uint64_t)E * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-  MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_gate_up_dev, H / 8,
-                 (uint64_t)(s->n_shared ? 1 : E) * 2 * I, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
+  MOE_TRY(map_3d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_gate_up_dev, H / 8, I,
+                 (uint64_t)E * 2, wbox, 16, 2, CU_TENSOR_MAP_SWIZZLE_128B));
+  MOE_TRY(map_3d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_gate_up_dev, H / 8, I,
+                 (uint64_t)(s->n_shared ? 1 : E) * 2, wbox, 16, 2, CU_TENSOR_MAP_SWIZZLE_128B));
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + L.xs);
   cudaError_t ge = launch_gather_x(static_cast<const uint16_t*>(x), plan->sorted_rows_dev, K, R, S,
                                    T, H, xs, ctrl, nsm, stream);
@@ -225,7 +248,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   a.E = E;
   a.rows_per_expert = 2 * I;
   a.half_rows = I;
-  a.mtiles = I / ffn_tile_m();
+  a.mtiles = I / (ffn_tile_m() / 2);  // 64 gate + 64 up rows per unit
   a.kdim = H;
   a.kgroups = H / 64;
   a.s_exp = ex->s_gate_up_dev;
@@ -240,6 +263,9 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   cudaError_t e = launch_ffn_gate_up(tw, twsh, tx, a, a.max_units < nsm ? a.max_units : nsm, stream);
   if (e != cudaSuccess) return cuda_fail(e, "ffn gate_up launch");
 
+  // packed down weights: boxes of 128 rows x 32 words; a reduction length
+  // that is not a multiple of 256 reads zero-filled words past the row end
+  // in its last box
   MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ex->q_down_dev, I / 8, (uint64_t)E * H,
                  wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_down_dev, I / 8,
@@ -248,8 +274,8 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
                  CU_TENSOR_MAP_SWIZZLE_128B));
   a.sorted_rows = nullptr;
   a.rows_per_expert = H;
-  a.half_rows = ffn_tile_m();            // two consecutive 128-row tiles per unit
-  a.mtiles = H / (2 * ffn_tile_m());
+  a.half_rows = 0;
+  a.mtiles = H / ffn_tile_m();            // 128 consecutive rows per unit
   a.kdim = I;
   a.kgroups = I / 64;
   a.s_exp = ex->s_down_dev;

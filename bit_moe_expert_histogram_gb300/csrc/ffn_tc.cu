@@ -14,43 +14,49 @@
 // multiple of 16) over the tokens of one block-map entry, so an expert with
 // 5 rows pads to 16, not to 128.
 //
-// A unit is (block-map entry, 256 weight rows) = two 128-row matrices with
-// one accumulator each: for gate_up the matching gate and up rows (the
-// epilogue applies SwiGLU to the pair), for down two consecutive 128-row
-// tiles of the down matrix. One persistent CTA per SM takes units from a
-// device-wide counter, the shared expert's (widest) units first; the last
-// CTA to finish resets the counter for the next launch.
+// A unit is (block-map entry, 128 weight rows) with one accumulator. For
+// down these are 128 consecutive rows of the down matrix. For gate_up they
+// are 64 gate rows j0..j0+63 and the 64 matching up rows, laid out so that
+// each 32-row TMEM lane quarter q holds gate rows j0+16q..j0+16q+15 in its
+// lanes 0..15 and the same up rows in lanes 16..31: the SwiGLU epilogue
+// pairs lane l with lane l+16 by one warp shuffle. One persistent CTA per SM
+// takes units from a device-wide counter, the shared expert's (widest) units
+// first; the last CTA to finish resets the counter for the next launch.
 // Warp roles (24 warps):
-//   warp 0        unit queue and W producer: takes units, publishes them to
-//                 the CTA through a small shared-memory queue, and loads the
-//                 packed nibble tiles by TMA, 128 rows x 128 B (256 reduction
-//                 elements) per matrix, 128-byte swizzle
+//   warp 0        unit queue and W producer: takes units, decodes their
+//                 block-map entry once and publishes it to the CTA through
+//                 a small shared-memory queue, prefetches the unit's scales
+//                 into L2, and loads the packed nibble tiles by TMA, 128
+//                 rows x 128 B (256 reduction elements), 128-byte swizzle
+//                 (gate_up: four boxes of 16 gate + 16 up rows)
 //   warp 1        B producer: the entry's activation rows, consecutive in
 //                 the plan-ordered operand (x gathered by gather_x_kernel,
 //                 or h), loaded as TMA tiles of 16 rows x 64 elements
 //                 (128-byte swizzle)
 //   warp 2        TMEM allocator and MMA issuer (one thread)
-//   warps 4..7    epilogue: tcgen05.ld of the fp32 accumulators, released as
-//                 soon as they are in registers, then SwiGLU (or plain) -> bf16
-//   warps 8..23   dequantisation of the nibble tiles into TMEM (tcgen05.st);
-//                 each thread rebuilds half of one row's 64-element slice.
-//                 Each packed word is rebuilt as the pairs (i, i+4), the
-//                 cheapest nibble placement, so along the reduction every
-//                 group of 8 elements sits in the order 0,4,1,5,2,6,3,7; the
+//   warps 4..7    epilogue: tcgen05.ld of the fp32 accumulator, then SwiGLU
+//                 (or plain) -> bf16 stores
+//   warps 8..23   dequantisation of the nibble tiles into TMEM (tcgen05.st):
+//                 warp 8 + 4g + q rebuilds 64 reduction elements (group g of
+//                 every slot) of the 32 rows in lane quarter q. Each
+//                 packed word is rebuilt as the pairs (i, i+4), the cheapest
+//                 nibble placement, so along the reduction every group of 8
+//                 elements sits in the order 0,4,1,5,2,6,3,7; the
 //                 activations are stored in the same order (gather_x_kernel
 //                 for x, the gate_up epilogue for h), which leaves each dot
 //                 product's terms unchanged
 // Rings: kNW shared-memory W stages (freed by the dequant warps once read,
 // behind a proxy fence); kNS slots of kKS reduction elements, each a
 // shared-memory B stage plus a TMEM A stage, filled under one barrier (the
-// dequant warps' arrivals and the B tiles' bytes) and freed together by
-// one MMA commit, so the MMA thread synchronises once per 16 MMAs; one
-// accumulator pair (freed by the epilogue). Roles that mostly wait sleep in their barrier waits. Every
-// wait is bounded; on a timeout the CTA records MOE_ERR_TIMEOUT, drains what
-// it started, frees TMEM and returns. Before exit the MMA thread waits for
-// the arrival of every commit it issued; if that wait itself runs out, the
-// tensor pipe has stopped, and the CTA records MOE_ERR_TIMEOUT and leaves
-// its TMEM columns allocated rather than free columns MMAs may still write.
+// dequant warps' arrivals and the B tiles' bytes) and freed together by one
+// MMA commit, 16 MMAs per handshake (runs of 16 fresh A tiles keep the
+// tensor pipe busier than runs of 8); two accumulators, so the MMA moves on to the next unit while
+// the epilogue drains the last one. Every wait is bounded; on a timeout the
+// CTA records MOE_ERR_TIMEOUT, drains what it started, frees TMEM and
+// returns. Before exit the MMA thread waits for the arrival of every commit
+// it issued; if that wait itself runs out, the tensor pipe has stopped, and
+// the CTA records MOE_ERR_TIMEOUT and leaves its TMEM columns allocated
+// rather than free columns MMAs may still write.
 #include <atomic>
 
 #include "common.cuh"
@@ -59,27 +65,27 @@
 namespace moe {
 
 namespace {
-constexpr int kTileM = 128;                // weight rows per matrix (MMA M)
+constexpr int kTileM = 128;                // weight rows per unit (MMA M)
 constexpr int kTileN = 128;                // most tokens per tile (MMA N)
-constexpr int kMats = 2;                   // matrices (accumulators) per unit
 constexpr int kKW = 256;                   // reduction elements per W stage
 constexpr int kKA = 64;                    // reduction elements per 128-byte swizzle atom
-constexpr int kKS = 128;                   // reduction elements per slot (MMA handshake)
+constexpr int kKS = 256;                   // reduction elements per slot (16 MMAs per handshake)
 constexpr int kSlotsPerW = kKW / kKS;      // slots per W stage
 constexpr int kNW = 4;                     // W stages (shared memory)
 constexpr int kNS = 2;                     // slots: B (shared memory) + A (TMEM)
 constexpr int kNU = 4;                     // unit queue slots
+constexpr int kNAcc = 2;                   // accumulators (TMEM)
+constexpr int kGateRows = 16;              // gate (and up) rows per lane quarter, gate_up
 constexpr int kDequantWarps = 16;
 constexpr int kEpiWarps = 4;
 constexpr int kUnitReaders = 2 + kEpiWarps + kDequantWarps;  // B producer, MMA, epilogue, dequant
 constexpr int kThreads = (8 + kDequantWarps) * 32;
 constexpr int kBAtom = kTileN * 128;       // 128 rows x 64 bf16
-constexpr int kBStage = (kKS / kKA) * kBAtom;  // one slot of B: two atoms
-constexpr int kWMat = kTileM * (kKW / 2);  // 128 rows x 128 B of nibbles
-constexpr int kWStage = kMats * kWMat;
-constexpr int kAccCols = kMats * kTileN;   // accumulator pair
-constexpr int kACols = kMats * (kKS / 2);  // A columns per slot (2 bf16 per column)
-constexpr int kABase = kAccCols;
+constexpr int kBStage = (kKS / kKA) * kBAtom;  // one slot of B: four atoms
+constexpr int kWStage = kTileM * (kKW / 2);    // 128 rows x 128 B of nibbles
+constexpr int kWBoxGate = 2 * kGateRows * (kKW / 2);  // one gate_up box: 16 gate + 16 up rows
+constexpr int kACols = kKS / 2;            // A columns per slot (2 bf16 per column)
+constexpr int kABase = kNAcc * kTileN;
 constexpr int kTmemCols = 512;
 constexpr int kSmemW = 0;
 constexpr int kSmemB = kNW * kWStage;
@@ -87,6 +93,8 @@ constexpr int kSmemBar = kSmemB + kNS * kBStage;
 constexpr int kSmemBytes = kSmemBar + 512 + 1024;
 static_assert(kABase + kNS * kACols <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(4 * kWBoxGate == kWStage, "gate_up boxes fill a W stage");
+static_assert(kSlotsPerW == 1, "one slot per W stage");
 
 // barrier slots
 __host__ __device__ constexpr int b_wfull(int s) { return s; }
@@ -95,9 +103,9 @@ __host__ __device__ constexpr int b_sfull(int s) { return 2 * kNW + s; }
 __host__ __device__ constexpr int b_sfree(int s) { return 2 * kNW + kNS + s; }
 __host__ __device__ constexpr int b_ufull(int q) { return 2 * kNW + 2 * kNS + q; }
 __host__ __device__ constexpr int b_uempty(int q) { return 2 * kNW + 2 * kNS + kNU + q; }
-constexpr int kBarAccFull = 2 * kNW + 2 * kNS + 2 * kNU;
-constexpr int kBarAccEmpty = kBarAccFull + 1;
-constexpr int kNumBars = kBarAccEmpty + 1;
+__host__ __device__ constexpr int b_accfull(int b) { return 2 * kNW + 2 * kNS + 2 * kNU + b; }
+__host__ __device__ constexpr int b_accempty(int b) { return 2 * kNW + 2 * kNS + 2 * kNU + kNAcc + b; }
+constexpr int kNumBars = 2 * kNW + 2 * kNS + 2 * kNU + 2 * kNAcc;
 constexpr int kRingOff = kNumBars * 8 + 16;  // unit queue after the barrier words
 static_assert(kRingOff + 16 * kNU <= 512, "barrier area");
 
@@ -127,6 +135,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "r"(taddr)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tm), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+      : "memory");
+}
+// silu(g) * u in fp32 (the result is rounded to bf16 by the caller)
+__device__ __forceinline__ float swiglu(float g, float u) {
+  return g * u * __frcp_rn(1.0f + __expf(-g));
+}
 
 // One unit as published in the CTA's queue: its index (-1 = no more units)
 // and its block-map entry, decoded once by the W producer so that no other
@@ -140,7 +160,7 @@ struct Unit {
 __device__ __forceinline__ bool next_unit(uint32_t ufull, uint32_t uempty, const volatile int* ring,
                                           uint32_t uc, volatile int* abort, int lane, Unit* t) {
   const int q = uc % kNU;
-  if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(ufull + 8u * q, (uc / kNU) & 1u, abort)))
+  if (!__all_sync(0xFFFFFFFFu, mbar_wait(ufull + 8u * q, (uc / kNU) & 1u, abort)))
     return false;
   t->u = ring[4 * q];
   t->e = ring[4 * q + 1];
@@ -150,17 +170,43 @@ __device__ __forceinline__ bool next_unit(uint32_t ufull, uint32_t uempty, const
   if (lane == 0) mbar_arrive(uempty + 8u * q);
   return true;
 }
+
+// The same for a single thread (the MMA issuer), which spins: its waits are
+// short and on the critical path.
+__device__ __forceinline__ bool next_unit_1(uint32_t ufull, uint32_t uempty,
+                                            const volatile int* ring, uint32_t uc,
+                                            volatile int* abort, Unit* t) {
+  const int q = uc % kNU;
+  if (!mbar_wait(ufull + 8u * q, (uc / kNU) & 1u, abort)) return false;
+  t->u = ring[4 * q];
+  t->e = ring[4 * q + 1];
+  t->row0 = ring[4 * q + 2];
+  t->nrows = ring[4 * q + 3];
+  mbar_arrive(uempty + 8u * q);
+  return true;
+}
+
+// Weight row (within its expert) of A-tile row r of unit tile mt.
+template <bool GATED>
+__device__ __forceinline__ int weight_row(const FfnArgs& a, int mt, int r) {
+  if (GATED) {
+    const int l = r & 31;
+    return (l < kGateRows ? 0 : a.half_rows) + mt * (kTileM / 2) + kGateRows * (r >> 5) +
+           (l & (kGateRows - 1));
+  }
+  return mt * kTileM + r;
+}
 }  // namespace
 
-// GATED (gate_up): matrix 0 = gate rows mt*128.., matrix 1 = up rows
-// I + mt*128.. (a.half_rows = I); the epilogue writes bf16(silu(g) * u) to
-// column mt*128 + r. Otherwise (down): matrices are rows mt*256.. and
-// mt*256 + 128.. (a.half_rows = 128), written to columns mt*256 + 128*m + r.
+// GATED (gate_up): unit tile mt covers h columns mt*64 .. mt*64+63 (gate
+// rows and up rows I + ..., a.half_rows = I, a 3-D tensor map over
+// (word, row of the half, 2*expert + half)); the epilogue writes
+// bf16(silu(g) * u). Otherwise (down): rows mt*128 .., written to columns
+// mt*128 + r.
 template <bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_w4_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_wsh,
                   const __grid_constant__ CUtensorMap tm_b, const FfnArgs a) {
-  constexpr int kMtRows = GATED ? kTileM : 2 * kTileM;  // weight rows advanced per M tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -187,8 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(b_ufull(q)), 1);
       mbar_init(bar(b_uempty(q)), kUnitReaders);
     }
-    mbar_init(bar(kBarAccFull), 1);
-    mbar_init(bar(kBarAccEmpty), kEpiWarps);
+    for (int b = 0; b < kNAcc; ++b) {
+      mbar_init(bar(b_accfull(b)), 1);
+      mbar_init(bar(b_accempty(b)), kEpiWarps);
+    }
     *abort_flag = 0;
     *tmem_keep = 0;
     fence_mbar_init();
@@ -209,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int units = min(*a.num_blocks * a.mtiles, a.max_units);
   const int wstages = (a.kdim + kKW - 1) / kKW;  // W stages per unit (the last may be half)
-  const int bstages = a.kdim / kKS;              // slots per unit
+  const int bstages = wstages;                   // slots per unit (one per W stage)
+  const int ksteps_last = ((a.kdim - (bstages - 1) * kKS) / 16);  // MMAs of the last slot
   const uint32_t ufull0 = bar(b_ufull(0)), uempty0 = bar(b_uempty(0));
   bool ok = true;
 
@@ -223,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, uc = 0;
       for (;; ++uc) {
         const int q = uc % kNU;
-        if (!mbar_wait_sleep(bar(b_uempty(q)), ((uc / kNU) & 1u) ^ 1u, abort_flag)) {
+        if (!mbar_wait(bar(b_uempty(q)), ((uc / kNU) & 1u) ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -244,32 +293,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring[4 * q + 3] = nrows;
         mbar_arrive(bar(b_ufull(q)));
         if (u < 0) break;
-        const CUtensorMap* tw = (e < a.E) ? &tm_w : &tm_wsh;
-        const int wrow = (e < a.E ? e : 0) * a.rows_per_expert + mt * kMtRows;
+        const bool routed = e < a.E;
+        const CUtensorMap* tw = routed ? &tm_w : &tm_wsh;
+        const int ew = routed ? e : 0;
         {
-          // the unit's scales and biases (128 rows x kgroups bf16 per matrix,
-          // contiguous) into L2 ahead of the dequant warps' loads
-          const size_t ebase = e < a.E ? (size_t)e * a.rows_per_expert * a.kgroups : 0;
-          const uint16_t* sx = e < a.E ? a.s_exp : a.s_sh;
-          const uint16_t* bx = e < a.E ? a.b_exp : a.b_sh;
-          const uint32_t bytes = (uint32_t)(kTileM * a.kgroups * 2);
-#pragma unroll
-          for (int m = 0; m < kMats; ++m) {
-            const size_t off = ebase + (size_t)(m * a.half_rows + mt * kMtRows) * a.kgroups;
+          // the unit's scales and biases into L2 ahead of the dequant
+          // warps' loads: gate_up 64 gate + 64 up rows, down 128 rows
+          const size_t ebase = (size_t)ew * a.rows_per_expert * a.kgroups;
+          const uint16_t* sx = routed ? a.s_exp : a.s_sh;
+          const uint16_t* bx = routed ? a.b_exp : a.b_sh;
+          const int runs = GATED ? 2 : 1;
+          const int run_rows = kTileM / runs;
+          const uint32_t bytes = (uint32_t)(run_rows * a.kgroups * 2);
+          for (int h = 0; h < runs; ++h) {
+            const size_t off = ebase + (size_t)(h * a.half_rows + mt * run_rows) * a.kgroups;
             bulk_prefetch_l2(sx + off, bytes);
             bulk_prefetch_l2(bx + off, bytes);
           }
         }
         for (int st = 0; st < wstages; ++st, ++it) {
           const int s = it % kNW;
-          if (!mbar_wait_sleep(bar(b_wfree(s)), ((it / kNW) & 1u) ^ 1u, abort_flag)) {
+          if (!mbar_wait(bar(b_wfree(s)), ((it / kNW) & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bar(b_wfull(s)), (uint32_t)kWStage);
-          tma_load_2d(sW + s * kWStage, tw, st * (kKW / 8), wrow, bar(b_wfull(s)), pol);
-          tma_load_2d(sW + s * kWStage + kWMat, tw, st * (kKW / 8), wrow + a.half_rows,
-                      bar(b_wfull(s)), pol);
+          if (GATED) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              tma_load_3d(sW + s * kWStage + qq * kWBoxGate, tw, st * (kKW / 8),
+                          mt * (kTileM / 2) + kGateRows * qq, 2 * ew, bar(b_wfull(s)), pol);
+          } else {
+            tma_load_2d(sW + s * kWStage, tw, st * (kKW / 8), ew * a.rows_per_expert + mt * kTileM,
+                        bar(b_wfull(s)), pol);
+          }
         }
         if (!ok) break;
       }
@@ -289,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- B producer --
-    // activation rows are read again by the unit's other weight tiles
+    // activation rows are read again by the entry's other weight tiles
     const uint64_t bpol = policy_evict_last();
     uint32_t it = 0, uc = 0;
     Unit t;
@@ -304,19 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unit's are other units' or zero past the end; their columns are
       // never read back)
       const int nbox = (t.nrows + 15) >> 4;
-      const uint32_t bytes = (uint32_t)nbox * 16 * 128 * (kKS / kKA);
       for (int st = 0; st < bstages; ++st, ++it) {
         const int s = it % kNS;
+        const int natoms = min(kKS / kKA, (a.kdim - st * kKS) / kKA);  // 64-wide atoms in this slot
+        const uint32_t bytes = (uint32_t)nbox * 16 * 128 * natoms;
         bool good = true;
-        if (lane == 0) good = mbar_wait_sleep(bar(b_sfree(s)), ((it / kNS) & 1u) ^ 1u, abort_flag);
+        if (lane == 0) good = mbar_wait(bar(b_sfree(s)), ((it / kNS) & 1u) ^ 1u, abort_flag);
         if (!__shfl_sync(0xFFFFFFFFu, good ? 1 : 0, 0)) {
           ok = false;
           break;
         }
         if (lane == 0) mbar_arrive_expect_tx(bar(b_sfull(s)), bytes);
         __syncwarp();
-        if (lane < nbox * (kKS / kKA)) {
-          const int bx = lane / (kKS / kKA), at = lane % (kKS / kKA);
+        if (lane < nbox * natoms) {
+          const int bx = lane / natoms, at = lane % natoms;
           tma_load_2d(sB + s * kBStage + at * kBAtom + bx * 16 * 128, &tm_b, st * kKS + at * kKA,
                       t.row0 + 16 * bx, bar(b_sfull(s)), bpol);
         }
@@ -331,30 +389,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // -------------------------------------------------------- MMA issuer --
-    uint32_t it = 0, uc = 0, committed = 0;
+    uint32_t it = 0, uc = 0, done_units = 0;
     Unit t;
-    // every operand address of a slot's 16 MMAs, computed once: B descriptor
-    // per 16-element step (+32 B inside an atom, next atom every 4 steps)
-    // and A columns (matrix m at +kKS/2), for both slots
-    uint64_t bdk[kNS][kKS / 16];
-    uint32_t ak[kNS][kKS / 16];
-#pragma unroll
-    for (int ss = 0; ss < kNS; ++ss)
-#pragma unroll
-      for (int kk = 0; kk < kKS / 16; ++kk) {
-        bdk[ss][kk] = smem_desc_sw128(sB + ss * kBStage + (kk >> 2) * kBAtom + (kk & 3) * 32);
-        ak[ss][kk] = tmem + kABase + ss * kACols + kk * 8;
-      }
-    while (ok) {
-      if (!next_unit(ufull0, uempty0, ring, uc++, abort_flag, lane, &t)) {
+    // B descriptors: slot s, step kk at +32 B inside an atom, next atom
+    // every 4 steps; the descriptor's address field is addr >> 4, so an
+    // offset adds (offset >> 4) without carrying out of the field
+    const uint64_t bdesc0 = smem_desc_sw128(sB);
+    // lane 0 alone runs the loop (the other lanes go straight to the end)
+    while (ok && lane == 0) {
+      if (!next_unit_1(ufull0, uempty0, ring, uc++, abort_flag, &t)) {
         ok = false;
         break;
       }
       if (t.u < 0) break;
-      if (lane == 0) {
+      {
         const int n_mma = max(16, (t.nrows + 15) & ~15);
         const uint32_t idesc = idesc_bf16(kTileM, n_mma);
-        if (!mbar_wait(bar(kBarAccEmpty), (committed & 1u) ^ 1u, abort_flag)) ok = false;
+        const uint32_t ab = done_units % kNAcc;
+        const uint32_t dacc = tmem + ab * kTileN;
+        if (!mbar_wait(bar(b_accempty(ab)), ((done_units / kNAcc) & 1u) ^ 1u, abort_flag)) ok = false;
         tc_fence_after();
         for (int st = 0; st < bstages && ok; ++st, ++it) {
           const int s = it % kNS;
@@ -364,31 +417,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t acc = st != 0 ? 1u : 0u;
-          const uint32_t d1 = tmem + kTileN;
-// one accumulator's 8 MMAs, then the other's: runs of MMAs into the same
-// accumulator issue faster than alternating ones
-#define MOE_SLOT_MMAS(SS)                                                  \
-  mma_bf16_ts(tmem, ak[SS][0], bdk[SS][0], idesc, acc);                    \
-  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk)                  \
-    mma_bf16_ts_acc(tmem, ak[SS][kk], bdk[SS][kk], idesc);                 \
-  mma_bf16_ts(d1, ak[SS][0] + kKS / 2, bdk[SS][0], idesc, acc);            \
-  _Pragma("unroll") for (int kk = 1; kk < kKS / 16; ++kk)                  \
-    mma_bf16_ts_acc(d1, ak[SS][kk] + kKS / 2, bdk[SS][kk], idesc);
-          if (s == 0) {
-            MOE_SLOT_MMAS(0)
+          const uint32_t acol = tmem + kABase + s * kACols;
+          const uint64_t bd = bdesc0 + (uint64_t)((s * kBStage) >> 4);
+          mma_bf16_ts(dacc, acol, bd, idesc, st != 0 ? 1u : 0u);
+          if (st + 1 < bstages || ksteps_last == kKS / 16) {
+#pragma unroll
+            for (int kk = 1; kk < kKS / 16; ++kk)
+              mma_bf16_ts_acc(dacc, acol + kk * 8,
+                              bd + (uint64_t)((((kk >> 2) * kBAtom) + (kk & 3) * 32) >> 4), idesc);
           } else {
-            MOE_SLOT_MMAS(1)
+            for (int kk = 1; kk < ksteps_last; ++kk)
+              mma_bf16_ts_acc(dacc, acol + kk * 8,
+                              bd + (uint64_t)((((kk >> 2) * kBAtom) + (kk & 3) * 32) >> 4), idesc);
           }
-#undef MOE_SLOT_MMAS
           mma_commit(bar(b_sfree(s)));  // frees this slot's B stage and A stage
         }
         if (ok) {
-          mma_commit(bar(kBarAccFull));
-          ++committed;
+          mma_commit(bar(b_accfull(ab)));
+          ++done_units;
         }
       }
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     }
     if (lane == 0) {
       if (!ok) {
@@ -403,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool drained = true;
       for (uint32_t i = it > (uint32_t)kNS ? it - kNS : 0u; i < it; ++i)
         drained &= mbar_wait(bar(b_sfree(i % kNS)), (i / kNS) & 1u, &never);
-      if (committed > 0) drained &= mbar_wait(bar(kBarAccFull), (committed - 1) & 1u, &never);
+      for (uint32_t i = done_units > (uint32_t)kNAcc ? done_units - kNAcc : 0u; i < done_units; ++i)
+        drained &= mbar_wait(bar(b_accfull(i % kNAcc)), (i / kNAcc) & 1u, &never);
       if (!drained) {
         // an MMA commit is still pending after the wait limit: the tensor
         // pipe has stopped. Its MMAs may still write TMEM, so the columns
@@ -426,44 +475,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (t.u < 0) break;
       const int mt = t.u % a.mtiles;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(kBarAccFull), done & 1u, abort_flag))) {
+      const uint32_t ab = done % kNAcc;
+      if (!__all_sync(0xFFFFFFFFu,
+                      mbar_wait(bar(b_accfull(ab)), (done / kNAcc) & 1u, abort_flag))) {
         ok = false;
         break;
       }
       ++done;
       tc_fence_after();
-      const uint32_t dbase = tmem + lane_off;
+      const uint32_t dbase = tmem + lane_off + ab * kTileN;
       const int nch = (t.nrows + 15) >> 4;  // >= 1
-      // gate_up writes h in the (i, i+4)-paired order the down GEMM's
-      // rebuilt weights use along its reduction; down writes y_slots in
-      // natural order
-      const int ocol = GATED ? i4_pos(mt * kMtRows + r) : mt * kMtRows + r;
-      uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + ocol;
-      for (int ci = 0; ci < nch; ++ci) {
-        uint32_t g[16], uu[16];
-        tmem_ld16(dbase + ci * 16, g);
-        tmem_ld16(dbase + kTileN + ci * 16, uu);
-        tmem_wait_ld();
-        if (ci == nch - 1) {  // accumulators fully read: hand them back to the MMA
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarAccEmpty));
-        }
-        const int nlim = min(16, t.nrows - ci * 16);
+      if (GATED) {
+        // lane l < 16 holds gate row j, lane l + 16 up row j, j = j0 +
+        // 16*quarter + l: the pair exchanges halves of each 16-token chunk
+        // and lane l writes tokens 0..7, lane l + 16 tokens 8..15
+        const int j = mt * (kTileM / 2) + kGateRows * quarter + (lane & (kGateRows - 1));
+        const bool lo = lane < kGateRows;
+        uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + i4_pos(j);
+        for (int ci = 0; ci < nch; ++ci) {
+          uint32_t v[16];
+          tmem_ld16(dbase + ci * 16, v);
+          tmem_wait_ld();
+          const int tok0 = ci * 16 + (lo ? 0 : 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (i < nlim) {
-            uint16_t* o = out + (size_t)(ci * 16 + i) * a.out_ld;
-            const float gv = __uint_as_float(g[i]), uv = __uint_as_float(uu[i]);
-            if (GATED) {
-              o[0] = (uint16_t)f2bf(gv / (1.0f + expf(-gv)) * uv);
-            } else {
-              o[0] = (uint16_t)f2bf(gv);
-              o[kTileM] = (uint16_t)f2bf(uv);
-            }
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t send = lo ? v[8 + k] : v[k];
+            const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, send, kGateRows);
+            const float g = __uint_as_float(lo ? v[k] : got);
+            const float u = __uint_as_float(lo ? got : v[8 + k]);
+            if (tok0 + k < t.nrows)
+              out[(size_t)(tok0 + k) * a.out_ld] = (uint16_t)f2bf(swiglu(g, u));
           }
         }
+      } else {
+        uint16_t* out = a.out + (size_t)t.row0 * a.out_ld + mt * kTileM + r;
+        for (int ci = 0; ci < nch; ++ci) {
+          uint32_t v[16];
+          tmem_ld16(dbase + ci * 16, v);
+          tmem_wait_ld();
+          const int nlim = min(16, t.nrows - ci * 16);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < nlim) out[(size_t)(ci * 16 + i) * a.out_ld] = (uint16_t)f2bf(__uint_as_float(v[i]));
+        }
       }
+      // accumulator fully read: hand it back to the MMA
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(b_accempty(ab)));
     }
     if (!ok && lane == 0) {
       set_error(a.ctrl, MOE_ERR_TIMEOUT, KID_FFN, 4);
@@ -473,16 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ dequant into TMEM --
     const int d = warp - 8;              // 0..15
     const int quarter = warp & 3;        // TMEM lanes this warp may touch
-    const int grp = d >> 2;              // 0..3
-    const int mat = grp >> 1;            // matrix 0 / 1
-    const int kh = grp & 1;              // half of each 64-element slice
+    const int g4 = d >> 2;               // which 32 elements of every slot
     const int r = quarter * 32 + lane;   // tile row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t sw = (uint32_t)(r & 7);
     uint32_t wit = 0, ait = 0, uc = 0;
-    // this thread's scale / bias row of a unit's matrix `mat`
+    // this thread's scale / bias row of a unit
     auto group_rows = [&](const Unit& t, const uint16_t** sp, const uint16_t** bp) {
-      const int wr = mat * a.half_rows + (t.u % a.mtiles) * kMtRows + r;
+      const int wr = weight_row<GATED>(a, t.u % a.mtiles, r);
       const size_t goff = (size_t)wr * a.kgroups;
       const size_t ebase = t.e < a.E ? (size_t)t.e * a.rows_per_expert * a.kgroups : 0;
       *sp = (t.e < a.E ? a.s_exp : a.s_sh) + ebase + goff;
@@ -522,55 +579,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             b_next = load_groups(bp2, 0, a.kgroups);
           }
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(b_wfull(s)), (wit / kNW) & 1u, abort_flag))) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(b_wfull(s)), (wit / kNW) & 1u, abort_flag))) {
           ok = false;
           break;
         }
-        // chunk 2j + kh of the row holds this thread's 32 elements of
-        // sub-stage j; chunk c of row r sits at chunk c ^ (r % 8) (128-byte swizzle)
-        uint4 wv[kKW / kKA];
-        const uint32_t rowaddr = sW + s * kWStage + mat * kWMat + r * 128;
-#pragma unroll
-        for (int j = 0; j < kKW / kKA; ++j)
-          wv[j] = lds128(rowaddr + 16u * ((uint32_t)(2 * j + kh) ^ sw));
+        // this thread's 8 words are 16-byte chunks 2*g4 and 2*g4 + 1 of its
+        // row (64-element group 4*st + g4); chunk c of row r sits at chunk
+        // c ^ (r % 8) (128-byte swizzle). In a half last stage only groups
+        // 0 and 1 exist: the other warps rebuild the zero-filled words, whose
+        // columns the MMA never reads.
+        const uint32_t rowaddr = sW + s * kWStage + r * 128;
+        const uint4 w0 = lds128(rowaddr + 16u * ((uint32_t)(2 * g4) ^ sw));
+        const uint4 w1 = lds128(rowaddr + 16u * ((uint32_t)(2 * g4 + 1) ^ sw));
         // the stage goes back to the TMA producer: order these generic-proxy
         // reads before its async-proxy refill (write-after-read across proxies)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(b_wfree(s)));
-        const int nslot = min(kSlotsPerW, bstages - st * kSlotsPerW);
-#pragma unroll
-        for (int js = 0; js < kSlotsPerW; ++js) {
-          if (js >= nslot) break;
-          const int as = ait % kNS;
-          if (!__all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u,
-                                                       abort_flag))) {
-            ok = false;
-            break;
-          }
-          ++ait;
-          tc_fence_after();
-#pragma unroll
-          for (int jj = 0; jj < kKS / kKA; ++jj) {
-            const int j = js * (kKS / kKA) + jj;  // 64-element group 4*st + j of this row
-            const uint32_t sv = (j & 2) ? s_cur.y : s_cur.x;
-            const uint32_t bv = (j & 2) ? b_cur.y : b_cur.x;
-            const uint32_t s2 = (j & 1) ? dup_hi(sv) : dup_lo(sv);
-            const uint32_t b2 = (j & 1) ? dup_hi(bv) : dup_lo(bv);
-            uint32_t v[16];
-            dequant_word_i4(wv[j].x, s2, b2, &v[0]);
-            dequant_word_i4(wv[j].y, s2, b2, &v[4]);
-            dequant_word_i4(wv[j].z, s2, b2, &v[8]);
-            dequant_word_i4(wv[j].w, s2, b2, &v[12]);
-            tmem_st16(tmem + lane_off + kABase + as * kACols + mat * (kKS / 2) + jj * (kKA / 2) +
-                          kh * 16,
-                      v);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(b_sfull(as)));
+        const int as = ait % kNS;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u,
+                                               abort_flag))) {
+          ok = false;
+          break;
         }
+        ++ait;
+        tc_fence_after();
+        const uint32_t sv = (g4 & 2) ? s_cur.y : s_cur.x;
+        const uint32_t bv = (g4 & 2) ? b_cur.y : b_cur.x;
+        const uint32_t s2 = (g4 & 1) ? dup_hi(sv) : dup_lo(sv);
+        const uint32_t b2 = (g4 & 1) ? dup_hi(bv) : dup_lo(bv);
+        uint32_t v[16];
+        const uint32_t tcol = tmem + lane_off + kABase + as * kACols + g4 * 32;
+        dequant_word_i4(w0.x, s2, b2, &v[0]);
+        dequant_word_i4(w0.y, s2, b2, &v[4]);
+        dequant_word_i4(w0.z, s2, b2, &v[8]);
+        dequant_word_i4(w0.w, s2, b2, &v[12]);
+        tmem_st16(tcol, v);
+        dequant_word_i4(w1.x, s2, b2, &v[0]);
+        dequant_word_i4(w1.y, s2, b2, &v[4]);
+        dequant_word_i4(w1.z, s2, b2, &v[8]);
+        dequant_word_i4(w1.w, s2, b2, &v[12]);
+        tmem_st16(tcol + 16, v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(b_sfull(as)));
       }
       t = nt;
     }

@@ -23,7 +23,7 @@ struct FfnArgs {
   int E;                       // routed experts; entry expert E = shared
   int rows_per_expert;         // weight rows per expert (2I or H)
   int half_rows;               // gate_up: I (first up row); down: 0
-  int mtiles;                  // 128-row weight tiles per entry
+  int mtiles;                  // unit tiles per entry (gate_up: 64 gate + 64 up rows; down: 128 rows)
   int kdim;                    // reduction length (H for gate_up, I for down)
   int kgroups;                 // 64-wide groups per weight row (Kdim / 64)
   const uint16_t* s_exp;       // [E][rows][kgroups] bf16 scales
