@@ -596,6 +596,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(b_wfree(s)));
+        // rebuild into registers first: only the TMEM stores wait for the
+        // slot, so a freed slot refills in the time of two stores
+        const uint32_t sv = (g4 & 2) ? s_cur.y : s_cur.x;
+        const uint32_t bv = (g4 & 2) ? b_cur.y : b_cur.x;
+        const uint32_t s2 = (g4 & 1) ? dup_hi(sv) : dup_lo(sv);
+        const uint32_t b2 = (g4 & 1) ? dup_hi(bv) : dup_lo(bv);
+        uint32_t v0[16], v1[16];
+        dequant_word_i4(w0.x, s2, b2, &v0[0]);
+        dequant_word_i4(w0.y, s2, b2, &v0[4]);
+        dequant_word_i4(w0.z, s2, b2, &v0[8]);
+        dequant_word_i4(w0.w, s2, b2, &v0[12]);
+        dequant_word_i4(w1.x, s2, b2, &v1[0]);
+        dequant_word_i4(w1.y, s2, b2, &v1[4]);
+        dequant_word_i4(w1.z, s2, b2, &v1[8]);
+        dequant_word_i4(w1.w, s2, b2, &v1[12]);
         const int as = ait % kNS;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar(b_sfree(as)), ((ait / kNS) & 1u) ^ 1u,
                                                abort_flag))) {
@@ -604,22 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ait;
         tc_fence_after();
-        const uint32_t sv = (g4 & 2) ? s_cur.y : s_cur.x;
-        const uint32_t bv = (g4 & 2) ? b_cur.y : b_cur.x;
-        const uint32_t s2 = (g4 & 1) ? dup_hi(sv) : dup_lo(sv);
-        const uint32_t b2 = (g4 & 1) ? dup_hi(bv) : dup_lo(bv);
-        uint32_t v[16];
         const uint32_t tcol = tmem + lane_off + kABase + as * kACols + g4 * 32;
-        dequant_word_i4(w0.x, s2, b2, &v[0]);
-        dequant_word_i4(w0.y, s2, b2, &v[4]);
-        dequant_word_i4(w0.z, s2, b2, &v[8]);
-        dequant_word_i4(w0.w, s2, b2, &v[12]);
-        tmem_st16(tcol, v);
-        dequant_word_i4(w1.x, s2, b2, &v[0]);
-        dequant_word_i4(w1.y, s2, b2, &v[4]);
-        dequant_word_i4(w1.z, s2, b2, &v[8]);
-        dequant_word_i4(w1.w, s2, b2, &v[12]);
-        tmem_st16(tcol + 16, v);
+        tmem_st16(tcol, v0);
+        tmem_st16(tcol + 16, v1);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
