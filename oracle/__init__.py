@@ -57,6 +57,8 @@ def lib():
             L.orc_rmsnorm_rows.argtypes = [P, i, i, P]
             L.orc_rmsnorm_gain_rows.argtypes = [P, P, i, i, P]
             L.orc_gdn_scan.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, P]
+            L.orc_gdn_scan64.argtypes = [P, P, P, P, P, P, i, i, i, i, i, P, P]
+            L.orc_gdn_chunked.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, P, P, P, P]
             L.orc_attn_decode.restype = i
             L.orc_attn_decode.argtypes = [P, P, P, P, i, i, i, i, i, i, i, P]
             L.orc_residual_add.argtypes = [P, P, C.c_size_t, P]
@@ -250,6 +252,46 @@ def gdn_scan(q, k, v, alpha, beta, state):
     lib().orc_gdn_scan(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(state), T, n_k, n_v, dk, dv,
                        _p(s_out), _p(o))
     return o, s_out
+
+
+def gdn_scan64(q, k, v, alpha, beta, state):
+    """The recurrence of gdn_scan with its results in fp64: (o [T][n_v][dv]
+    before the bf16 rounding, the final state [n_v][dv][dk])."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    alpha = _c(alpha, np.float32)
+    beta = _c(beta, np.float32)
+    state = _c(state, np.float32)
+    T, n_k, dk = q.shape
+    n_v, dv = v.shape[1], v.shape[2]
+    o64 = np.empty((T, n_v, dv), np.float64)
+    s64 = np.empty((n_v, dv, dk), np.float64)
+    lib().orc_gdn_scan64(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(state), T, n_k, n_v, dk,
+                         dv, _p(s64), _p(o64))
+    return o64, s64
+
+
+def gdn_chunked(q, k, v, alpha, beta, state, C):
+    """The gated delta rule in chunks of C tokens (the chunked form written
+    out in orc_gdn_chunked): returns (o bf16 bits, final state fp32, o in
+    fp64, the fp64 state after every chunk [n_chunks][n_v][dv][dk])."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    alpha = _c(alpha, np.float32)
+    beta = _c(beta, np.float32)
+    state = _c(state, np.float32)
+    T, n_k, dk = q.shape
+    n_v, dv = v.shape[1], v.shape[2]
+    nc = (T + C - 1) // C
+    o = np.empty((T, n_v, dv), np.uint16)
+    s_out = np.empty_like(state)
+    o64 = np.empty((T, n_v, dv), np.float64)
+    sc = np.empty((nc, n_v, dv, dk), np.float64)
+    lib().orc_gdn_chunked(_p(q), _p(k), _p(v), _p(alpha), _p(beta), _p(state), T, n_k, n_v, dk,
+                          dv, C, _p(s_out), _p(o), _p(o64), _p(sc))
+    return o, s_out, o64, sc
 
 
 def route(L, K):

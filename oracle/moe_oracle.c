@@ -500,9 +500,10 @@ int orc_attn_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* 
  *   o_t = S q_t   (RNE to bf16).
  * q, k [T][n_k][dk] and v [T][n_v][dv] are bf16 bits; alpha, beta [T][n_v]
  * and the states [n_v][dv][dk] are fp32 (s_out may equal s_in). */
-void orc_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
-                  const float* beta, const float* s_in, int T, int n_k, int n_v, int dk, int dv,
-                  float* s_out, uint16_t* o) {
+static void gdn_scan_core(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const float* alpha, const float* beta, const float* s_in, int T,
+                          int n_k, int n_v, int dk, int dv, float* s_out, uint16_t* o,
+                          double* o64, double* s_out64) {
   const int group = n_v / n_k;
   double* S = (double*)malloc(sizeof(double) * (size_t)dv * dk);
   double* Sk = (double*)malloc(sizeof(double) * (size_t)dv);
@@ -529,13 +530,158 @@ void orc_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
       for (int i = 0; i < dv; ++i) {
         double acc = 0.0;
         for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * orc_bf16_value(qt[j]);
-        o[((size_t)t * n_v + h) * dv + i] = orc_bf16_rne(acc);
+        if (o) o[((size_t)t * n_v + h) * dv + i] = orc_bf16_rne(acc);
+        if (o64) o64[((size_t)t * n_v + h) * dv + i] = acc;
       }
     }
-    for (size_t i = 0; i < (size_t)dv * dk; ++i) s_out[(size_t)h * dv * dk + i] = (float)S[i];
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) {
+      if (s_out) s_out[(size_t)h * dv * dk + i] = (float)S[i];
+      if (s_out64) s_out64[(size_t)h * dv * dk + i] = S[i];
+    }
   }
   free(S);
   free(Sk);
+}
+
+void orc_gdn_scan(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                  const float* beta, const float* s_in, int T, int n_k, int n_v, int dk, int dv,
+                  float* s_out, uint16_t* o) {
+  gdn_scan_core(q, k, v, alpha, beta, s_in, T, n_k, n_v, dk, dv, s_out, o, NULL, NULL);
+}
+
+/* The same recurrence with its results kept in fp64 (outputs before the
+ * bf16 rounding, and the final state): for comparing other forms of the
+ * rule with it at full precision. */
+void orc_gdn_scan64(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                    const float* beta, const float* s_in, int T, int n_k, int n_v, int dk,
+                    int dv, double* s_out64, double* o64) {
+  gdn_scan_core(q, k, v, alpha, beta, s_in, T, n_k, n_v, dk, dv, NULL, NULL, o64, s_out64);
+}
+
+/*
+ * The same gated delta rule in its chunked (parallel) form: chunks of C
+ * tokens, each solved as a whole from the state S0 before it. This is the
+ * WY / UT-transform form of the delta rule (Yang et al., "Gated Delta
+ * Networks: Improving Mamba2 with Delta Rule", chunkwise algorithm),
+ * written out here from the recurrence above. Within a chunk (tokens
+ * t = 1..n), with g_t = alpha_1 ... alpha_t (g_0 = 1) and
+ * u_t = beta_t (v_t - alpha_t S_{t-1} k_t), the recurrence reads
+ * S_t = alpha_t S_{t-1} + u_t k_t^T, so S_t = g_t S0 + sum_{s<=t} (g_t/g_s) u_s k_s^T.
+ * Putting that S_{t-1} into u_t gives a unit lower-triangular system:
+ *   (1) g_t, t = 1..n
+ *   (2) A[t][s] = beta_t (g_t / g_s) (k_t . k_s) for s < t, 0 otherwise
+ *   (3) Tm = (I + A)^-1 (forward substitution)
+ *   (4) W1 = Tm diag(beta) V  [n x dv],  W2 = Tm diag(beta g) K  [n x dk]
+ *   (5) U = W1 - W2 S0^T  [n x dv]  (row t = u_t)
+ *   (6) O = diag(g) Q S0^T + (Mk o (Q K^T)) U, Mk[t][s] = g_t / g_s for s <= t, else 0
+ *   (7) S = g_n S0 + U^T diag(g_n / g) K
+ * o_t = row t of O. All in fp64; o is rounded to bf16 at the end, as in
+ * orc_gdn_scan. s_chunks64 (nullable) receives the state after every chunk,
+ * [n_chunks][n_v][dv][dk]; o64 (nullable) the unrounded outputs.
+ */
+void orc_gdn_chunked(const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* alpha,
+                     const float* beta, const float* s_in, int T, int n_k, int n_v, int dk,
+                     int dv, int C, float* s_out, uint16_t* o, double* o64, double* s_chunks64) {
+  const int group = n_v / n_k;
+  const int n_chunks = (T + C - 1) / C;
+  double* S = (double*)malloc(sizeof(double) * (size_t)dv * dk);
+  double* Sn = (double*)malloc(sizeof(double) * (size_t)dv * dk);
+  double* g = (double*)malloc(sizeof(double) * (size_t)C);
+  double* Kc = (double*)malloc(sizeof(double) * (size_t)C * dk);
+  double* Qc = (double*)malloc(sizeof(double) * (size_t)C * dk);
+  double* Vc = (double*)malloc(sizeof(double) * (size_t)C * dv);
+  double* A = (double*)malloc(sizeof(double) * (size_t)C * C);
+  double* Tm = (double*)malloc(sizeof(double) * (size_t)C * C);
+  double* W1 = (double*)malloc(sizeof(double) * (size_t)C * dv);
+  double* W2 = (double*)malloc(sizeof(double) * (size_t)C * dk);
+  double* U = (double*)malloc(sizeof(double) * (size_t)C * dv);
+  double* QK = (double*)malloc(sizeof(double) * (size_t)C * C);
+  for (int h = 0; h < n_v; ++h) {
+    const int hk = h / group;
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) S[i] = s_in[(size_t)h * dv * dk + i];
+    for (int c = 0; c < n_chunks; ++c) {
+      const int t0 = c * C, n = (T - t0 < C) ? T - t0 : C;
+      const float* al = alpha + (size_t)t0 * n_v + h;
+      const float* be = beta + (size_t)t0 * n_v + h;
+      for (int t = 0; t < n; ++t) {
+        for (int j = 0; j < dk; ++j) {
+          Kc[(size_t)t * dk + j] = orc_bf16_value(k[((size_t)(t0 + t) * n_k + hk) * dk + j]);
+          Qc[(size_t)t * dk + j] = orc_bf16_value(q[((size_t)(t0 + t) * n_k + hk) * dk + j]);
+        }
+        for (int i = 0; i < dv; ++i)
+          Vc[(size_t)t * dv + i] = orc_bf16_value(v[((size_t)(t0 + t) * n_v + h) * dv + i]);
+      }
+      /* (1) */
+      for (int t = 0; t < n; ++t) g[t] = (t ? g[t - 1] : 1.0) * (double)al[(size_t)t * n_v];
+      /* (2) and Q K^T */
+      for (int t = 0; t < n; ++t)
+        for (int s2 = 0; s2 < n; ++s2) {
+          double kk = 0.0, qk = 0.0;
+          for (int j = 0; j < dk; ++j) {
+            kk += Kc[(size_t)t * dk + j] * Kc[(size_t)s2 * dk + j];
+            qk += Qc[(size_t)t * dk + j] * Kc[(size_t)s2 * dk + j];
+          }
+          A[(size_t)t * C + s2] = s2 < t ? (double)be[(size_t)t * n_v] * (g[t] / g[s2]) * kk : 0.0;
+          QK[(size_t)t * C + s2] = s2 <= t ? (g[t] / g[s2]) * qk : 0.0;
+        }
+      /* (3) Tm (I + A) = I, row by row: Tm[t] = e_t - sum_{r<t} A[t][r] Tm[r] */
+      for (int t = 0; t < n; ++t)
+        for (int s2 = 0; s2 < n; ++s2) {
+          double x = (s2 == t) ? 1.0 : 0.0;
+          for (int r = s2; r < t; ++r) x -= A[(size_t)t * C + r] * Tm[(size_t)r * C + s2];
+          Tm[(size_t)t * C + s2] = s2 <= t ? x : 0.0;
+        }
+      /* (4) */
+      for (int t = 0; t < n; ++t) {
+        for (int i = 0; i < dv; ++i) {
+          double x = 0.0;
+          for (int s2 = 0; s2 <= t; ++s2)
+            x += Tm[(size_t)t * C + s2] * (double)be[(size_t)s2 * n_v] * Vc[(size_t)s2 * dv + i];
+          W1[(size_t)t * dv + i] = x;
+        }
+        for (int j = 0; j < dk; ++j) {
+          double x = 0.0;
+          for (int s2 = 0; s2 <= t; ++s2)
+            x += Tm[(size_t)t * C + s2] * (double)be[(size_t)s2 * n_v] * g[s2] *
+                 Kc[(size_t)s2 * dk + j];
+          W2[(size_t)t * dk + j] = x;
+        }
+      }
+      /* (5) */
+      for (int t = 0; t < n; ++t)
+        for (int i = 0; i < dv; ++i) {
+          double x = W1[(size_t)t * dv + i];
+          for (int j = 0; j < dk; ++j) x -= W2[(size_t)t * dk + j] * S[(size_t)i * dk + j];
+          U[(size_t)t * dv + i] = x;
+        }
+      /* (6) */
+      for (int t = 0; t < n; ++t)
+        for (int i = 0; i < dv; ++i) {
+          double x = 0.0;
+          for (int j = 0; j < dk; ++j) x += Qc[(size_t)t * dk + j] * S[(size_t)i * dk + j];
+          x *= g[t];
+          for (int s2 = 0; s2 <= t; ++s2) x += QK[(size_t)t * C + s2] * U[(size_t)s2 * dv + i];
+          const size_t oi = ((size_t)(t0 + t) * n_v + h) * dv + i;
+          if (o) o[oi] = orc_bf16_rne(x);
+          if (o64) o64[oi] = x;
+        }
+      /* (7) */
+      for (int i = 0; i < dv; ++i)
+        for (int j = 0; j < dk; ++j) {
+          double x = g[n - 1] * S[(size_t)i * dk + j];
+          for (int t = 0; t < n; ++t)
+            x += U[(size_t)t * dv + i] * (g[n - 1] / g[t]) * Kc[(size_t)t * dk + j];
+          Sn[(size_t)i * dk + j] = x;
+        }
+      memcpy(S, Sn, sizeof(double) * (size_t)dv * dk);
+      if (s_chunks64)
+        memcpy(s_chunks64 + ((size_t)c * n_v + h) * dv * dk, S, sizeof(double) * (size_t)dv * dk);
+    }
+    for (size_t i = 0; i < (size_t)dv * dk; ++i)
+      if (s_out) s_out[(size_t)h * dv * dk + i] = (float)S[i];
+  }
+  free(S); free(Sn); free(g); free(Kc); free(Qc); free(Vc); free(A); free(Tm); free(W1);
+  free(W2); free(U); free(QK);
 }
 
 int orc_num_threads(void) {

@@ -491,3 +491,46 @@ def test_gdn_matches_the_matrix_form_in_torch():
         got = synth.bf16_bits_to_f32(o[t]).astype(np.float64)
         assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max()
     assert np.allclose(s_end, S.numpy(), rtol=1e-5, atol=1e-6)
+
+
+# --------------------------------------- Gated DeltaNet, chunked form --
+@pytest.mark.parametrize("C", [1, 16, 64, 24])
+def test_gdn_chunked_equals_the_recurrence(C):
+    """The chunked (WY / UT) form of the gated delta rule against the
+    token-by-token recurrence (itself pinned above to closed forms and to
+    the matrix form in torch): in fp64 the state after every chunk and
+    every output agree to rounding, for chunk sizes 1, 16, 64 and 24 (a
+    ragged last chunk of 16)."""
+    T, n_k, n_v, dk, dv = 64, 2, 4, 32, 16
+    q, k, v, alpha, beta, s0 = synth.gen_gdn(T, n_k, n_v, dk, dv, seed=31)
+    o_c, s_c, o64_c, sc = oracle.gdn_chunked(q, k, v, alpha, beta, s0, C)
+    o64_r, s64_r = oracle.gdn_scan64(q, k, v, alpha, beta, s0)
+    scale = np.abs(o64_r).max()
+    assert np.abs(o64_c - o64_r).max() <= 1e-11 * scale
+    for c in range(sc.shape[0]):
+        t_end = min((c + 1) * C, T)
+        _, s_pref = oracle.gdn_scan64(q[:t_end], k[:t_end], v[:t_end], alpha[:t_end],
+                                      beta[:t_end], s0)
+        assert np.abs(sc[c] - s_pref).max() <= 1e-11 * np.abs(s_pref).max(), c
+    assert np.abs(s_c.astype(np.float64) - s64_r).max() <= 1e-6 * np.abs(s64_r).max()
+    o_r, _ = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    # the bf16 outputs may differ only where the fp64 values straddle a rounding boundary
+    assert np.mean(o_c != o_r) < 1e-3
+
+
+def test_gdn_chunked_special_cases():
+    """beta = 0: no write, each chunk only decays the state (the triangular
+    system is the identity); one chunk holding the whole sequence equals the
+    recurrence too; a planted mistake in the decay (alpha squared) is
+    caught."""
+    T, n_k, n_v, dk, dv = 20, 1, 2, 16, 8
+    q, k, v, alpha, beta, s0 = synth.gen_gdn(T, n_k, n_v, dk, dv, seed=32)
+    _, _, _, sc = oracle.gdn_chunked(q, k, v, alpha, np.zeros_like(beta), s0, 8)
+    decay = np.cumprod(alpha.astype(np.float64), axis=0)
+    for c, t_end in enumerate((8, 16, 20)):
+        assert np.allclose(sc[c], s0 * decay[t_end - 1][:, None, None], rtol=1e-12)
+    _, _, o64_whole, _ = oracle.gdn_chunked(q, k, v, alpha, beta, s0, T)
+    o64_r, _ = oracle.gdn_scan64(q, k, v, alpha, beta, s0)
+    assert np.abs(o64_whole - o64_r).max() <= 1e-11 * np.abs(o64_r).max()
+    _, _, o64_bad, _ = oracle.gdn_chunked(q, k, v, alpha * alpha, beta, s0, 8)
+    assert np.abs(o64_bad - o64_r).max() > 1e-3 * np.abs(o64_r).max()
