@@ -34,7 +34,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_max_blocks", "moe_workspace_init", "moe_r
            "moe_status_string",
            "moe_last_error", "moe_plan_noalloc", "moe_layer_path", "moe_decode_layers",
            "moe_decoder_blocks", "moe_attn_workspace_bytes", "moe_attn_decode",
-           "moe_gdn_scan")
+           "moe_gdn_scan", "moe_gdn_chunked_workspace_bytes", "moe_gdn_chunked_scan")
 
 
 class MoeError(RuntimeError):
@@ -101,6 +101,8 @@ def load():
             L.moe_max_blocks.argtypes = [pS]
             L.moe_layer_path.restype = I32
             L.moe_layer_path.argtypes = [pS]
+            L.moe_gdn_chunked_workspace_bytes.restype = SZ
+            L.moe_gdn_chunked_workspace_bytes.argtypes = [C.POINTER(GdnShape)]
             L.moe_attn_workspace_bytes.restype = SZ
             L.moe_attn_workspace_bytes.argtypes = [C.POINTER(AttnShape)]
             for name, args in (
@@ -117,7 +119,9 @@ def load():
                     ("moe_decode_layers", [pS, I32, P, P, P, P, P, SZ, P]),
                     ("moe_decoder_blocks", [pS, I32, P, P, P, P, P, I32, P, P, SZ, P]),
                     ("moe_attn_decode", [C.POINTER(AttnShape), P, P, P, P, I32, P, P, SZ, P]),
-                    ("moe_gdn_scan", [C.POINTER(GdnShape), P, P, P, P, P, P, P, P, P])):
+                    ("moe_gdn_scan", [C.POINTER(GdnShape), P, P, P, P, P, P, P, P, P]),
+                    ("moe_gdn_chunked_scan",
+                     [C.POINTER(GdnShape), P, P, P, P, P, P, P, P, P, SZ, P])):
                 f = getattr(L, name)
                 f.restype = C.c_int
                 f.argtypes = args
@@ -248,6 +252,23 @@ def moe_gdn_scan(shape, q, k, v, alpha, beta, state_in, state_out, o, stream=Non
     """Gated delta rule over shape.T tokens (state_out may be state_in)."""
     _check(load().moe_gdn_scan(C.byref(shape), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
                                _p(state_in), _p(state_out), _p(o), _s(stream)), "moe_gdn_scan")
+
+
+def alloc_gdn_workspace(shape, device):
+    """Device workspace of the chunked scan (moe_gdn_chunked_workspace_bytes)."""
+    nbytes = load().moe_gdn_chunked_workspace_bytes(C.byref(shape))
+    if nbytes == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_gdn_chunked_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def moe_gdn_chunked_scan(shape, q, k, v, alpha, beta, state_in, state_out, o, ws, stream=None):
+    """Chunked (parallel) form of the gated delta rule; same results as
+    moe_gdn_scan within fp32 rounding (state_out may be state_in)."""
+    _check(load().moe_gdn_chunked_scan(C.byref(shape), _p(q), _p(k), _p(v), _p(alpha), _p(beta),
+                                       _p(state_in), _p(state_out), _p(o), _p(ws),
+                                       ws.numel() * ws.element_size(), _s(stream)),
+           "moe_gdn_chunked_scan")
 
 
 def gain_table(gains):

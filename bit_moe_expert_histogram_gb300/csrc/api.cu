@@ -646,6 +646,30 @@ moe_status_t moe_gdn_scan(const moe_gdn_shape_t* shape, const void* q_dev, const
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "gated delta scan launch");
 }
 
+size_t moe_gdn_chunked_workspace_bytes(const moe_gdn_shape_t* shape) {
+  if (!gdn_supported(shape) || shape->dv > 128) return 0;
+  return gdn_chunk_ws_bytes(shape);
+}
+
+moe_status_t moe_gdn_chunked_scan(const moe_gdn_shape_t* shape, const void* q_dev,
+                                  const void* k_dev, const void* v_dev, const float* alpha_dev,
+                                  const float* beta_dev, const float* state_in_dev,
+                                  float* state_out_dev, void* o_dev, void* ws_dev,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  if (!gdn_supported(shape) || shape->dv > 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!q_dev || !k_dev || !v_dev || !alpha_dev || !beta_dev || !state_in_dev || !state_out_dev ||
+      !o_dev || !ws_dev || !aligned16(q_dev) || !aligned16(k_dev) || !aligned16(v_dev) ||
+      !aligned16(state_in_dev) || !aligned16(state_out_dev) || !aligned16(o_dev) ||
+      !aligned16(ws_dev))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < gdn_chunk_ws_bytes(shape)) return MOE_ERR_WORKSPACE;
+  cudaError_t e = launch_gdn_chunked(
+      shape, static_cast<const uint16_t*>(q_dev), static_cast<const uint16_t*>(k_dev),
+      static_cast<const uint16_t*>(v_dev), alpha_dev, beta_dev, state_in_dev, state_out_dev,
+      static_cast<uint16_t*>(o_dev), static_cast<float*>(ws_dev), (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "chunked gated delta scan launch");
+}
+
 size_t moe_attn_workspace_bytes(const moe_attn_shape_t* shape) {
   if (!attn_supported(shape)) return 0;
   return 256 + attn_part_floats(shape) * 4;

@@ -163,6 +163,12 @@ bool gdn_supported(const moe_gdn_shape_t* s);
 cudaError_t launch_gdn_scan(const moe_gdn_shape_t* s, const uint16_t* q, const uint16_t* k,
                             const uint16_t* v, const float* alpha, const float* beta,
                             const float* s_in, float* s_out, uint16_t* o, cudaStream_t stream);
+// Chunked form of the same rule (gdn_chunk.cu): workspace bytes, launch.
+size_t gdn_chunk_ws_bytes(const moe_gdn_shape_t* s);
+cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, const uint16_t* k,
+                               const uint16_t* v, const float* alpha, const float* beta,
+                               const float* s_in, float* s_out, uint16_t* o, float* ws,
+                               cudaStream_t stream);
 // Host helpers shared by the C-ABI translation units (api.cu keeps the state).
 bool shape_supported(const moe_shape_t* shape);
 void set_last_error(const char* text);

@@ -383,6 +383,26 @@ moe_status_t moe_gdn_scan(const moe_gdn_shape_t* shape, const void* q_dev, const
                           const float* state_in_dev, float* state_out_dev, void* o_dev,
                           moe_stream_t stream);
 
+/* The same rule in its chunked (parallel) form, for prompts: chunks of 64
+ * tokens, each solved as a whole from the state before it (the WY / UT form
+ * of the delta rule: with g_t the running product of alpha over the chunk,
+ * the chunk's writes solve a unit lower-triangular system whose matrix and
+ * right-hand sides depend only on the chunk's k, v, alpha and beta), so the
+ * work inside a chunk runs in parallel over its tokens and only the chunks
+ * follow one another. Same inputs, outputs and supported shapes as
+ * moe_gdn_scan (dv <= 128 as well), results within fp32 rounding of it;
+ * fp32 arithmetic. ws_dev: device workspace of at least
+ * moe_gdn_chunked_workspace_bytes(shape) bytes, 16-byte aligned, caller
+ * owned (per chunk and value head the chunk's two solved right-hand sides,
+ * its decay-masked q.k matrix and its decays). Errors: as moe_gdn_scan, plus
+ * MOE_ERR_WORKSPACE when ws_bytes is too small. */
+size_t moe_gdn_chunked_workspace_bytes(const moe_gdn_shape_t* shape);
+moe_status_t moe_gdn_chunked_scan(const moe_gdn_shape_t* shape, const void* q_dev,
+                                  const void* k_dev, const void* v_dev, const float* alpha_dev,
+                                  const float* beta_dev, const float* state_in_dev,
+                                  float* state_out_dev, void* o_dev, void* ws_dev,
+                                  size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

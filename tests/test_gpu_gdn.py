@@ -72,3 +72,58 @@ def test_gdn_rejects_unsupported_shapes():
                  (0, 16, 32, 128, 128)]:
         with pytest.raises(m.MoeError):
             m.moe_gdn_scan(m.make_gdn_shape(*args), z, z, z, z, z, z, z, z)
+
+
+# ----------------------------------------------------- chunked form --
+def run_chunked(T, n_k, n_v, dk, dv, inputs, state=None):
+    q, k, v, alpha, beta, s0 = inputs
+    if state is not None:
+        s0 = state
+    shape = m.make_gdn_shape(T, n_k, n_v, dk, dv)
+    ws = m.alloc_gdn_workspace(shape, "cuda")
+    sd = dev_f32(s0)
+    o = torch.zeros((T, n_v, dv), dtype=torch.int16, device="cuda")
+    m.moe_gdn_chunked_scan(shape, d16(q, "cuda"), d16(k, "cuda"), d16(v, "cuda"), dev_f32(alpha),
+                           dev_f32(beta), sd, sd, o, ws)
+    torch.cuda.synchronize()
+    return h16(o).copy(), sd.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,n_k,n_v,dv", [(1, 16, 32, 128), (64, 16, 32, 128), (2048, 16, 32, 128),
+                                          (100, 4, 8, 64), (65, 2, 2, 16), (130, 16, 32, 128)])
+def test_gdn_chunked_against_the_oracle(T, n_k, n_v, dv):
+    """The chunked scan (chunks of 64, ragged last chunks included) against
+    the oracle's token-by-token recurrence, outputs and final state."""
+    inp = synth.gen_gdn(T, n_k, n_v, 128, dv, seed=T * 3 + n_v)
+    o, s_end = run_chunked(T, n_k, n_v, 128, dv, inp)
+    o_ref, s_ref = oracle.gdn_scan(*inp)
+    close(f64(o), f64(o_ref), "o")
+    close(s_end, s_ref, "state")
+
+
+def test_gdn_chunked_equals_the_recurrent_kernel_and_carries_state():
+    """Both device forms give the same outputs and state within the layer's
+    tolerance; the chunked form's state carries across calls (two calls of
+    96 tokens against one of 192)."""
+    T, n_k, n_v, dv = 192, 16, 32, 128
+    inp = synth.gen_gdn(T, n_k, n_v, 128, dv, seed=9)
+    q, k, v, alpha, beta, s0 = inp
+    o_r, s_r, _ = run(T, n_k, n_v, 128, dv, 0, inputs=inp)
+    o_c, s_c = run_chunked(T, n_k, n_v, 128, dv, inp)
+    close(f64(o_c), f64(o_r), "o")
+    close(s_c, s_r, "state")
+    o_a, s_a = run_chunked(96, n_k, n_v, 128, dv, (q[:96], k[:96], v[:96], alpha[:96], beta[:96], s0))
+    o_b, s_b = run_chunked(96, n_k, n_v, 128, dv, (q[96:], k[96:], v[96:], alpha[96:], beta[96:], s_a))
+    close(f64(np.concatenate([o_a, o_b])), f64(o_c), "o in two calls")
+    close(s_b, s_c, "state in two calls")
+
+
+def test_gdn_chunked_rejects_unsupported_shapes_and_small_workspace():
+    z = torch.zeros(64, dtype=torch.float32, device="cuda")
+    shape = m.make_gdn_shape(4, 2, 2, 128, 256)   # dv > 128
+    assert m.load().moe_gdn_chunked_workspace_bytes(shape) == 0
+    with pytest.raises(m.MoeError):
+        m.moe_gdn_chunked_scan(shape, z, z, z, z, z, z, z, z, z)
+    shape = m.make_gdn_shape(4, 2, 2, 128, 16)
+    with pytest.raises(m.MoeError):
+        m.moe_gdn_chunked_scan(shape, z, z, z, z, z, z, z, z, z)   # 256 bytes of workspace
