@@ -15,18 +15,26 @@
 //   U  = W1 - W2 S0^T
 //   O  = diag(g) Q S0^T + (Mk o Q K^T) U,   Mk[t][s] = g_t / g_s for s <= t
 //   S  = g_C S0 + U^T diag(g_C / g) K
+// The gate ratios are taken as g_t / g_s = exp(G_t - G_s) with G_t the sum
+// of log alpha over the chunk, so a chunk of fast decay never divides two
+// products that underflow.
 // Two launches:
-//   gdn_chunk_prep_kernel  one CTA per (chunk, value head), all chunks at
-//                          once: g, K K^T and Q K^T, A, then W1 and W2 by
-//                          forward substitution (each thread owns one
-//                          column of [W1 | W2], so the substitution needs no
-//                          barrier), and P = Mk o Q K^T, into the workspace
-//   gdn_chunk_scan_kernel  one CTA per (value head, 32 or 16 state rows): row i of
-//                          S only ever meets row i of the state, so the
-//                          chunks run in order within the CTA and the rows
-//                          of a head in parallel across CTAs; U, O and the
-//                          new rows from the chunk's W1, W2, P, Q and K
-// All arithmetic is fp32 (the inputs are bf16, exact in fp32).
+//   gdn_chunk_prep_kernel     one CTA per (chunk, value head), all chunks at
+//                             once: G, K K^T and Q K^T, A and P = Mk o Q K^T,
+//                             T = (I + A)^-1 by 16 x 16 blocks, then
+//                             W1 = T diag(beta) V and W2 = T diag(beta g) K,
+//                             into the workspace
+//   gdn_chunk_scan_tc_kernel  one CTA per (value head, 32 state rows): row i
+//                             of S only ever meets row i of the state, so the
+//                             chunks run in order within the CTA and the rows
+//                             of a head in parallel across CTAs; U, O and the
+//                             new rows from the chunk's W1, W2, P, Q and K
+//   (gdn_chunk_scan_kernel, the same scan on CUDA cores, 16 rows per CTA,
+//   serves value heads whose size is not a multiple of 32)
+// Sums are fp32. The products run on the tensor cores with mma.sync (bf16
+// inputs where both factors are bf16; tf32 where one carries fp32 values,
+// that factor split into two tf32 parts so that the product keeps about fp32
+// accuracy).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -37,9 +45,10 @@ constexpr int kDK = 128;   // key head size
 constexpr int kCh = 64;    // tokens per chunk
 constexpr int kThr = 256;
 
-// per (chunk, head) block of the workspace: W1 [C][dv], W2 [C][dk], P [C][C], g [C]
+// per (chunk, head) block of the workspace: W1 [C][dv], W2 [C][dk],
+// P [C][C], g [C] (g_t), gr [C] (g_C / g_t)
 __host__ __device__ __forceinline__ size_t blk_floats(int dv) {
-  return (size_t)kCh * dv + (size_t)kCh * kDK + (size_t)kCh * kCh + kCh;
+  return (size_t)kCh * dv + (size_t)kCh * kDK + (size_t)kCh * kCh + 2 * kCh;
 }
 
 __device__ __forceinline__ void bf8_to_f(const uint4& v, float* f) {
@@ -47,139 +56,299 @@ __device__ __forceinline__ void bf8_to_f(const uint4& v, float* f) {
   f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
 }
 
-constexpr int kPrepSmemFloats = kDK * kCh * 2 + kCh * kDK + kCh * kCh + kCh * 256 + 2 * kCh;
+// fp32 -> tf32 (round to nearest, ties away) in a 32-bit register
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo with both parts tf32: three tf32 products (hi*hi + hi*lo +
+// lo*hi) then carry an fp32 operand at about fp32 accuracy
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+// D += A * B, m16n8k8, tf32 inputs, fp32 accumulators (fragment layouts of
+// the PTX ISA: A row-major a0 (g, c) a1 (g+8, c) a2 (g, c+4) a3 (g+8, c+4);
+// B column-major b0 (k = c, n = g) b1 (c+4, g); D d0 (g, 2c) d1 (g, 2c+1)
+// d2 (g+8, 2c) d3 (g+8, 2c+1); g = lane / 4, c = lane % 4)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulators (A row-major: reg 0
+// row g cols 2c, 2c+1; reg 1 row g+8; regs 2, 3 the same 8 columns on; B
+// column-major: reg 0 k = 2c, 2c+1 at n = g, reg 1 k + 8)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// prep tiles: bf16 rows of 136 halves (68 words) and fp32 rows of 72 / 68
+// floats put the fragment loads and stores of the MMAs on 32 distinct banks
+constexpr int kLdH = 136;
+constexpr int kLdA = 72;
+constexpr int kLdT = 68;
+constexpr int kPrepSmemBytes = (kCh * kLdA + kCh * kLdT + 3 * 256 + 3 * kCh) * 4 + 3 * kCh * kLdH * 2;
 constexpr int kLd = kDK + 1;  // padded row of a [C][dk] tile: rows t and t+1 start in other banks
 constexpr int kLdP = kCh + 1;
+// tensor-core scan tiles (32 state rows): padded so that every fragment
+// load of the MMAs touches 32 distinct banks
+constexpr int kTcLdS = 40;    // ST [dk][40]
+constexpr int kTcLd = 132;    // W2, Q [C][132] (A operands)
+constexpr int kTcLdK = 136;   // K [C][136] (B operand)
+constexpr int kTcLdP = 68;    // P [C][68]
+constexpr int kTcLdU = 40;    // W1 rows, U, Ug [C][40]
+constexpr int kTcSmemFloats =
+    kDK * kTcLdS + 2 * kCh * kTcLd + kCh * kTcLdK + kCh * kTcLdP + 3 * kCh * kTcLdU + 2 * kCh;
 template <int R>
 constexpr int scan_smem_floats() {
-  return kDK * (R + 1) + 2 * kCh * kLd + kCh * kDK + kCh * kLdP + 3 * kCh * R + kCh;
+  return kDK * (R + 1) + 2 * kCh * kLd + kCh * kDK + kCh * kLdP + 3 * kCh * R + 2 * kCh;
 }
 }  // namespace
 
-__global__ void __launch_bounds__(kThr, 1)
+// grid (n_chunks, n_v): one CTA per (chunk, value head), two CTAs per SM.
+//  1. K, Q, V of the chunk into shared memory as bf16; G_t = sum of log alpha
+//     over the chunk (a warp scan), so every gate ratio g_t / g_s is
+//     exp(G_t - G_s) and never a quotient of two products that underflow
+//  2. K K^T and Q K^T on the tensor cores (mma.sync m16n8k16 bf16, exact
+//     products, fp32 sums), lower triangle only; A and P from them
+//  3. T = (I + A)^-1 by 16 x 16 blocks: the four diagonal blocks by
+//     forward substitution (one thread per column), then the blocks below
+//     them by distance from the diagonal, T_ij = -T_ii sum_k A_ik T_kj
+//  4. W1 = (T diag(beta)) V and W2 = (T diag(beta g)) K on the tensor cores
+//     (mma.sync m16n8k8 tf32): the fp32 left factor is split into tf32
+//     hi + lo, the bf16 right factor is exact in tf32
+__global__ void __launch_bounds__(kThr, 2)
     gdn_chunk_prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                           const uint16_t* __restrict__ v, const float* __restrict__ alpha,
                           const float* __restrict__ beta, int T, int n_k, int n_v, int dv,
                           float* __restrict__ ws) {
   extern __shared__ float sm[];
-  float* KT = sm;                // [dk][C]  K transposed
-  float* QT = KT + kDK * kCh;    // [dk][C]  Q transposed
-  float* V = QT + kDK * kCh;     // [C][128] (dv columns used)
-  float* A = V + kCh * kDK;      // [C][C]
-  float* W = A + kCh * kCh;      // [C][256]: columns 0..dv-1 W1, 128..255 W2
-  float* g = W + kCh * 256;      // [C]
-  float* bt = g + kCh;           // [C]
-  const int tid = threadIdx.x;
+  float* As = sm;                                      // [C][kLdA]
+  float* Ts = As + kCh * kLdA;                         // [C][kLdT]
+  float* Xs = Ts + kCh * kLdT;                         // 3 x [16][16] scratch
+  float* G = Xs + 3 * 256;                             // [C] log gates
+  float* bt = G + kCh;                                 // [C] beta
+  float* bg = bt + kCh;                                // [C] beta g
+  uint16_t* Kb = reinterpret_cast<uint16_t*>(bg + kCh);  // [C][kLdH]
+  uint16_t* Qb = Kb + kCh * kLdH;                      // [C][kLdH]
+  uint16_t* Vb = Qb + kCh * kLdH;                      // [C][kLdH]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, cq = lane & 3;
   const int c = blockIdx.x, h = blockIdx.y, hk = h / (n_v / n_k);
   const int t0 = c * kCh, n = min(kCh, T - t0);
   // tokens past the sequence end read as k = q = v = 0, alpha = 1, beta = 0:
   // they leave every quantity below unchanged
+  const uint4 z4 = make_uint4(0, 0, 0, 0);
   for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
-    const int t = idx % kCh, ch = idx / kCh;
-    float kf[8] = {0, 0, 0, 0, 0, 0, 0, 0}, qf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const int t = idx >> 4, ch = idx & 15;
+    uint4 kv = z4, qv = z4;
     if (t < n) {
       const size_t src = ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8;
-      bf8_to_f(__ldg(reinterpret_cast<const uint4*>(k + src)), kf);
-      bf8_to_f(__ldg(reinterpret_cast<const uint4*>(q + src)), qf);
+      kv = __ldg(reinterpret_cast<const uint4*>(k + src));
+      qv = __ldg(reinterpret_cast<const uint4*>(q + src));
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      KT[(ch * 8 + e) * kCh + t] = kf[e];
-      QT[(ch * 8 + e) * kCh + t] = qf[e];
-    }
+    *reinterpret_cast<uint4*>(Kb + t * kLdH + ch * 8) = kv;
+    *reinterpret_cast<uint4*>(Qb + t * kLdH + ch * 8) = qv;
   }
   const int vch = dv / 8;
   for (int idx = tid; idx < kCh * vch; idx += kThr) {
     const int t = idx / vch, ch = idx % vch;
-    float vf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (t < n)
-      bf8_to_f(__ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + t) * n_v + h) * dv + ch * 8)),
-               vf);
-    float4* dst = reinterpret_cast<float4*>(V + t * kDK + ch * 8);
-    dst[0] = make_float4(vf[0], vf[1], vf[2], vf[3]);
-    dst[1] = make_float4(vf[4], vf[5], vf[6], vf[7]);
+    uint4 vv = z4;
+    if (t < n) vv = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + t) * n_v + h) * dv + ch * 8));
+    *reinterpret_cast<uint4*>(Vb + t * kLdH + ch * 8) = vv;
   }
-  if (tid < kCh) {
-    g[tid] = tid < n ? __ldg(alpha + (size_t)(t0 + tid) * n_v + h) : 1.0f;
-    bt[tid] = tid < n ? __ldg(beta + (size_t)(t0 + tid) * n_v + h) : 0.0f;
-  }
-  __syncthreads();
-  if (tid == 0) {  // g_t = alpha_1 ... alpha_t
-    float p = 1.0f;
-    for (int t = 0; t < kCh; ++t) {
-      p *= g[t];
-      g[t] = p;
-    }
-  }
-  __syncthreads();
   float* blk = ws + ((size_t)c * n_v + h) * blk_floats(dv);
   float* gW1 = blk;
   float* gW2 = gW1 + (size_t)kCh * dv;
   float* gP = gW2 + (size_t)kCh * kDK;
   float* gG = gP + (size_t)kCh * kCh;
+  if (warp == 0) {
+    // log alpha, bounded below so that a gate of exactly 0 still gives
+    // finite differences (exp(-100) is 0 to fp32 precision in every product)
+    const int ta = 2 * lane, tb = 2 * lane + 1;
+    const float la = ta < n ? fmaxf(logf(__ldg(alpha + (size_t)(t0 + ta) * n_v + h)), -100.0f) : 0.0f;
+    const float lb = tb < n ? fmaxf(logf(__ldg(alpha + (size_t)(t0 + tb) * n_v + h)), -100.0f) : 0.0f;
+    float incl = la + lb;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    const float Ga = incl - lb, Gb = incl;
+    G[ta] = Ga;
+    G[tb] = Gb;
+    const float GC = __shfl_sync(0xffffffffu, incl, 31);
+    const float ba = ta < n ? __ldg(beta + (size_t)(t0 + ta) * n_v + h) : 0.0f;
+    const float bb = tb < n ? __ldg(beta + (size_t)(t0 + tb) * n_v + h) : 0.0f;
+    const float ga = expf(Ga), gb = expf(Gb);
+    bt[ta] = ba;
+    bt[tb] = bb;
+    bg[ta] = ba * ga;
+    bg[tb] = bb * gb;
+    *reinterpret_cast<float2*>(gG + ta) = make_float2(ga, gb);
+    *reinterpret_cast<float2*>(gG + kCh + ta) = make_float2(expf(GC - Ga), expf(GC - Gb));
+  }
+  __syncthreads();
   {
-    // K K^T and Q K^T, 4 x 4 tiles: rows t = 4ty.., columns s = 4tx..
-    const int ty = tid >> 4, tx = tid & 15;
-    float ga[4][4], qa[4][4];
+    // 2. warps 0-3: K K^T -> A, warps 4-7: Q K^T -> P; warp row tile mt,
+    // column tiles 0 .. 2mt+1 (the rest lies above the diagonal)
+    const int pq = warp >> 2, mt = warp & 3, ntn = 2 * mt + 2;
+    const uint16_t* L = pq ? Qb : Kb;
+    float acc[8][4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
+    const int ra = 16 * mt + gq;
+#pragma unroll 2
+    for (int kb = 0; kb < kDK / 16; ++kb) {
+      const int j = 16 * kb + 2 * cq;
+      uint32_t af[4];
+      af[0] = *reinterpret_cast<const uint32_t*>(L + ra * kLdH + j);
+      af[1] = *reinterpret_cast<const uint32_t*>(L + (ra + 8) * kLdH + j);
+      af[2] = *reinterpret_cast<const uint32_t*>(L + ra * kLdH + j + 8);
+      af[3] = *reinterpret_cast<const uint32_t*>(L + (ra + 8) * kLdH + j + 8);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) ga[a][b] = qa[a][b] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < kDK; ++j) {
-      const float4 kt = *reinterpret_cast<const float4*>(KT + j * kCh + 4 * ty);
-      const float4 ks = *reinterpret_cast<const float4*>(KT + j * kCh + 4 * tx);
-      const float4 qt = *reinterpret_cast<const float4*>(QT + j * kCh + 4 * ty);
-      const float kr[4] = {kt.x, kt.y, kt.z, kt.w}, kc[4] = {ks.x, ks.y, ks.z, ks.w};
-      const float qr[4] = {qt.x, qt.y, qt.z, qt.w};
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          ga[a][b] = __fmaf_rn(kr[a], kc[b], ga[a][b]);
-          qa[a][b] = __fmaf_rn(qr[a], kc[b], qa[a][b]);
+      for (int u = 0; u < 8; ++u)
+        if (u < ntn) {
+          const uint16_t* kr = Kb + (8 * u + gq) * kLdH + j;
+          mma_bf16(acc[u], af, *reinterpret_cast<const uint32_t*>(kr),
+                   *reinterpret_cast<const uint32_t*>(kr + 8));
         }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int t = 4 * ty + a;
-      float pr[4];
+    for (int u = 0; u < 8; ++u)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int s = 4 * tx + b;
-        const float ratio = g[t] / g[s];
-        A[t * kCh + s] = s < t ? bt[t] * ratio * ga[a][b] : 0.0f;
-        pr[b] = s <= t ? ratio * qa[a][b] : 0.0f;
+      for (int e = 0; e < 4; e += 2) {
+        const int t = ra + 8 * (e >> 1), s = 8 * u + 2 * cq;
+        float2 val = make_float2(0.0f, 0.0f);
+        if (u < ntn) {
+          const float r0 = s <= t ? expf(G[t] - G[s]) : 0.0f;
+          const float r1 = s + 1 <= t ? expf(G[t] - G[s + 1]) : 0.0f;
+          if (pq)
+            val = make_float2(r0 * acc[u][e], r1 * acc[u][e + 1]);
+          else
+            val = make_float2(s < t ? bt[t] * r0 * acc[u][e] : 0.0f,
+                              s + 1 < t ? bt[t] * r1 * acc[u][e + 1] : 0.0f);
+        }
+        if (pq)
+          *reinterpret_cast<float2*>(gP + (size_t)t * kCh + s) = val;
+        else if (u < ntn)
+          *reinterpret_cast<float2*>(As + t * kLdA + s) = val;
       }
-      *reinterpret_cast<float4*>(gP + (size_t)t * kCh + 4 * tx) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-    }
   }
-  if (tid < kCh) gG[tid] = g[tid];
   __syncthreads();
-  // W1 = (I + A)^-1 diag(beta) V, W2 = (I + A)^-1 diag(beta g) K: thread
-  // `col` owns one column and substitutes forward, row after row
-  const int col = tid;
-  const bool is_w1 = col < dv;
-  const bool is_w2 = col >= 128 && col - 128 < kDK;
-  if (is_w1 || is_w2) {
-    for (int t = 0; t < kCh; ++t) {
-      // four interleaved partial sums keep the dependent chain short
-      float x0 = is_w1 ? bt[t] * V[t * kDK + col] : bt[t] * g[t] * KT[(col - 128) * kCh + t];
-      float x1 = 0.0f, x2 = 0.0f, x3 = 0.0f;
-      int s = 0;
-      for (; s + 4 <= t; s += 4) {
-        x0 = __fmaf_rn(-A[t * kCh + s], W[s * 256 + col], x0);
-        x1 = __fmaf_rn(-A[t * kCh + s + 1], W[(s + 1) * 256 + col], x1);
-        x2 = __fmaf_rn(-A[t * kCh + s + 2], W[(s + 2) * 256 + col], x2);
-        x3 = __fmaf_rn(-A[t * kCh + s + 3], W[(s + 3) * 256 + col], x3);
+  // 3. diagonal blocks of T: thread (b, cc) solves column cc of block b;
+  // entries above the diagonal come out as 0
+  if (tid < 64) {
+    const int b = tid >> 4, cc = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float* ar = As + (16 * b + r) * kLdA + 16 * b;
+      float a0 = r == cc ? 1.0f : 0.0f, a1 = 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < r; ++s2) {
+        if (s2 & 1)
+          a1 = __fmaf_rn(-ar[s2], x[s2], a1);
+        else
+          a0 = __fmaf_rn(-ar[s2], x[s2], a0);
       }
-      for (; s < t; ++s) x0 = __fmaf_rn(-A[t * kCh + s], W[s * 256 + col], x0);
-      const float x = (x0 + x1) + (x2 + x3);
-      W[t * 256 + col] = x;
-      if (is_w1)
-        gW1[(size_t)t * dv + col] = x;
-      else
-        gW2[(size_t)t * kDK + (col - 128)] = x;
+      x[r] = a0 + a1;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdT + 16 * b + cc] = x[r];
+  }
+  __syncthreads();
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;
+    // X_ij = sum_{k=j}^{i-1} A_ik T_kj for the blocks (i, j = i - d)
+    for (int e = tid; e < nb * 256; e += kThr) {
+      const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
+      float a0 = 0.0f, a1 = 0.0f;
+      for (int kk = j; kk < i; ++kk) {
+        const float* ar = As + (16 * i + r) * kLdA + 16 * kk;
+        const float* tc = Ts + (16 * kk) * kLdT + 16 * j + cc;
+#pragma unroll
+        for (int s2 = 0; s2 < 16; s2 += 2) {
+          a0 = __fmaf_rn(ar[s2], tc[s2 * kLdT], a0);
+          a1 = __fmaf_rn(ar[s2 + 1], tc[(s2 + 1) * kLdT], a1);
+        }
+      }
+      Xs[e] = a0 + a1;
+    }
+    __syncthreads();
+    // T_ij = -T_ii X_ij (T_ii lower triangular)
+    for (int e = tid; e < nb * 256; e += kThr) {
+      const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
+      const float* tr = Ts + (16 * i + r) * kLdT + 16 * i;
+      const float* xc = Xs + (j << 8) + cc;
+      float a0 = 0.0f, a1 = 0.0f;
+      for (int s2 = 0; s2 <= r; ++s2) {
+        if (s2 & 1)
+          a1 = __fmaf_rn(tr[s2], xc[s2 * 16], a1);
+        else
+          a0 = __fmaf_rn(tr[s2], xc[s2 * 16], a0);
+      }
+      Ts[(16 * i + r) * kLdT + 16 * j + cc] = -(a0 + a1);
+    }
+    __syncthreads();
+  }
+  {
+    // 4. warps 0-3: W1 (right factor V, column scale beta), warps 4-7: W2
+    // (right factor K, column scale beta g); each warp takes half of the
+    // column tiles and row tiles {0, 3} or {1, 2} (the same number of
+    // k-steps, T being lower triangular)
+    const int pw = warp >> 2, nh = (warp >> 1) & 1, mp = warp & 1;
+    const int ntot = pw ? kDK / 8 : dv / 8, nhalf = ntot / 2, nbase = nh * nhalf;
+    const uint16_t* R = pw ? Kb : Vb;
+    const float* sc = pw ? bg : bt;
+    float* dst = pw ? gW2 : gW1;
+    const int ld = pw ? kDK : dv;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const int mt = pass == 0 ? mp : 3 - mp;
+      const int ra = 16 * mt + gq;
+      float acc[8][4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
+#pragma unroll 1
+      for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
+        const int s0 = 8 * kb + cq;
+        const float c0 = sc[s0], c1 = sc[s0 + 4];
+        uint32_t hi[4], lo[4];
+        split_tf32(Ts[ra * kLdT + s0] * c0, hi[0], lo[0]);
+        split_tf32(Ts[(ra + 8) * kLdT + s0] * c0, hi[1], lo[1]);
+        split_tf32(Ts[ra * kLdT + s0 + 4] * c1, hi[2], lo[2]);
+        split_tf32(Ts[(ra + 8) * kLdT + s0 + 4] * c1, hi[3], lo[3]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (u < nhalf) {
+            const int col = 8 * (nbase + u) + gq;
+            const uint32_t b0 = (uint32_t)R[s0 * kLdH + col] << 16;
+            const uint32_t b1 = (uint32_t)R[(s0 + 4) * kLdH + col] << 16;
+            mma_tf32(acc[u], hi, b0, b1);
+            mma_tf32(acc[u], lo, b0, b1);
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (u < nhalf)
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int t = ra + 8 * (e >> 1), col = 8 * (nbase + u) + 2 * cq;
+            *reinterpret_cast<float2*>(dst + (size_t)t * ld + col) =
+                make_float2(acc[u][e], acc[u][e + 1]);
+          }
     }
   }
 }
@@ -202,7 +371,7 @@ __global__ void __launch_bounds__(kThr, 1)
   float* W1r = P + kCh * kLdP;           // [C][R]
   float* U = W1r + kCh * R;              // [C][R]
   float* Ug = U + kCh * R;               // [C][R]: U[t][i] * g_C / g_t
-  float* g = Ug + kCh * R;               // [C]
+  float* g = Ug + kCh * R;               // [C] g_t, then [C] g_C / g_t
   const int tid = threadIdx.x;
   const int h = blockIdx.x, hk = h / (n_v / n_k);
   const int r0 = R * blockIdx.y;
@@ -246,7 +415,7 @@ __global__ void __launch_bounds__(kThr, 1)
       const int t = idx / R, i = idx % R;
       W1r[idx] = __ldcg(gW1 + (size_t)t * dv + r0 + i);
     }
-    if (tid < kCh) g[tid] = __ldcg(gG + tid);
+    if (tid < 2 * kCh) g[tid] = __ldcg(gG + tid);
     for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
       const int t = idx / (kDK / 8), ch = idx % (kDK / 8);
       float kf[8] = {0, 0, 0, 0, 0, 0, 0, 0}, qf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -281,7 +450,7 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int e = 0; e < OI; ++e) {
       const float uu = W1r[ot * R + oi + e] - u[e];
       U[ot * R + oi + e] = uu;
-      Ug[ot * R + oi + e] = uu * (gC / g[ot]);
+      Ug[ot * R + oi + e] = uu * g[kCh + ot];
     }
     __syncthreads();
     // O[t][i] = g_t QS[t][i] + sum_{s <= t} P[t][s] U[s][i]
@@ -332,6 +501,202 @@ __global__ void __launch_bounds__(kThr, 1)
     *reinterpret_cast<float4*>(dst + e) = make_float4(sr[e], sr[e + 1], sr[e + 2], sr[e + 3]);
 }
 
+// The same scan with its four products per chunk on the tensor cores
+// (mma.sync m16n8k8, tf32 inputs, fp32 accumulation): U = W1 - W2 S0^T and
+// Q S0^T share the state fragments; O = g Q S0^T + P U; S = g_C S0 +
+// Ug^T K. Operands that carry fp32 values (W2, S, P, U, Ug) are split into
+// tf32 hi + lo and multiplied as hi*hi + hi*lo + lo*hi; q and k are bf16,
+// exact in tf32. 32 state rows of one value head per CTA, 8 warps.
+__global__ void __launch_bounds__(kThr, 1)
+    gdn_chunk_scan_tc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                             const float* __restrict__ ws, const float* s_in, float* s_out,
+                             uint16_t* __restrict__ o, int T, int n_k, int n_v, int dv) {
+  constexpr int R = 32;
+  extern __shared__ float sm[];
+  float* ST = sm;                        // [dk][kTcLdS]: ST[j][i] = S[r0 + i][j]
+  float* W2 = ST + kDK * kTcLdS;         // [C][kTcLd]
+  float* Qs = W2 + kCh * kTcLd;          // [C][kTcLd]
+  float* Kf = Qs + kCh * kTcLd;          // [C][kTcLdK]
+  float* P = Kf + kCh * kTcLdK;          // [C][kTcLdP]
+  float* W1r = P + kCh * kTcLdP;         // [C][kTcLdU]
+  float* U = W1r + kCh * kTcLdU;         // [C][kTcLdU]
+  float* Ug = U + kCh * kTcLdU;          // [C][kTcLdU]: U[t][i] * g_C / g_t
+  float* g = Ug + kCh * kTcLdU;          // [C] g_t, then [C] g_C / g_t
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, cq = lane & 3;
+  const int h = blockIdx.x, hk = h / (n_v / n_k);
+  const int r0 = R * blockIdx.y;
+  for (int idx = tid; idx < R * kDK / 4; idx += kThr) {
+    const int i = idx % R, j = (idx / R) * 4;
+    const float4 v = *reinterpret_cast<const float4*>(s_in + ((size_t)h * dv + r0 + i) * kDK + j);
+    ST[(j + 0) * kTcLdS + i] = v.x;
+    ST[(j + 1) * kTcLdS + i] = v.y;
+    ST[(j + 2) * kTcLdS + i] = v.z;
+    ST[(j + 3) * kTcLdS + i] = v.w;
+  }
+  // U / QS / O tiles: rows 16*mt.., columns 8*nt0.. and 8*(nt0+1)..
+  const int mt = warp & 3, nt0 = 2 * (warp >> 2);
+  // state tiles: rows 16*ms.., columns 8*ns0 .. 8*ns0 + 31
+  const int ms = warp & 1, ns0 = 4 * (warp >> 1);
+  const int n_chunks = (T + kCh - 1) / kCh;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int t0 = c * kCh, n = min(kCh, T - t0);
+    const float* blk = ws + ((size_t)c * n_v + h) * blk_floats(dv);
+    const float* gW1 = blk;
+    const float* gW2 = gW1 + (size_t)kCh * dv;
+    const float* gP = gW2 + (size_t)kCh * kDK;
+    const float* gG = gP + (size_t)kCh * kCh;
+    __syncthreads();  // the previous chunk's reads are done, its state is in ST
+    for (int idx = tid; idx < kCh * kDK / 4; idx += kThr) {
+      const int t = idx / (kDK / 4), j = (idx % (kDK / 4)) * 4;
+      *reinterpret_cast<float4*>(W2 + t * kTcLd + j) =
+          __ldcg(reinterpret_cast<const float4*>(gW2 + (size_t)t * kDK + j));
+    }
+    for (int idx = tid; idx < kCh * kCh / 4; idx += kThr) {
+      const int t = idx / (kCh / 4), sc = (idx % (kCh / 4)) * 4;
+      *reinterpret_cast<float4*>(P + t * kTcLdP + sc) =
+          __ldcg(reinterpret_cast<const float4*>(gP + (size_t)t * kCh + sc));
+    }
+    for (int idx = tid; idx < kCh * R; idx += kThr) {
+      const int t = idx / R, i = idx % R;
+      W1r[t * kTcLdU + i] = __ldcg(gW1 + (size_t)t * dv + r0 + i);
+    }
+    if (tid < 2 * kCh) g[tid] = __ldcg(gG + tid);
+    for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
+      const int t = idx / (kDK / 8), ch = idx % (kDK / 8);
+      float kf[8] = {0, 0, 0, 0, 0, 0, 0, 0}, qf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (t < n) {
+        const size_t src = ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8;
+        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(k + src)), kf);
+        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(q + src)), qf);
+      }
+      float4* qd = reinterpret_cast<float4*>(Qs + t * kTcLd + ch * 8);
+      qd[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
+      qd[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
+      float4* kd = reinterpret_cast<float4*>(Kf + t * kTcLdK + ch * 8);
+      kd[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
+      kd[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
+    }
+    __syncthreads();
+    // (1) W2 S0^T and (2) Q S0^T over j = 0..127
+    float au[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, aq[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll 2
+    for (int kb = 0; kb < kDK / 8; ++kb) {
+      const int j = 8 * kb + cq;
+      const int ra = 16 * mt + gq;
+      uint32_t wh[4], wl[4], qa[4];
+      split_tf32(W2[ra * kTcLd + j], wh[0], wl[0]);
+      split_tf32(W2[(ra + 8) * kTcLd + j], wh[1], wl[1]);
+      split_tf32(W2[ra * kTcLd + j + 4], wh[2], wl[2]);
+      split_tf32(W2[(ra + 8) * kTcLd + j + 4], wh[3], wl[3]);
+      qa[0] = __float_as_uint(Qs[ra * kTcLd + j]);
+      qa[1] = __float_as_uint(Qs[(ra + 8) * kTcLd + j]);
+      qa[2] = __float_as_uint(Qs[ra * kTcLd + j + 4]);
+      qa[3] = __float_as_uint(Qs[(ra + 8) * kTcLd + j + 4]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col = 8 * (nt0 + u) + gq;
+        uint32_t sh0, sl0, sh1, sl1;
+        split_tf32(ST[j * kTcLdS + col], sh0, sl0);
+        split_tf32(ST[(j + 4) * kTcLdS + col], sh1, sl1);
+        mma_tf32(au[u], wh, sh0, sh1);
+        mma_tf32(au[u], wh, sl0, sl1);
+        mma_tf32(au[u], wl, sh0, sh1);
+        mma_tf32(aq[u], qa, sh0, sh1);
+        mma_tf32(aq[u], qa, sl0, sl1);
+      }
+    }
+    const float gC = g[kCh - 1];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int t = 16 * mt + gq + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
+        const float2 w = *reinterpret_cast<const float2*>(W1r + t * kTcLdU + i);
+        const float2 uu = make_float2(w.x - au[u][e], w.y - au[u][e + 1]);
+        const float r = g[kCh + t];
+        *reinterpret_cast<float2*>(U + t * kTcLdU + i) = uu;
+        *reinterpret_cast<float2*>(Ug + t * kTcLdU + i) = make_float2(uu.x * r, uu.y * r);
+      }
+    __syncthreads();
+    // (3) O = g Q S0^T + P U; P is zero above the diagonal
+    float ao[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
+      const int sc = 8 * kb + cq;
+      const int ra = 16 * mt + gq;
+      uint32_t ph[4], pl[4];
+      split_tf32(P[ra * kTcLdP + sc], ph[0], pl[0]);
+      split_tf32(P[(ra + 8) * kTcLdP + sc], ph[1], pl[1]);
+      split_tf32(P[ra * kTcLdP + sc + 4], ph[2], pl[2]);
+      split_tf32(P[(ra + 8) * kTcLdP + sc + 4], ph[3], pl[3]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col = 8 * (nt0 + u) + gq;
+        uint32_t uh0, ul0, uh1, ul1;
+        split_tf32(U[sc * kTcLdU + col], uh0, ul0);
+        split_tf32(U[(sc + 4) * kTcLdU + col], uh1, ul1);
+        mma_tf32(ao[u], ph, uh0, uh1);
+        mma_tf32(ao[u], ph, ul0, ul1);
+        mma_tf32(ao[u], pl, uh0, uh1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; e += 2) {
+        const int t = 16 * mt + gq + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
+        if (t < n) {
+          const float o0 = g[t] * aq[u][e] + ao[u][e];
+          const float o1 = g[t] * aq[u][e + 1] + ao[u][e + 1];
+          *reinterpret_cast<uint32_t*>(o + ((size_t)(t0 + t) * n_v + h) * dv + r0 + i) =
+              pack_bf2(o0, o1);
+        }
+      }
+    // (4) S = g_C S0 + Ug^T K: rows i (M), columns j (N), over t (K)
+    float as[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * ms + gq + 8 * (e >> 1), j = 8 * (ns0 + u) + 2 * cq + (e & 1);
+        as[u][e] = gC * ST[j * kTcLdS + i];
+      }
+#pragma unroll 2
+    for (int kb = 0; kb < kCh / 8; ++kb) {
+      const int t = 8 * kb + cq;
+      const int ia = 16 * ms + gq;
+      uint32_t uh[4], ul[4];
+      split_tf32(Ug[t * kTcLdU + ia], uh[0], ul[0]);
+      split_tf32(Ug[t * kTcLdU + ia + 8], uh[1], ul[1]);
+      split_tf32(Ug[(t + 4) * kTcLdU + ia], uh[2], ul[2]);
+      split_tf32(Ug[(t + 4) * kTcLdU + ia + 8], uh[3], ul[3]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int col = 8 * (ns0 + u) + gq;
+        const uint32_t k0 = __float_as_uint(Kf[t * kTcLdK + col]);
+        const uint32_t k1 = __float_as_uint(Kf[(t + 4) * kTcLdK + col]);
+        mma_tf32(as[u], uh, k0, k1);
+        mma_tf32(as[u], ul, k0, k1);
+      }
+    }
+    __syncthreads();  // every read of the old state is done
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 16 * ms + gq + 8 * (e >> 1), j = 8 * (ns0 + u) + 2 * cq + (e & 1);
+        ST[j * kTcLdS + i] = as[u][e];
+      }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < R * kDK / 4; idx += kThr) {
+    const int i = idx % R, j = (idx / R) * 4;
+    *reinterpret_cast<float4*>(s_out + ((size_t)h * dv + r0 + i) * kDK + j) =
+        make_float4(ST[(j + 0) * kTcLdS + i], ST[(j + 1) * kTcLdS + i], ST[(j + 2) * kTcLdS + i],
+                    ST[(j + 3) * kTcLdS + i]);
+  }
+}
+
 size_t gdn_chunk_ws_bytes(const moe_gdn_shape_t* s) {
   const size_t n_chunks = ((size_t)s->T + kCh - 1) / kCh;
   return n_chunks * (size_t)s->n_v * blk_floats(s->dv) * sizeof(float);
@@ -342,8 +707,8 @@ cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, cons
                                const float* s_in, float* s_out, uint16_t* o, float* ws,
                                cudaStream_t stream) {
   static bool attr_set = false;
-  constexpr int prep_smem = kPrepSmemFloats * 4;
-  constexpr int scan16 = scan_smem_floats<16>() * 4, scan32 = scan_smem_floats<32>() * 4;
+  constexpr int prep_smem = kPrepSmemBytes;
+  constexpr int scan16 = scan_smem_floats<16>() * 4, scan_tc = kTcSmemFloats * 4;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gdn_chunk_prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
@@ -351,8 +716,8 @@ cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, cons
     e = cudaFuncSetAttribute(gdn_chunk_scan_kernel<16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, scan16);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gdn_chunk_scan_kernel<32>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, scan32);
+    e = cudaFuncSetAttribute(gdn_chunk_scan_tc_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, scan_tc);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -361,9 +726,10 @@ cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, cons
       q, k, v, alpha, beta, s->T, s->n_k, s->n_v, s->dv, ws);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // 32 state rows per CTA when dv allows (fewer CTAs re-reading each chunk's tiles)
+  // the tensor-core scan (32 state rows per CTA) when dv allows, else the
+  // CUDA-core one with 16 rows
   if (s->dv % 32 == 0)
-    gdn_chunk_scan_kernel<32><<<dim3(s->n_v, s->dv / 32), kThr, scan32, stream>>>(
+    gdn_chunk_scan_tc_kernel<<<dim3(s->n_v, s->dv / 32), kThr, scan_tc, stream>>>(
         q, k, ws, s_in, s_out, o, s->T, s->n_k, s->n_v, s->dv);
   else
     gdn_chunk_scan_kernel<16><<<dim3(s->n_v, s->dv / 16), kThr, scan16, stream>>>(

@@ -390,11 +390,14 @@ moe_status_t moe_gdn_scan(const moe_gdn_shape_t* shape, const void* q_dev, const
  * right-hand sides depend only on the chunk's k, v, alpha and beta), so the
  * work inside a chunk runs in parallel over its tokens and only the chunks
  * follow one another. Same inputs, outputs and supported shapes as
- * moe_gdn_scan (dv <= 128 as well), results within fp32 rounding of it;
- * fp32 arithmetic. ws_dev: device workspace of at least
- * moe_gdn_chunked_workspace_bytes(shape) bytes, 16-byte aligned, caller
- * owned (per chunk and value head the chunk's two solved right-hand sides,
- * its decay-masked q.k matrix and its decays). Errors: as moe_gdn_scan, plus
+ * moe_gdn_scan (dv <= 128 as well), results within the layer's tolerance
+ * of it (fp32 sums; the products run on the tensor cores, bf16 operands
+ * exact, fp32 operands split into two tf32 parts; decay ratios taken as
+ * exp of differences of summed log alpha). ws_dev: device workspace of at
+ * least moe_gdn_chunked_workspace_bytes(shape) bytes, 16-byte aligned,
+ * caller owned (per chunk and value head the chunk's two solved right-hand
+ * sides, its decay-masked q.k matrix and two decay vectors; the contents
+ * need no initialisation). Errors: as moe_gdn_scan, plus
  * MOE_ERR_WORKSPACE when ws_bytes is too small. */
 size_t moe_gdn_chunked_workspace_bytes(const moe_gdn_shape_t* shape);
 moe_status_t moe_gdn_chunked_scan(const moe_gdn_shape_t* shape, const void* q_dev,

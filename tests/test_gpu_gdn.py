@@ -101,6 +101,23 @@ def test_gdn_chunked_against_the_oracle(T, n_k, n_v, dv):
     close(s_end, s_ref, "state")
 
 
+@pytest.mark.parametrize("lo,hi", [(0.05, 0.5), (0.0, 0.02)])
+def test_gdn_chunked_fast_decay(lo, hi):
+    """Heads that forget fast: alpha in [lo, hi) drives the running product
+    of a 64-token chunk far below the smallest fp32 number (and alpha = 0
+    occurs), where the chunk's gate ratios still have to come out right."""
+    T, n_k, n_v, dv = 160, 16, 32, 128
+    q, k, v, _, beta, s0 = synth.gen_gdn(T, n_k, n_v, 128, dv, seed=21)
+    alpha = np.random.default_rng(22).uniform(lo, hi, (T, n_v)).astype(np.float32)
+    alpha[::7, ::3] = np.float32(lo)
+    inp = (q, k, v, alpha, beta, s0)
+    o, s_end = run_chunked(T, n_k, n_v, 128, dv, inp)
+    o_ref, s_ref = oracle.gdn_scan(*inp)
+    assert np.isfinite(f64(o)).all() and np.isfinite(s_end).all()
+    close(f64(o), f64(o_ref), "o")
+    close(s_end, s_ref, "state")
+
+
 def test_gdn_chunked_equals_the_recurrent_kernel_and_carries_state():
     """Both device forms give the same outputs and state within the layer's
     tolerance; the chunked form's state carries across calls (two calls of
