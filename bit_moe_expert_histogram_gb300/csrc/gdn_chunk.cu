@@ -105,11 +105,11 @@ constexpr int kLdP = kCh + 1;
 // load of the MMAs touches 32 distinct banks
 constexpr int kTcLdS = 40;    // ST [dk][40]
 constexpr int kTcLd = 132;    // W2, Q [C][132] (A operands)
-constexpr int kTcLdK = 136;   // K [C][136] (B operand)
 constexpr int kTcLdP = 68;    // P [C][68]
 constexpr int kTcLdU = 40;    // W1 rows, U, Ug [C][40]
-constexpr int kTcSmemFloats =
-    kDK * kTcLdS + 2 * kCh * kTcLd + kCh * kTcLdK + kCh * kTcLdP + 3 * kCh * kTcLdU + 2 * kCh;
+// one stage: W2, P, W1 rows, g and g_C / g in fp32, Q and K in bf16
+constexpr int kTcStageFloats = kCh * kTcLd + kCh * kTcLdP + kCh * kTcLdU + 2 * kCh + kCh * kLdH;
+constexpr int kTcSmemFloats = kDK * kTcLdS + kCh * kTcLdU + 2 * kTcStageFloats;
 template <int R>
 constexpr int scan_smem_floats() {
   return kDK * (R + 1) + 2 * kCh * kLd + kCh * kDK + kCh * kLdP + 3 * kCh * R + 2 * kCh;
@@ -501,12 +501,85 @@ __global__ void __launch_bounds__(kThr, 1)
     *reinterpret_cast<float4*>(dst + e) = make_float4(sr[e], sr[e + 1], sr[e + 2], sr[e + 3]);
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// One chunk's tiles for the tensor-core scan, in shared memory
+struct ScanStage {
+  float* W2;     // [C][kTcLd]
+  float* P;      // [C][kTcLdP]
+  float* W1r;    // [C][kTcLdU]: W1 columns r0 .. r0+31
+  float* g;      // [C] g_t, then [C] g_C / g_t
+  uint16_t* Qb;  // [C][kLdH] bf16
+  uint16_t* Kb;  // [C][kLdH] bf16
+};
+__device__ __forceinline__ ScanStage scan_stage(float* base) {
+  ScanStage st;
+  st.W2 = base;
+  st.P = st.W2 + kCh * kTcLd;
+  st.W1r = st.P + kCh * kTcLdP;
+  st.g = st.W1r + kCh * kTcLdU;
+  st.Qb = reinterpret_cast<uint16_t*>(st.g + 2 * kCh);
+  st.Kb = st.Qb + kCh * kLdH;
+  return st;
+}
+
+// every thread issues its share of chunk c's copies (one commit group)
+__device__ __forceinline__ void scan_issue(const ScanStage& st, const uint16_t* __restrict__ q,
+                                           const uint16_t* __restrict__ k,
+                                           const float* __restrict__ ws, int c, int T, int n_k,
+                                           int n_v, int dv, int h, int hk, int r0, int tid) {
+  const int t0 = c * kCh, n = min(kCh, T - t0);
+  const float* blk = ws + ((size_t)c * n_v + h) * blk_floats(dv);
+  const float* gW1 = blk;
+  const float* gW2 = gW1 + (size_t)kCh * dv;
+  const float* gP = gW2 + (size_t)kCh * kDK;
+  const float* gG = gP + (size_t)kCh * kCh;
+#pragma unroll
+  for (int m = 0; m < kCh * kDK / 4 / kThr; ++m) {
+    const int idx = tid + m * kThr, t = idx >> 5, j = (idx & 31) * 4;
+    cp_async16(st.W2 + t * kTcLd + j, gW2 + (size_t)t * kDK + j, 16);
+  }
+#pragma unroll
+  for (int m = 0; m < kCh * kCh / 4 / kThr; ++m) {
+    const int idx = tid + m * kThr, t = idx >> 4, sc = (idx & 15) * 4;
+    cp_async16(st.P + t * kTcLdP + sc, gP + (size_t)t * kCh + sc, 16);
+  }
+#pragma unroll
+  for (int m = 0; m < kCh * 32 / 4 / kThr; ++m) {
+    const int idx = tid + m * kThr, t = idx >> 3, i = (idx & 7) * 4;
+    cp_async16(st.W1r + t * kTcLdU + i, gW1 + (size_t)t * dv + r0 + i, 16);
+  }
+  if (tid < 2 * kCh / 4) cp_async16(st.g + 4 * tid, gG + 4 * tid, 16);
+#pragma unroll
+  for (int m = 0; m < kCh * (kDK / 8) / kThr; ++m) {
+    const int idx = tid + m * kThr, t = idx >> 4, ch = idx & 15;
+    // tokens past the end read as zeros (from a valid address)
+    const size_t src = t < n ? ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8 : 0;
+    const int bytes = t < n ? 16 : 0;
+    cp_async16(st.Qb + t * kLdH + ch * 8, q + src, bytes);
+    cp_async16(st.Kb + t * kLdH + ch * 8, k + src, bytes);
+  }
+  cp_async_commit();
+}
+
 // The same scan with its four products per chunk on the tensor cores
 // (mma.sync m16n8k8, tf32 inputs, fp32 accumulation): U = W1 - W2 S0^T and
 // Q S0^T share the state fragments; O = g Q S0^T + P U; S = g_C S0 +
-// Ug^T K. Operands that carry fp32 values (W2, S, P, U, Ug) are split into
-// tf32 hi + lo and multiplied as hi*hi + hi*lo + lo*hi; q and k are bf16,
-// exact in tf32. 32 state rows of one value head per CTA, 8 warps.
+// (diag(g_C / g) U)^T K. Operands that carry fp32 values (W2, S, P, U) are
+// split into tf32 hi + lo and multiplied as hi*hi + hi*lo + lo*hi; q and k
+// are bf16, exact in tf32. 32 state rows of one value head per CTA, 8 warps;
+// the next chunk's tiles are copied in (cp.async, two stages) while the
+// current one is computed.
 __global__ void __launch_bounds__(kThr, 1)
     gdn_chunk_scan_tc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                              const float* __restrict__ ws, const float* s_in, float* s_out,
@@ -514,18 +587,14 @@ __global__ void __launch_bounds__(kThr, 1)
   constexpr int R = 32;
   extern __shared__ float sm[];
   float* ST = sm;                        // [dk][kTcLdS]: ST[j][i] = S[r0 + i][j]
-  float* W2 = ST + kDK * kTcLdS;         // [C][kTcLd]
-  float* Qs = W2 + kCh * kTcLd;          // [C][kTcLd]
-  float* Kf = Qs + kCh * kTcLd;          // [C][kTcLdK]
-  float* P = Kf + kCh * kTcLdK;          // [C][kTcLdP]
-  float* W1r = P + kCh * kTcLdP;         // [C][kTcLdU]
-  float* U = W1r + kCh * kTcLdU;         // [C][kTcLdU]
-  float* Ug = U + kCh * kTcLdU;          // [C][kTcLdU]: U[t][i] * g_C / g_t
-  float* g = Ug + kCh * kTcLdU;          // [C] g_t, then [C] g_C / g_t
+  float* U = ST + kDK * kTcLdS;          // [C][kTcLdU]
+  float* const stage0 = U + kCh * kTcLdU;  // two stages of kTcStageFloats
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, cq = lane & 3;
   const int h = blockIdx.x, hk = h / (n_v / n_k);
   const int r0 = R * blockIdx.y;
+  const int n_chunks = (T + kCh - 1) / kCh;
+  scan_issue(scan_stage(stage0), q, k, ws, 0, T, n_k, n_v, dv, h, hk, r0, tid);
   for (int idx = tid; idx < R * kDK / 4; idx += kThr) {
     const int i = idx % R, j = (idx / R) * 4;
     const float4 v = *reinterpret_cast<const float4*>(s_in + ((size_t)h * dv + r0 + i) * kDK + j);
@@ -538,61 +607,39 @@ __global__ void __launch_bounds__(kThr, 1)
   const int mt = warp & 3, nt0 = 2 * (warp >> 2);
   // state tiles: rows 16*ms.., columns 8*ns0 .. 8*ns0 + 31
   const int ms = warp & 1, ns0 = 4 * (warp >> 1);
-  const int n_chunks = (T + kCh - 1) / kCh;
   for (int c = 0; c < n_chunks; ++c) {
+    const ScanStage sg = scan_stage(stage0 + (c & 1) * kTcStageFloats);
     const int t0 = c * kCh, n = min(kCh, T - t0);
-    const float* blk = ws + ((size_t)c * n_v + h) * blk_floats(dv);
-    const float* gW1 = blk;
-    const float* gW2 = gW1 + (size_t)kCh * dv;
-    const float* gP = gW2 + (size_t)kCh * kDK;
-    const float* gG = gP + (size_t)kCh * kCh;
-    __syncthreads();  // the previous chunk's reads are done, its state is in ST
-    for (int idx = tid; idx < kCh * kDK / 4; idx += kThr) {
-      const int t = idx / (kDK / 4), j = (idx % (kDK / 4)) * 4;
-      *reinterpret_cast<float4*>(W2 + t * kTcLd + j) =
-          __ldcg(reinterpret_cast<const float4*>(gW2 + (size_t)t * kDK + j));
+    // the other stage was last read by chunk c-1, before the barrier that
+    // ended it (or never): refill it with chunk c+1, then wait for chunk c
+    if (c + 1 < n_chunks) {
+      scan_issue(scan_stage(stage0 + ((c + 1) & 1) * kTcStageFloats), q, k, ws, c + 1, T, n_k,
+                 n_v, dv, h, hk, r0, tid);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    for (int idx = tid; idx < kCh * kCh / 4; idx += kThr) {
-      const int t = idx / (kCh / 4), sc = (idx % (kCh / 4)) * 4;
-      *reinterpret_cast<float4*>(P + t * kTcLdP + sc) =
-          __ldcg(reinterpret_cast<const float4*>(gP + (size_t)t * kCh + sc));
-    }
-    for (int idx = tid; idx < kCh * R; idx += kThr) {
-      const int t = idx / R, i = idx % R;
-      W1r[t * kTcLdU + i] = __ldcg(gW1 + (size_t)t * dv + r0 + i);
-    }
-    if (tid < 2 * kCh) g[tid] = __ldcg(gG + tid);
-    for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
-      const int t = idx / (kDK / 8), ch = idx % (kDK / 8);
-      float kf[8] = {0, 0, 0, 0, 0, 0, 0, 0}, qf[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (t < n) {
-        const size_t src = ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8;
-        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(k + src)), kf);
-        bf8_to_f(__ldg(reinterpret_cast<const uint4*>(q + src)), qf);
-      }
-      float4* qd = reinterpret_cast<float4*>(Qs + t * kTcLd + ch * 8);
-      qd[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
-      qd[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
-      float4* kd = reinterpret_cast<float4*>(Kf + t * kTcLdK + ch * 8);
-      kd[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
-      kd[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
-    }
-    __syncthreads();
+    __syncthreads();  // chunk c's tiles and the state are in place
+    const float* W2 = sg.W2;
+    const float* P = sg.P;
+    const float* g = sg.g;
+    const uint16_t* Qb = sg.Qb;
+    const uint16_t* Kb = sg.Kb;
     // (1) W2 S0^T and (2) Q S0^T over j = 0..127
     float au[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, aq[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    const int ra = 16 * mt + gq;
 #pragma unroll 2
     for (int kb = 0; kb < kDK / 8; ++kb) {
       const int j = 8 * kb + cq;
-      const int ra = 16 * mt + gq;
       uint32_t wh[4], wl[4], qa[4];
       split_tf32(W2[ra * kTcLd + j], wh[0], wl[0]);
       split_tf32(W2[(ra + 8) * kTcLd + j], wh[1], wl[1]);
       split_tf32(W2[ra * kTcLd + j + 4], wh[2], wl[2]);
       split_tf32(W2[(ra + 8) * kTcLd + j + 4], wh[3], wl[3]);
-      qa[0] = __float_as_uint(Qs[ra * kTcLd + j]);
-      qa[1] = __float_as_uint(Qs[(ra + 8) * kTcLd + j]);
-      qa[2] = __float_as_uint(Qs[ra * kTcLd + j + 4]);
-      qa[3] = __float_as_uint(Qs[(ra + 8) * kTcLd + j + 4]);
+      qa[0] = (uint32_t)Qb[ra * kLdH + j] << 16;
+      qa[1] = (uint32_t)Qb[(ra + 8) * kLdH + j] << 16;
+      qa[2] = (uint32_t)Qb[ra * kLdH + j + 4] << 16;
+      qa[3] = (uint32_t)Qb[(ra + 8) * kLdH + j + 4] << 16;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int col = 8 * (nt0 + u) + gq;
@@ -606,24 +653,20 @@ __global__ void __launch_bounds__(kThr, 1)
         mma_tf32(aq[u], qa, sl0, sl1);
       }
     }
-    const float gC = g[kCh - 1];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
-        const int t = 16 * mt + gq + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
-        const float2 w = *reinterpret_cast<const float2*>(W1r + t * kTcLdU + i);
-        const float2 uu = make_float2(w.x - au[u][e], w.y - au[u][e + 1]);
-        const float r = g[kCh + t];
-        *reinterpret_cast<float2*>(U + t * kTcLdU + i) = uu;
-        *reinterpret_cast<float2*>(Ug + t * kTcLdU + i) = make_float2(uu.x * r, uu.y * r);
+        const int t = ra + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
+        const float2 w = *reinterpret_cast<const float2*>(sg.W1r + t * kTcLdU + i);
+        *reinterpret_cast<float2*>(U + t * kTcLdU + i) =
+            make_float2(w.x - au[u][e], w.y - au[u][e + 1]);
       }
     __syncthreads();
     // (3) O = g Q S0^T + P U; P is zero above the diagonal
     float ao[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
     for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
       const int sc = 8 * kb + cq;
-      const int ra = 16 * mt + gq;
       uint32_t ph[4], pl[4];
       split_tf32(P[ra * kTcLdP + sc], ph[0], pl[0]);
       split_tf32(P[(ra + 8) * kTcLdP + sc], ph[1], pl[1]);
@@ -644,7 +687,7 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
-        const int t = 16 * mt + gq + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
+        const int t = ra + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
         if (t < n) {
           const float o0 = g[t] * aq[u][e] + ao[u][e];
           const float o1 = g[t] * aq[u][e + 1] + ao[u][e + 1];
@@ -652,7 +695,8 @@ __global__ void __launch_bounds__(kThr, 1)
               pack_bf2(o0, o1);
         }
       }
-    // (4) S = g_C S0 + Ug^T K: rows i (M), columns j (N), over t (K)
+    // (4) S = g_C S0 + (diag(g_C / g) U)^T K: rows i (M), columns j (N), over t (K)
+    const float gC = g[kCh - 1];
     float as[4][4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -665,21 +709,22 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int kb = 0; kb < kCh / 8; ++kb) {
       const int t = 8 * kb + cq;
       const int ia = 16 * ms + gq;
+      const float r0g = g[kCh + t], r4g = g[kCh + t + 4];
       uint32_t uh[4], ul[4];
-      split_tf32(Ug[t * kTcLdU + ia], uh[0], ul[0]);
-      split_tf32(Ug[t * kTcLdU + ia + 8], uh[1], ul[1]);
-      split_tf32(Ug[(t + 4) * kTcLdU + ia], uh[2], ul[2]);
-      split_tf32(Ug[(t + 4) * kTcLdU + ia + 8], uh[3], ul[3]);
+      split_tf32(U[t * kTcLdU + ia] * r0g, uh[0], ul[0]);
+      split_tf32(U[t * kTcLdU + ia + 8] * r0g, uh[1], ul[1]);
+      split_tf32(U[(t + 4) * kTcLdU + ia] * r4g, uh[2], ul[2]);
+      split_tf32(U[(t + 4) * kTcLdU + ia + 8] * r4g, uh[3], ul[3]);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int col = 8 * (ns0 + u) + gq;
-        const uint32_t k0 = __float_as_uint(Kf[t * kTcLdK + col]);
-        const uint32_t k1 = __float_as_uint(Kf[(t + 4) * kTcLdK + col]);
+        const uint32_t k0 = (uint32_t)Kb[t * kLdH + col] << 16;
+        const uint32_t k1 = (uint32_t)Kb[(t + 4) * kLdH + col] << 16;
         mma_tf32(as[u], uh, k0, k1);
         mma_tf32(as[u], ul, k0, k1);
       }
     }
-    __syncthreads();  // every read of the old state is done
+    __syncthreads();  // every read of the old state and of this stage is done
 #pragma unroll
     for (int u = 0; u < 4; ++u)
 #pragma unroll
