@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(1024)
                    const float* __restrict__ w, int H, int K, int R, int n_shared,
                    uint16_t* __restrict__ y, uint16_t* __restrict__ x_next, const uint16_t* h_in,
                    uint16_t* h_out, const uint16_t* __restrict__ gain) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   float acc[8];
 #pragma unroll
@@ -105,6 +107,8 @@ __global__ void __launch_bounds__(1024) block_input_kernel(
     const uint16_t* __restrict__ h_in, const int32_t* __restrict__ tok,
     const uint16_t* __restrict__ embed, int vocab, const uint16_t* __restrict__ gain, int H,
     uint16_t* __restrict__ h0_out, uint16_t* __restrict__ x, Ctrl* ctrl) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x, c = threadIdx.x;
   uint4 v = make_uint4(0u, 0u, 0u, 0u);
   if (tok) {
@@ -142,8 +146,8 @@ __global__ void __launch_bounds__(1024) block_input_kernel(
 cudaError_t launch_block_input(const uint16_t* h_in, const int32_t* tok, const uint16_t* embed,
                                int vocab, const uint16_t* gain, int T, int H, uint16_t* h0_out,
                                uint16_t* x, Ctrl* ctrl, cudaStream_t stream) {
-  block_input_kernel<<<T, H / 8, 0, stream>>>(h_in, tok, embed, vocab, gain, H, h0_out, x, ctrl);
-  return cudaGetLastError();
+  return launch_pdl(block_input_kernel, dim3(T), dim3(H / 8), 0, stream, h_in, tok, embed, vocab,
+                    gain, H, h0_out, x, ctrl);
 }
 
 cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, const float* w, int T,
@@ -151,9 +155,8 @@ cudaError_t launch_combine(const uint16_t* y_slots, const int32_t* row_pos, cons
                            cudaStream_t stream, const uint16_t* h_in, uint16_t* h_out,
                            const uint16_t* gain) {
   const int threads = H / 8;  // H % 256 == 0 -> a whole number of warps, <= 1024 by validation
-  combine_kernel<<<T, threads, 0, stream>>>(y_slots, row_pos, w, H, K, T * K, n_shared, y,
-                                            x_next, h_in, h_out, gain);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(threads), 0, stream, y_slots, row_pos, w, H, K,
+                    T * K, n_shared, y, x_next, h_in, h_out, gain);
 }
 
 // Debug: dequantise a packed [N][Kd] matrix with the GEMMs' routine.

@@ -125,6 +125,29 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The MoE layer's kernels (router, plan, gather, grouped GEMMs, combine)
+// set up what reads no global memory (barriers, TMEM, tensor-map
+// prefetch), call pdl_wait(), then pdl_trigger(): with the trigger after
+// the wait, when a kernel starts every kernel two or more launches before it
+// on the stream has completed, so only the immediate predecessor's outputs
+// need the wait.
+// Launches kern on stream with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Asks L2 to fetch [p, p + bytes) (16-byte aligned, bytes % 16 == 0); no
 // data reaches the thread, so the copy can never be stale.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {

@@ -494,25 +494,6 @@ bool decode_supported(int T, int H, int E, int K, int I, int ns) {
 
 size_t decode_part_floats(int T, int H) { return (size_t)T * ((H + kDownRows - 1) / kDownRows); }
 
-namespace {
-// Launch with programmatic stream serialisation (the kernel may start while
-// its predecessor in the stream is still running; it waits in pdl_wait).
-cudaError_t launch_pdl(void (*kernel)(DecodeArgs), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, const DecodeArgs& a) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
-}
-}  // namespace
-
 cudaError_t launch_decode_layer(const DecodeArgs& a, cudaStream_t stream) {
   const int T = a.T, slots = a.K + a.ns;
   cudaError_t err = launch_pdl(dec_route_kernel, dim3((T * a.E + 3) / 4), dim3(128), 0, stream, a);

@@ -254,6 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // everything above reads no global memory
+  pdl_trigger();
 
   const int units = min(*a.num_blocks * a.mtiles, a.max_units);
   const int wstages = (a.kdim + kKW - 1) / kKW;  // W stages per unit (the last may be half)
@@ -658,8 +660,8 @@ static cudaError_t launch_one(const CUtensorMap& tw, const CUtensorMap& twsh, co
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  ffn_w4_kernel<GATED><<<grid, kThreads, kSmemBytes, stream>>>(tw, twsh, tb, a);
-  return cudaGetLastError();
+  return launch_pdl(ffn_w4_kernel<GATED>, dim3(grid), dim3(kThreads), kSmemBytes, stream, tw, twsh,
+                    tb, a);
 }
 
 cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
@@ -682,6 +684,8 @@ __global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__
                                                        const int32_t* __restrict__ sorted_rows,
                                                        int K, int R, int S, int T, int hv,
                                                        uint4* __restrict__ xs, Ctrl* ctrl) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = (size_t)S * hv;
   for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
     const int p = (int)(i / hv), c = (int)(i - (size_t)p * hv);
@@ -700,10 +704,9 @@ cudaError_t launch_gather_x(const uint16_t* x, const int32_t* sorted_rows, int K
   const size_t n = (size_t)S * (H / 8);
   const size_t want = (n + 255) / 256;
   const int grid = (int)(want < (size_t)nsm * 8 ? want : (size_t)nsm * 8);
-  gather_x_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(
-      reinterpret_cast<const uint4*>(x), sorted_rows, K, R, S, T, H / 8, reinterpret_cast<uint4*>(xs),
-      ctrl);
-  return cudaGetLastError();
+  return launch_pdl(gather_x_kernel, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream,
+                    reinterpret_cast<const uint4*>(x), sorted_rows, K, R, S, T, H / 8,
+                    reinterpret_cast<uint4*>(xs), ctrl);
 }
 
 int ffn_tile_m() { return kTileM; }

@@ -147,6 +147,8 @@ __global__ void __launch_bounds__(kThr, 2)
   const int gq = lane >> 2, cq = lane & 3;
   const int c = blockIdx.x, h = blockIdx.y, hk = h / (n_v / n_k);
   const int t0 = c * kCh, n = min(kCh, T - t0);
+  pdl_wait();
+  pdl_trigger();
   // tokens past the sequence end read as k = q = v = 0, alpha = 1, beta = 0:
   // they leave every quantity below unchanged
   const uint4 z4 = make_uint4(0, 0, 0, 0);
@@ -375,6 +377,8 @@ __global__ void __launch_bounds__(kThr, 1)
   const int tid = threadIdx.x;
   const int h = blockIdx.x, hk = h / (n_v / n_k);
   const int r0 = R * blockIdx.y;
+  pdl_wait();  // the workspace comes from the prep kernel
+  pdl_trigger();
   // this thread's state entries for the update: row si, columns sj..sj+SJ-1
   const int si = tid / (kDK / SJ), sj = (tid % (kDK / SJ)) * SJ;
   float sr[SJ];
@@ -594,6 +598,8 @@ __global__ void __launch_bounds__(kThr, 1)
   const int h = blockIdx.x, hk = h / (n_v / n_k);
   const int r0 = R * blockIdx.y;
   const int n_chunks = (T + kCh - 1) / kCh;
+  pdl_wait();  // the workspace comes from the prep kernel
+  pdl_trigger();
   scan_issue(scan_stage(stage0), q, k, ws, 0, T, n_k, n_v, dv, h, hk, r0, tid);
   for (int idx = tid; idx < R * kDK / 4; idx += kThr) {
     const int i = idx % R, j = (idx / R) * 4;
@@ -767,19 +773,18 @@ cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, cons
     attr_set = true;
   }
   const int n_chunks = (s->T + kCh - 1) / kCh;
-  gdn_chunk_prep_kernel<<<dim3(n_chunks, s->n_v), kThr, prep_smem, stream>>>(
-      q, k, v, alpha, beta, s->T, s->n_k, s->n_v, s->dv, ws);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(gdn_chunk_prep_kernel, dim3(n_chunks, s->n_v), dim3(kThr),
+                             (size_t)prep_smem, stream, q, k, v, alpha, beta, s->T, s->n_k, s->n_v,
+                             s->dv, ws);
   if (e != cudaSuccess) return e;
   // the tensor-core scan (32 state rows per CTA) when dv allows, else the
   // CUDA-core one with 16 rows
   if (s->dv % 32 == 0)
-    gdn_chunk_scan_tc_kernel<<<dim3(s->n_v, s->dv / 32), kThr, scan_tc, stream>>>(
-        q, k, ws, s_in, s_out, o, s->T, s->n_k, s->n_v, s->dv);
-  else
-    gdn_chunk_scan_kernel<16><<<dim3(s->n_v, s->dv / 16), kThr, scan16, stream>>>(
-        q, k, ws, s_in, s_out, o, s->T, s->n_k, s->n_v, s->dv);
-  return cudaGetLastError();
+    return launch_pdl(gdn_chunk_scan_tc_kernel, dim3(s->n_v, s->dv / 32), dim3(kThr),
+                      (size_t)scan_tc, stream, q, k, (const float*)ws, s_in, s_out, o, s->T, s->n_k,
+                      s->n_v, s->dv);
+  return launch_pdl(gdn_chunk_scan_kernel<16>, dim3(s->n_v, s->dv / 16), dim3(kThr), (size_t)scan16,
+                    stream, q, k, (const float*)ws, s_in, s_out, o, s->T, s->n_k, s->n_v, s->dv);
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* 
                                                                  int R, int E, int chunk,
                                                                  int32_t* __restrict__ hist,
                                                                  Ctrl* ctrl) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int h[kMaxE];
   for (int e = threadIdx.x; e < E; e += kPlanThreads) h[e] = 0;
   __syncthreads();
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     plan_scatter_kernel(const int32_t* __restrict__ ids, int T, int K, int E, int n_shared,
                         int BM, const int32_t* __restrict__ hist, int nchunks, int chunk,
                         moe_plan_t plan) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int base[kMaxE];                 // this block's next position per expert
   __shared__ int wcnt[kPlanWarps][kMaxE];     // per-round, per-warp counts -> prefixes
   __shared__ int warp_sums[32];
@@ -199,12 +203,11 @@ cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, i
                         cudaStream_t stream) {
   const int R = T * K;
   const int nchunks = (R + chunk - 1) / chunk;
-  plan_hist_kernel<<<nchunks, kPlanThreads, 0, stream>>>(ids, R, E, chunk, hist, ctrl);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(plan_hist_kernel, dim3(nchunks), dim3(kPlanThreads), 0, stream, ids,
+                               R, E, chunk, hist, ctrl);
   if (err != cudaSuccess) return err;
-  plan_scatter_kernel<<<nchunks, kPlanThreads, 0, stream>>>(ids, T, K, E, n_shared, BM, hist,
-                                                           nchunks, chunk, plan);
-  return cudaGetLastError();
+  return launch_pdl(plan_scatter_kernel, dim3(nchunks), dim3(kPlanThreads), 0, stream, ids, T, K,
+                    E, n_shared, BM, hist, nchunks, chunk, plan);
 }
 
 }  // namespace moe

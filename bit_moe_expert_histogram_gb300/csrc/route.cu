@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(128) route_logits_kernel(const uint16_t* __res
                                                            const float* __restrict__ bias, int T,
                                                            int H, int E,
                                                            float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * PT;
   const int e0 = (blockIdx.y * 4 + warp) * PE;
@@ -94,6 +96,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32) route_topk_kernel(const float
                                                                     int T, int E, int K,
                                                                     int32_t* __restrict__ ids,
                                                                     float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ TopkWarpSmem<1024> S[kTopkWarps];
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -104,18 +108,16 @@ __global__ void __launch_bounds__(kTopkWarps * 32) route_topk_kernel(const float
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
                          int E, int K, float* logits, int32_t* ids, float* w,
                          cudaStream_t stream) {
-  if (T >= 8) {
-    dim3 grid((T + 7) / 8, (E + 31) / 32);
-    route_logits_kernel<8, 8><<<grid, 128, 0, stream>>>(x, wr, bias, T, H, E, logits);
-  } else {
-    dim3 grid(T, (E + 7) / 8);
-    route_logits_kernel<1, 2><<<grid, 128, 0, stream>>>(x, wr, bias, T, H, E, logits);
-  }
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err;
+  if (T >= 8)
+    err = launch_pdl(route_logits_kernel<8, 8>, dim3((T + 7) / 8, (E + 31) / 32), dim3(128), 0,
+                     stream, x, wr, bias, T, H, E, logits);
+  else
+    err = launch_pdl(route_logits_kernel<1, 2>, dim3(T, (E + 7) / 8), dim3(128), 0, stream, x, wr,
+                     bias, T, H, E, logits);
   if (err != cudaSuccess) return err;
-  route_topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(
-      logits, T, E, K, ids, w);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel, dim3((T + kTopkWarps - 1) / kTopkWarps),
+                    dim3(kTopkWarps * 32), 0, stream, logits, T, E, K, ids, w);
 }
 
 }  // namespace moe

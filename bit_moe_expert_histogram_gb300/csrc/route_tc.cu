@@ -8,7 +8,8 @@
 // experts must still be those of the fixed-order fp32 logits, so:
 //   route_mma_kernel    A[t][e] = sum over one 256-wide K slice (TMA tiles of
 //                       128 experts x 128 tokens, fp32 partials per slice) and
-//                       the slice's sum of w^2 per expert
+//                       the slice's sum of w^2 per expert (the diagonal of
+//                       W W^T, on the tensor cores too: only a bound uses it)
 //   route_screen_kernel per token: A = the slices' sum + bias; with
 //                       d_e = 2^-10 * ||x_t|| * ||w_e|| (at least 20 times any
 //                       accumulation error of either order: both are below
@@ -29,10 +30,12 @@ namespace {
 
 constexpr int kRtTile = 128;            // experts (MMA M) and tokens (MMA N) per tile
 constexpr int kRtKB = 4;                // 64-element K blocks per CTA (a 256-wide slice)
+constexpr int kRtThreads = 256;
 constexpr int kRtBlock = kRtTile * 128; // bytes of one 128-row x 64-element bf16 tile
 constexpr int kRtSmem = 2 * kRtKB * kRtBlock + 1024 + 64;
-constexpr int kScreenWarps = 8;
+constexpr int kScreenWarps = 4;        // tokens per screen block (one warp each)
 constexpr int kScreenMaxE = 256;        // 8 experts per lane in the screen
+constexpr int kScreenMaxJ = 8;          // H / 256 at most (the row in registers; K slices)
 
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -55,9 +58,11 @@ __device__ __forceinline__ void tmem_ld16r(uint32_t taddr, uint32_t (&v)[16]) {
 
 }  // namespace
 
-// Grid (token tiles, expert tiles, K slices); 128 threads. P[s][t][e] fp32,
-// Wn[s][e] = sum of w^2 over slice s (written by the first token tile).
-__global__ void __launch_bounds__(128, 1)
+// Grid (token tiles, expert tiles, K slices); 256 threads. P[s][t][e] fp32,
+// Wn[s][e] = sum of w^2 over slice s (by the first token tile: the diagonal
+// of W W^T, 16 more MMAs with the expert tile as both operands, into TMEM
+// columns 128..255).
+__global__ void __launch_bounds__(kRtThreads, 1)
     route_mma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                      int T, int E, float* __restrict__ P, float* __restrict__ Wn, Ctrl* ctrl) {
   extern __shared__ uint8_t smem_raw[];
@@ -70,20 +75,24 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kRtTile, e0 = blockIdx.y * kRtTile, s = blockIdx.z;
   const int k0 = s * kRtKB * 64;
+  const bool norms = blockIdx.x == 0;
   if (threadIdx.x == 0) {
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kRtTile);
+    tmem_alloc(smem_u32(tmem_slot), 2 * kRtTile);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // everything above reads no global memory
+  pdl_trigger();
   volatile int never = 0;
+  bool ok = true;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_x);
@@ -94,10 +103,7 @@ __global__ void __launch_bounds__(128, 1)
       tma_load_2d(sA + kb * kRtBlock, &tm_w, k0 + kb * 64, e0, bar_tma, pol);
       tma_load_2d(sB + kb * kRtBlock, &tm_x, k0 + kb * 64, t0, bar_tma, pol);
     }
-  }
-  // every thread waits for the tiles (the norms below read them); bounded
-  bool ok = mbar_wait(bar_tma, 0, &never);
-  if (threadIdx.x == 0) {
+    ok = mbar_wait(bar_tma, 0, &never);  // bounded
     if (ok) {
       tc_fence_after();
       const uint32_t idesc = idesc_bf16(kRtTile, kRtTile);
@@ -107,42 +113,33 @@ __global__ void __launch_bounds__(128, 1)
         for (int kk = 0; kk < 4; ++kk)
           mma_bf16_ss(tmem, smem_desc_sw128(sA + kb * kRtBlock + kk * 32),
                       smem_desc_sw128(sB + kb * kRtBlock + kk * 32), idesc, (kb | kk) != 0);
+      if (norms) {
+#pragma unroll
+        for (int kb = 0; kb < kRtKB; ++kb)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + kRtTile, smem_desc_sw128(sA + kb * kRtBlock + kk * 32),
+                        smem_desc_sw128(sA + kb * kRtBlock + kk * 32), idesc, (kb | kk) != 0);
+      }
       mma_commit(bar_mma);
     } else {
       set_error(ctrl, MOE_ERR_TIMEOUT, KID_ROUTE, 1);
     }
   }
-  // slice norms of the experts' rows: row r of a tile is 128 contiguous bytes
-  // (the swizzle only permutes its 16-byte chunks)
-  if (ok && blockIdx.x == 0 && e0 + (int)threadIdx.x < E) {
-    const int r = threadIdx.x;
-    float ss = 0.0f;
-#pragma unroll
-    for (int kb = 0; kb < kRtKB; ++kb) {
-      const uint8_t* row = gbase + kb * kRtBlock + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * c);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          ss = __fmaf_rn(bf_lo(u[i]), bf_lo(u[i]), ss);
-          ss = __fmaf_rn(bf_hi(u[i]), bf_hi(u[i]), ss);
-        }
-      }
-    }
-    Wn[(size_t)s * E + e0 + r] = ss;
-  }
   ok = __syncthreads_and(ok);
   if (ok && mbar_wait(bar_mma, 0, &never)) {
     tc_fence_after();
-    const int e = e0 + warp * 32 + lane;
-    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    // warps q and q + 4 read TMEM lane quarter q (experts), half the columns each
+    const int q = warp & 3, half = warp >> 2;
+    const int e = e0 + q * 32 + lane;
+    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
     float* out = P + (size_t)s * T * E;
+    const int c_begin = half * (kRtTile / 2), c_end = c_begin + kRtTile / 2;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kRtTile; c0 += 16) {
-      uint32_t v[16];
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+      uint32_t v[16], u[16];
       tmem_ld16r(taddr + c0, v);
+      tmem_ld16r(taddr + c0 + 16, u);
       tmem_wait_ld();
       if (e < E) {
 #pragma unroll
@@ -150,7 +147,26 @@ __global__ void __launch_bounds__(128, 1)
           const int t = t0 + c0 + i;
           if (t < T) out[(size_t)t * E + e] = __uint_as_float(v[i]);
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = t0 + c0 + 16 + i;
+          if (t < T) out[(size_t)t * E + e] = __uint_as_float(u[i]);
+        }
       }
+    }
+    if (norms && half == 0) {
+      // expert e's own column of W W^T: column 32q + lane of TMEM lane 32q + lane
+      uint32_t v[16], u[16];
+      tmem_ld16r(taddr + kRtTile + q * 32, v);
+      tmem_ld16r(taddr + kRtTile + q * 32 + 16, u);
+      tmem_wait_ld();
+      uint32_t d = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        d = lane == i ? v[i] : d;
+        d = lane == 16 + i ? u[i] : d;
+      }
+      if (e < E) Wn[(size_t)s * E + e] = __uint_as_float(d);
     }
   } else if (threadIdx.x == 0) {
     set_error(ctrl, MOE_ERR_TIMEOUT, KID_ROUTE, 2);
@@ -159,163 +175,202 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kRtTile);
+    tmem_dealloc(tmem, 2 * kRtTile);
   }
 }
 
-// Four warps per token (two tokens per block). Warp 0 of a token's group
-// forms the candidate set, the group's four warps compute the candidates'
-// fixed-order logits, and warp 0 selects the top K. See the file comment.
-constexpr int kScreenGroup = 4;                               // warps per token
-constexpr int kScreenTokens = kScreenWarps / kScreenGroup;    // tokens per block
-
-__device__ __forceinline__ void group_sync(int group) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kScreenGroup * 32) : "memory");
-}
-
+// One warp per token, kScreenWarps tokens per block, no barrier after the
+// expert norms: the warp forms the candidate set, computes the candidates'
+// fixed-order logits four at a time (four independent chains per lane) and
+// selects the top K among them. See the file comment.
 __global__ void __launch_bounds__(kScreenWarps * 32)
     route_screen_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                         const float* __restrict__ bias, const float* __restrict__ P,
                         const float* __restrict__ Wn, int T, int H, int E, int K, int S,
                         int32_t* __restrict__ ids, float* __restrict__ w) {
   __shared__ float wn[kScreenMaxE];
-  __shared__ float cval[kScreenTokens][kScreenMaxE];
-  __shared__ int cid[kScreenTokens][kScreenMaxE];
-  __shared__ unsigned long long ckey[kScreenTokens][kScreenMaxE];
-  __shared__ unsigned long long csel[kScreenTokens][32];
-  __shared__ int ncand[kScreenTokens];
+  __shared__ float cval[kScreenWarps][kScreenMaxE];
+  __shared__ int cid[kScreenWarps][kScreenMaxE];
+  __shared__ unsigned long long ckey[kScreenWarps][kScreenMaxE];
+  __shared__ unsigned long long csel[kScreenWarps][32];
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kScreenWarps + g;
+  const bool active = t < T;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(active ? t : 0) * H);
+  const int nj = H >> 8;  // at most kScreenMaxJ
+  constexpr int NL = kScreenMaxE / 32;
+  // the token's row stays in registers (lane chunk 32j + lane); it comes
+  // from before the router's first kernel, so it is read before the wait
+  uint4 xv[kScreenMaxJ];
+#pragma unroll
+  for (int j = 0; j < kScreenMaxJ; ++j)
+    xv[j] = active && j < nj ? __ldg(xr + 32 * j + lane) : make_uint4(0, 0, 0, 0);
+  pdl_wait();
+  pdl_trigger();
+  // the expert norms' slices (whole block) and this token's partial sums
+  // (experts lane + 32i): every load in flight at once
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float v[kScreenMaxJ];
+#pragma unroll
+    for (int s = 0; s < kScreenMaxJ; ++s) v[s] = s < S ? __ldcg(Wn + (size_t)s * E + e) : 0.0f;
     float a = 0.0f;
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) a += __ldcg(Wn + (size_t)s * E + e);
+#pragma unroll
+    for (int s = 0; s < kScreenMaxJ; ++s) a += v[s];
     wn[e] = sqrtf(a);
   }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = warp / kScreenGroup, gw = warp % kScreenGroup;
-  const int t = blockIdx.x * kScreenTokens + g;
-  if (t >= T) return;  // the whole group leaves together
-  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-  const int nj = H >> 8;
-  if (gw == 0) {
-    float xx = 0.0f;
-#pragma unroll 8
-    for (int j = 0; j < nj; ++j) {
-      const uint4 v = __ldg(xr + 32 * j + lane);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float pa[kScreenMaxJ][NL];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xx = __fmaf_rn(bf_lo(u[i]), bf_lo(u[i]), xx);
-        xx = __fmaf_rn(bf_hi(u[i]), bf_hi(u[i]), xx);
-      }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) xx += __shfl_xor_sync(0xFFFFFFFFu, xx, d);
-    const float xnorm = sqrtf(xx);
-    // approximate logits with their bounds, experts lane + 32i
-    constexpr int NL = kScreenMaxE / 32;
-    float lo[NL], hi[NL], a[NL];
-#pragma unroll
-    for (int i = 0; i < NL; ++i) a[i] = 0.0f;
-    // the loads of one slice for all eight experts are independent
-#pragma unroll 4
-    for (int s = 0; s < S; ++s) {
-      const float* ps = P + ((size_t)s * T + t) * E;
-#pragma unroll
-      for (int i = 0; i < NL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) a[i] += __ldcg(ps + e);
-      }
-    }
+  for (int s = 0; s < kScreenMaxJ; ++s) {
+    const float* ps = P + ((size_t)s * T + (active ? t : 0)) * E;
 #pragma unroll
     for (int i = 0; i < NL; ++i) {
       const int e = lane + 32 * i;
-      lo[i] = -INFINITY;
-      hi[i] = -INFINITY;
-      if (e < E) {
-        const float v = bias ? a[i] + bias[e] : a[i];
-        const float d = 0.0009765625f * xnorm * wn[e] + 1e-30f;
-        lo[i] = v - d;
-        hi[i] = v + d;
+      pa[s][i] = (active && s < S && e < E) ? __ldcg(ps + e) : 0.0f;
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+  float a[NL];
+#pragma unroll
+  for (int i = 0; i < NL; ++i) {
+    a[i] = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kScreenMaxJ; ++s) a[i] += pa[s][i];
+  }
+  float xx0 = 0.0f, xx1 = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kScreenMaxJ; ++j) {
+    const uint32_t u[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      xx0 = __fmaf_rn(bf_lo(u[i]), bf_lo(u[i]), xx0);
+      xx1 = __fmaf_rn(bf_hi(u[i]), bf_hi(u[i]), xx1);
+    }
+  }
+  float xx = xx0 + xx1;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) xx += __shfl_xor_sync(0xFFFFFFFFu, xx, d);
+  const float xnorm = sqrtf(xx);
+  // approximate logits with their bounds
+  float lo[NL], hi[NL];
+#pragma unroll
+  for (int i = 0; i < NL; ++i) {
+    const int e = lane + 32 * i;
+    lo[i] = -INFINITY;
+    hi[i] = -INFINITY;
+    if (e < E) {
+      const float v = bias ? a[i] + bias[e] : a[i];
+      const float d = 0.0009765625f * xnorm * wn[e] + 1e-30f;
+      lo[i] = v - d;
+      hi[i] = v + d;
+    }
+  }
+  // theta = the K-th largest lower bound: the K-th largest lane maximum is
+  // at most theta, and only values at or above it can be theta
+  float lmax = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NL; ++i) lmax = fmaxf(lmax, lo[i]);
+  int r = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r += __shfl_sync(0xFFFFFFFFu, lmax, j) > lmax;
+  const uint32_t tkey = __reduce_min_sync(0xFFFFFFFFu, r < K ? topk_key(lmax) : 0xFFFFFFFFu);
+  const float theta0 = topk_value(tkey);  // <= theta
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NL; ++i) cnt += lo[i] >= theta0;
+  int pre = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
+    if (lane >= d) pre += v;
+  }
+  const int n0 = __shfl_sync(0xFFFFFFFFu, pre, 31);
+  int pos = pre - cnt;
+#pragma unroll
+  for (int i = 0; i < NL; ++i)
+    if (lo[i] >= theta0) cval[g][pos++] = lo[i];
+  __syncwarp();
+  // theta = the smallest of these values with fewer than K of them above it
+  float th = INFINITY;
+  for (int i = lane; i < n0; i += 32) {
+    const float v = cval[g][i];
+    int above = 0;
+    for (int j = 0; j < n0; ++j) above += cval[g][j] > v;
+    if (above < K) th = fminf(th, v);
+  }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) th = fminf(th, __shfl_xor_sync(0xFFFFFFFFu, th, d));
+  // candidates: upper bound at least theta
+  cnt = 0;
+#pragma unroll
+  for (int i = 0; i < NL; ++i) cnt += hi[i] >= th;
+  pre = cnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
+    if (lane >= d) pre += v;
+  }
+  const int nc = __shfl_sync(0xFFFFFFFFu, pre, 31);
+  pos = pre - cnt;
+#pragma unroll
+  for (int i = 0; i < NL; ++i)
+    if (hi[i] >= th) cid[g][pos++] = lane + 32 * i;
+  __syncwarp();
+  // the candidates' rows into L1 at once (lane l: 128-byte line l of each
+  // 4 KB row), so the rounds below wait for one round trip, not one each
+  for (int c = 0; c < nc; ++c) {
+    const char* row = reinterpret_cast<const char*>(wr + (size_t)cid[g][c] * H);
+    for (int l = lane; l < (H * 2) / 128; l += 32)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(row + 128 * l));
+  }
+  // fixed-order fp32 logits of the candidates (route_logits_kernel's
+  // order), four candidates at a time; a missing fourth repeats the first
+  for (int c0 = 0; c0 < nc; c0 += 4) {
+    int e4[4];
+    const uint4* wq[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      e4[m] = cid[g][c0 + m < nc ? c0 + m : c0];
+      wq[m] = reinterpret_cast<const uint4*>(wr + (size_t)e4[m] * H);
+    }
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // four chunks of each of the four rows in flight at a time
+#pragma unroll
+    for (int j0 = 0; j0 < kScreenMaxJ; j0 += 4) {
+      uint4 wv[4][4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          wv[jj][m] = j0 + jj < nj ? __ldg(wq[m] + 32 * (j0 + jj) + lane) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (j0 + jj >= nj) break;
+        const uint4 xj = xv[j0 + jj];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint4 wj = wv[jj][m];
+          acc[m] = __fmaf_rn(bf_lo(xj.x), bf_lo(wj.x), acc[m]);
+          acc[m] = __fmaf_rn(bf_hi(xj.x), bf_hi(wj.x), acc[m]);
+          acc[m] = __fmaf_rn(bf_lo(xj.y), bf_lo(wj.y), acc[m]);
+          acc[m] = __fmaf_rn(bf_hi(xj.y), bf_hi(wj.y), acc[m]);
+          acc[m] = __fmaf_rn(bf_lo(xj.z), bf_lo(wj.z), acc[m]);
+          acc[m] = __fmaf_rn(bf_hi(xj.z), bf_hi(wj.z), acc[m]);
+          acc[m] = __fmaf_rn(bf_lo(xj.w), bf_lo(wj.w), acc[m]);
+          acc[m] = __fmaf_rn(bf_hi(xj.w), bf_hi(wj.w), acc[m]);
+        }
       }
     }
-    // theta = the K-th largest lower bound: the K-th largest lane maximum is
-    // at most theta, and only values at or above it can be theta
-    float lmax = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < NL; ++i) lmax = fmaxf(lmax, lo[i]);
-    int r = 0;
+    for (int m = 0; m < 4; ++m) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) r += __shfl_sync(0xFFFFFFFFu, lmax, j) > lmax;
-    const uint32_t tkey = __reduce_min_sync(0xFFFFFFFFu, r < K ? topk_key(lmax) : 0xFFFFFFFFu);
-    const float theta0 = topk_value(tkey);  // <= theta
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < NL; ++i) cnt += lo[i] >= theta0;
-    int pre = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
-      if (lane >= d) pre += v;
+      for (int d = 16; d >= 1; d >>= 1)
+        acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xFFFFFFFFu, acc[m], d));
+      if (lane == 0 && c0 + m < nc)
+        ckey[g][c0 + m] = topk_ckey(bias ? __fadd_rn(acc[m], bias[e4[m]]) : acc[m], e4[m]);
     }
-    const int n0 = __shfl_sync(0xFFFFFFFFu, pre, 31);
-    int pos = pre - cnt;
-#pragma unroll
-    for (int i = 0; i < NL; ++i)
-      if (lo[i] >= theta0) cval[g][pos++] = lo[i];
-    __syncwarp();
-    // theta = the smallest of these values with fewer than K of them above it
-    float th = INFINITY;
-    for (int i = lane; i < n0; i += 32) {
-      const float v = cval[g][i];
-      int above = 0;
-      for (int j = 0; j < n0; ++j) above += cval[g][j] > v;
-      if (above < K) th = fminf(th, v);
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) th = fminf(th, __shfl_xor_sync(0xFFFFFFFFu, th, d));
-    // candidates: upper bound at least theta
-    cnt = 0;
-#pragma unroll
-    for (int i = 0; i < NL; ++i) cnt += hi[i] >= th;
-    pre = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, pre, d);
-      if (lane >= d) pre += v;
-    }
-    pos = pre - cnt;
-#pragma unroll
-    for (int i = 0; i < NL; ++i)
-      if (hi[i] >= th) cid[g][pos++] = lane + 32 * i;
-    if (lane == 31) ncand[g] = pre;
   }
-  group_sync(g);
-  const int nc = ncand[g];
-  // fixed-order fp32 logits of the candidates (route_logits_kernel's order):
-  // candidate c goes to warp c mod 4 of the group
-  for (int c = gw; c < nc; c += kScreenGroup) {
-    const int e = cid[g][c];
-    const uint4* wq = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
-    float acc = 0.0f;
-#pragma unroll 8
-    for (int j = 0; j < nj; ++j) {
-      const uint4 xv = __ldg(xr + 32 * j + lane), wv = __ldg(wq + 32 * j + lane);
-      acc = __fmaf_rn(bf_lo(xv.x), bf_lo(wv.x), acc);
-      acc = __fmaf_rn(bf_hi(xv.x), bf_hi(wv.x), acc);
-      acc = __fmaf_rn(bf_lo(xv.y), bf_lo(wv.y), acc);
-      acc = __fmaf_rn(bf_hi(xv.y), bf_hi(wv.y), acc);
-      acc = __fmaf_rn(bf_lo(xv.z), bf_lo(wv.z), acc);
-      acc = __fmaf_rn(bf_hi(xv.z), bf_hi(wv.z), acc);
-      acc = __fmaf_rn(bf_lo(xv.w), bf_lo(wv.w), acc);
-      acc = __fmaf_rn(bf_hi(xv.w), bf_hi(wv.w), acc);
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, d));
-    if (lane == 0) ckey[g][c] = topk_ckey(bias ? __fadd_rn(acc, bias[e]) : acc, e);
-  }
-  group_sync(g);
-  if (gw != 0) return;
+  __syncwarp();
   for (int i = lane; i < nc; i += 32) {
     const unsigned long long ci = ckey[g][i];
     int rk = 0;
@@ -337,7 +392,8 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
 }
 
 bool route_tc_supported(int T, int H, int E, int K) {
-  return T >= kRouteTcMinT && E <= kScreenMaxE && K <= 32 && H % (kRtKB * 64) == 0;
+  return T >= kRouteTcMinT && E <= kScreenMaxE && K <= 32 && H % (kRtKB * 64) == 0 &&
+         H / (kRtKB * 64) <= kScreenMaxJ;
 }
 
 size_t route_tc_partial_floats(int T, int H, int E) {
@@ -358,12 +414,12 @@ cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, co
   float* P = part;
   float* Wn = part + (size_t)S * T * E;
   dim3 grid((T + kRtTile - 1) / kRtTile, (E + kRtTile - 1) / kRtTile, S);
-  route_mma_kernel<<<grid, 128, kRtSmem, stream>>>(tm_w, tm_x, T, E, P, Wn, ctrl);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = launch_pdl(route_mma_kernel, grid, dim3(kRtThreads), kRtSmem, stream, tm_w,
+                               tm_x, T, E, P, Wn, ctrl);
   if (err != cudaSuccess) return err;
-  route_screen_kernel<<<(T + kScreenTokens - 1) / kScreenTokens, kScreenWarps * 32, 0, stream>>>(
-      x, wr, bias, P, Wn, T, H, E, K, S, ids, w);
-  return cudaGetLastError();
+  return launch_pdl(route_screen_kernel, dim3((T + kScreenWarps - 1) / kScreenWarps),
+                    dim3(kScreenWarps * 32), 0, stream, x, wr, bias, (const float*)P,
+                    (const float*)Wn, T, H, E, K, S, ids, w);
 }
 
 }  // namespace moe
