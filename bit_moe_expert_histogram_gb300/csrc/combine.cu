@@ -15,6 +15,8 @@
 
 namespace moe {
 
+constexpr int kCombineBatch = 8;
+
 // One block per token; thread c owns the 8 elements [8c, 8c+8).
 __global__ void __launch_bounds__(1024)
     combine_kernel(const uint16_t* __restrict__ y_slots, const int32_t* __restrict__ row_pos,
@@ -28,21 +30,40 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   const int c = threadIdx.x;  // blockDim.x == H/8: one 16-byte chunk per thread
-  for (int k = 0; k < K; ++k) {
-    const int r = row_pos[t * K + k];
-    const float wk = w[t * K + k];
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_slots + (size_t)r * H) + c);
-    acc[0] = __fmaf_rn(wk, bf_lo(v.x), acc[0]);
-    acc[1] = __fmaf_rn(wk, bf_hi(v.x), acc[1]);
-    acc[2] = __fmaf_rn(wk, bf_lo(v.y), acc[2]);
-    acc[3] = __fmaf_rn(wk, bf_hi(v.y), acc[3]);
-    acc[4] = __fmaf_rn(wk, bf_lo(v.z), acc[4]);
-    acc[5] = __fmaf_rn(wk, bf_hi(v.z), acc[5]);
-    acc[6] = __fmaf_rn(wk, bf_lo(v.w), acc[6]);
-    acc[7] = __fmaf_rn(wk, bf_hi(v.w), acc[7]);
+  // the token's slot rows and weights, then its rows in batches of
+  // kCombineBatch with every load of a batch in flight (the sum keeps the
+  // ascending k order)
+  const uint4* ys = reinterpret_cast<const uint4*>(y_slots);
+  const size_t hv = (size_t)H / 8;
+  uint4 vsh = make_uint4(0u, 0u, 0u, 0u);
+  if (n_shared) vsh = __ldg(ys + (size_t)(R + t) * hv + c);
+  for (int k0 = 0; k0 < K; k0 += kCombineBatch) {
+    int r[kCombineBatch];
+    float wk[kCombineBatch];
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) {
+      r[j] = k0 + j < K ? __ldg(row_pos + t * K + k0 + j) : 0;
+      wk[j] = k0 + j < K ? __ldg(w + t * K + k0 + j) : 0.0f;
+    }
+    uint4 v[kCombineBatch];
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j)
+      v[j] = k0 + j < K ? __ldg(ys + (size_t)r[j] * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < kCombineBatch; ++j) {
+      if (k0 + j >= K) break;
+      acc[0] = __fmaf_rn(wk[j], bf_lo(v[j].x), acc[0]);
+      acc[1] = __fmaf_rn(wk[j], bf_hi(v[j].x), acc[1]);
+      acc[2] = __fmaf_rn(wk[j], bf_lo(v[j].y), acc[2]);
+      acc[3] = __fmaf_rn(wk[j], bf_hi(v[j].y), acc[3]);
+      acc[4] = __fmaf_rn(wk[j], bf_lo(v[j].z), acc[4]);
+      acc[5] = __fmaf_rn(wk[j], bf_hi(v[j].z), acc[5]);
+      acc[6] = __fmaf_rn(wk[j], bf_lo(v[j].w), acc[6]);
+      acc[7] = __fmaf_rn(wk[j], bf_hi(v[j].w), acc[7]);
+    }
   }
   if (n_shared) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_slots + (size_t)(R + t) * H) + c);
+    const uint4 v = vsh;
     acc[0] += bf_lo(v.x); acc[1] += bf_hi(v.x);
     acc[2] += bf_lo(v.y); acc[3] += bf_hi(v.y);
     acc[4] += bf_lo(v.z); acc[5] += bf_hi(v.z);

@@ -680,31 +680,45 @@ cudaError_t launch_ffn_down(const CUtensorMap& tw, const CUtensorMap& twsh, cons
 // tiles; each group of 8 elements is stored in the (i, i+4)-paired order of
 // the rebuilt weights. A row index outside [0, T) is recorded and copied as
 // zeros.
-__global__ void __launch_bounds__(256) gather_x_kernel(const uint4* __restrict__ x,
-                                                       const int32_t* __restrict__ sorted_rows,
-                                                       int K, int R, int S, int T, int hv,
-                                                       uint4* __restrict__ xs, Ctrl* ctrl) {
+// One warp per plan row p (grid-stride): the row's source token once, then
+// every 16-byte chunk of the row in flight at once (lane chunks lane + 32m).
+constexpr int kGatherWarps = 8;
+constexpr int kGatherChunks = 8;  // chunks per lane in flight (H <= 2048 in one pass)
+__global__ void __launch_bounds__(kGatherWarps * 32)
+    gather_x_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_rows, int K,
+                    int R, int S, int T, int hv, uint4* __restrict__ xs, Ctrl* ctrl) {
   pdl_wait();
   pdl_trigger();
-  const size_t n = (size_t)S * hv;
-  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
-    const int p = (int)(i / hv), c = (int)(i - (size_t)p * hv);
+  const int lane = threadIdx.x & 31;
+  for (int p = blockIdx.x * kGatherWarps + (threadIdx.x >> 5); p < S;
+       p += gridDim.x * kGatherWarps) {
     const int src = p < R ? __ldg(sorted_rows + p) / K : p - R;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (src >= 0 && src < T)
-      v = to_i4_order(__ldg(x + (size_t)src * hv + c));
-    else if (c == 0)
-      set_error(ctrl, MOE_ERR_BAD_INPUT, KID_FFN, p);
-    xs[i] = v;
+    const bool ok = src >= 0 && src < T;
+    if (!ok && lane == 0) set_error(ctrl, MOE_ERR_BAD_INPUT, KID_FFN, p);
+    const uint4* xr = x + (size_t)(ok ? src : 0) * hv;
+    uint4* dst = xs + (size_t)p * hv;
+    for (int c0 = 0; c0 < hv; c0 += 32 * kGatherChunks) {
+      uint4 v[kGatherChunks];
+#pragma unroll
+      for (int m = 0; m < kGatherChunks; ++m) {
+        const int c = c0 + 32 * m + lane;
+        v[m] = ok && c < hv ? __ldg(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int m = 0; m < kGatherChunks; ++m) {
+        const int c = c0 + 32 * m + lane;
+        if (c < hv) dst[c] = to_i4_order(v[m]);
+      }
+    }
   }
 }
 
 cudaError_t launch_gather_x(const uint16_t* x, const int32_t* sorted_rows, int K, int R, int S,
                             int T, int H, uint16_t* xs, Ctrl* ctrl, int nsm, cudaStream_t stream) {
-  const size_t n = (size_t)S * (H / 8);
-  const size_t want = (n + 255) / 256;
-  const int grid = (int)(want < (size_t)nsm * 8 ? want : (size_t)nsm * 8);
-  return launch_pdl(gather_x_kernel, dim3(grid > 0 ? grid : 1), dim3(256), 0, stream,
+  const int want = (S + kGatherWarps - 1) / kGatherWarps;
+  const int cap = nsm * 16;
+  const int grid = want < cap ? want : cap;
+  return launch_pdl(gather_x_kernel, dim3(grid > 0 ? grid : 1), dim3(kGatherWarps * 32), 0, stream,
                     reinterpret_cast<const uint4*>(x), sorted_rows, K, R, S, T, H / 8,
                     reinterpret_cast<uint4*>(xs), ctrl);
 }

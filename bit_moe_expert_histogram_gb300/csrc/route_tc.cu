@@ -316,15 +316,10 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
   for (int i = 0; i < NL; ++i)
     if (hi[i] >= th) cid[g][pos++] = lane + 32 * i;
   __syncwarp();
-  // the candidates' rows into L1 at once (lane l: 128-byte line l of each
-  // 4 KB row), so the rounds below wait for one round trip, not one each
-  for (int c = 0; c < nc; ++c) {
-    const char* row = reinterpret_cast<const char*>(wr + (size_t)cid[g][c] * H);
-    for (int l = lane; l < (H * 2) / 128; l += 32)
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(row + 128 * l));
-  }
   // fixed-order fp32 logits of the candidates (route_logits_kernel's
-  // order), four candidates at a time; a missing fourth repeats the first
+  // order), four candidates at a time with every chunk of the four rows in
+  // flight at once (one round trip per round); a missing fourth repeats the
+  // first
   for (int c0 = 0; c0 < nc; c0 += 4) {
     int e4[4];
     const uint4* wq[4];
@@ -334,19 +329,17 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
       wq[m] = reinterpret_cast<const uint4*>(wr + (size_t)e4[m] * H);
     }
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    // four chunks of each of the four rows in flight at a time
+    {
+      uint4 wv[kScreenMaxJ][4];
 #pragma unroll
-    for (int j0 = 0; j0 < kScreenMaxJ; j0 += 4) {
-      uint4 wv[4][4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
+      for (int jj = 0; jj < kScreenMaxJ; ++jj)
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-          wv[jj][m] = j0 + jj < nj ? __ldg(wq[m] + 32 * (j0 + jj) + lane) : make_uint4(0, 0, 0, 0);
+          wv[jj][m] = jj < nj ? __ldg(wq[m] + 32 * jj + lane) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        if (j0 + jj >= nj) break;
-        const uint4 xj = xv[j0 + jj];
+      for (int jj = 0; jj < kScreenMaxJ; ++jj) {
+        if (jj >= nj) break;
+        const uint4 xj = xv[jj];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const uint4 wj = wv[jj][m];
