@@ -255,11 +255,12 @@ def moe_gdn_scan(shape, q, k, v, alpha, beta, state_in, state_out, o, stream=Non
 
 
 def alloc_gdn_workspace(shape, device):
-    """Device workspace of the chunked scan (moe_gdn_chunked_workspace_bytes)."""
+    """Device workspace of the chunked scan (moe_gdn_chunked_workspace_bytes),
+    zero-filled: its status header must start at zero."""
     nbytes = load().moe_gdn_chunked_workspace_bytes(C.byref(shape))
     if nbytes == 0:
         raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_gdn_chunked_workspace_bytes")
-    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
 def moe_gdn_chunked_scan(shape, q, k, v, alpha, beta, state_in, state_out, o, ws, stream=None):

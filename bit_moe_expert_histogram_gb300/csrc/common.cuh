@@ -30,7 +30,7 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl must be 256 bytes");
 
-enum : int { KID_PLAN = 1, KID_FFN = 2, KID_DECODE = 3, KID_ROUTE = 4, KID_ATTN = 5 };
+enum : int { KID_PLAN = 1, KID_FFN = 2, KID_DECODE = 3, KID_ROUTE = 4, KID_ATTN = 5, KID_GDN = 6 };
 
 __device__ __forceinline__ void set_error(Ctrl* c, int code, int kid, int detail) {
   if (atomicCAS(&c->err, 0, code) == 0) {
@@ -317,6 +317,26 @@ __device__ __forceinline__ void mma_bf16_ts_acc(uint32_t d_tmem, uint32_t a_tmem
   asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
                "r"(a_tmem), "l"(b_desc), "r"(idesc)
                : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 16 consecutive TMEM columns of this warp's lane quarter, one per register.
+__device__ __forceinline__ void tmem_ld16r(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -81,24 +81,23 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// D += A * B, m16n8k16, bf16 inputs, fp32 accumulators (A row-major: reg 0
-// row g cols 2c, 2c+1; reg 1 row g+8; regs 2, 3 the same 8 columns on; B
-// column-major: reg 0 k = 2c, 2c+1 at n = g, reg 1 k + 8)
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 // prep tiles: bf16 rows of 136 halves (68 words) and fp32 rows of 72 / 68
 // floats put the fragment loads and stores of the MMAs on 32 distinct banks
 constexpr int kLdH = 136;
 constexpr int kLdA = 72;
 constexpr int kLdT = 68;
-constexpr int kPrepSmemBytes = (kCh * kLdA + kCh * kLdT + 3 * 256 + 3 * kCh) * 4 + 3 * kCh * kLdH * 2;
+// tensor-core prep: 128-byte-swizzled bf16 tiles of 128 rows x 64 elements
+// (16 KB atoms); region 0 holds the [K; Q] tile (two atoms) and A, later the
+// three parts of the step-4 left factor; then the V^T / K^T tile (256 rows)
+constexpr int kPrepAtom = 128 * 128;
+constexpr int kPrepKQBytes = 2 * kPrepAtom;
+constexpr int kPrepR0Bytes = 3 * kPrepAtom > kPrepKQBytes + kCh * kLdA * 4
+                                 ? 3 * kPrepAtom
+                                 : ((kPrepKQBytes + kCh * kLdA * 4 + 1023) & ~1023);
+constexpr int kPrepVKBytes = 256 * 128;
+constexpr int kPrepSmemBytes = 1024 + kPrepR0Bytes + kPrepVKBytes +
+                               (kCh * kLdT + 3 * 256 + 3 * kCh) * 4 + 2 * 8 + 16;
+constexpr uint32_t kPrepTmemCols = 256;
 constexpr int kLd = kDK + 1;  // padded row of a [C][dk] tile: rows t and t+1 start in other banks
 constexpr int kLdP = kCh + 1;
 // tensor-core scan tiles (32 state rows): padded so that every fragment
@@ -117,58 +116,138 @@ constexpr int scan_smem_floats() {
 }  // namespace
 
 // grid (n_chunks, n_v): one CTA per (chunk, value head), two CTAs per SM.
-//  1. K, Q, V of the chunk into shared memory as bf16; G_t = sum of log alpha
-//     over the chunk (a warp scan), so every gate ratio g_t / g_s is
-//     exp(G_t - G_s) and never a quotient of two products that underflow
-//  2. K K^T and Q K^T on the tensor cores (mma.sync m16n8k16 bf16, exact
-//     products, fp32 sums), lower triangle only; A and P from them
-//  3. T = (I + A)^-1 by 16 x 16 blocks: the four diagonal blocks by
-//     forward substitution (one thread per column), then the blocks below
-//     them by distance from the diagonal, T_ij = -T_ii sum_k A_ik T_kj
-//  4. W1 = (T diag(beta)) V and W2 = (T diag(beta g)) K on the tensor cores
-//     (mma.sync m16n8k8 tf32): the fp32 left factor is split into tf32
-//     hi + lo, the bf16 right factor is exact in tf32
+//  1. K, Q of the chunk into one 128-byte-swizzled K-major bf16 tile
+//     ([K; Q], 128 rows), V^T and K^T into another (256 rows over the chunk's
+//     64 tokens); G_t = sum of log alpha over the chunk (a warp scan), so
+//     every gate ratio g_t / g_s is exp(G_t - G_s) and never a quotient of
+//     two products that underflow
+//  2. [K; Q] K^T on the tensor cores: one thread issues tcgen05.mma
+//     (M = 128, N = 64, bf16, exact products, fp32 sums in TMEM); rows 0..63
+//     give A, rows 64..127 give P
+//  3. T = (I + A)^-1 by 16 x 16 blocks: the four diagonal blocks by forward
+//     substitution (one thread per column), then the blocks below them by
+//     distance from the diagonal, T_ij = -T_ii sum_k A_ik T_kj
+//  4. [T diag(beta); T diag(beta g)] [V | K] on the tensor cores (M = 128,
+//     N = 256): the fp32 left factor is split into three bf16 parts (24
+//     significant bits) and the three products summed in TMEM; W1 and W2
+//     are the two diagonal blocks of the result
 __global__ void __launch_bounds__(kThr, 2)
     gdn_chunk_prep_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                           const uint16_t* __restrict__ v, const float* __restrict__ alpha,
                           const float* __restrict__ beta, int T, int n_k, int n_v, int dv,
-                          float* __restrict__ ws) {
-  extern __shared__ float sm[];
-  float* As = sm;                                      // [C][kLdA]
-  float* Ts = As + kCh * kLdA;                         // [C][kLdT]
-  float* Xs = Ts + kCh * kLdT;                         // 3 x [16][16] scratch
-  float* G = Xs + 3 * 256;                             // [C] log gates
-  float* bt = G + kCh;                                 // [C] beta
-  float* bg = bt + kCh;                                // [C] beta g
-  uint16_t* Kb = reinterpret_cast<uint16_t*>(bg + kCh);  // [C][kLdH]
-  uint16_t* Qb = Kb + kCh * kLdH;                      // [C][kLdH]
-  uint16_t* Vb = Qb + kCh * kLdH;                      // [C][kLdH]
+                          float* __restrict__ ws, Ctrl* ctrl) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (sbase - raw);
+  // region 0: the [K; Q] tile (two 16 KB atoms) and A, later the three
+  // parts of the left factor of step 4 (16 KB each)
+  uint8_t* tKQ = gb;
+  float* As = reinterpret_cast<float*>(gb + kPrepKQBytes);  // [C][kLdA]
+  uint8_t* tTP = gb;
+  uint8_t* tVK = gb + kPrepR0Bytes;                          // 256 rows x 128 B
+  float* Ts = reinterpret_cast<float*>(tVK + kPrepVKBytes);  // [C][kLdT]
+  float* Xs = Ts + kCh * kLdT;                               // 3 x [16][16]
+  float* G = Xs + 3 * 256;                                   // [C] log gates
+  float* bt = G + kCh;                                       // [C] beta
+  float* bg = bt + kCh;                                      // [C] beta g
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bg + kCh);    // two mbarriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  const uint32_t bar1 = smem_u32(bars), bar2 = smem_u32(bars + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;
   const int c = blockIdx.x, h = blockIdx.y, hk = h / (n_v / n_k);
   const int t0 = c * kCh, n = min(kCh, T - t0);
+  if (tid == 0) {
+    mbar_init(bar1, 1);
+    mbar_init(bar2, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kPrepTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_trigger();
-  // tokens past the sequence end read as k = q = v = 0, alpha = 1, beta = 0:
-  // they leave every quantity below unchanged
+  volatile int never = 0;
+  // 1. tiles. Row r of a K-major tile holds 64 elements in 8 chunks of 16
+  // bytes; chunk cc of row r sits at r * 128 + ((cc ^ (r & 7)) << 4) within
+  // its 1024-byte-aligned atom. Tokens past the sequence end read as
+  // k = q = v = 0, alpha = 1, beta = 0: they change nothing below.
+  // Every load of a thread is issued before its stores (one round trip),
+  // warp 0's gates too.
   const uint4 z4 = make_uint4(0, 0, 0, 0);
-  for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
-    const int t = idx >> 4, ch = idx & 15;
-    uint4 kv = z4, qv = z4;
-    if (t < n) {
-      const size_t src = ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8;
-      kv = __ldg(reinterpret_cast<const uint4*>(k + src));
-      qv = __ldg(reinterpret_cast<const uint4*>(q + src));
+  float alpha_a = 1.0f, alpha_b = 1.0f, beta_a = 0.0f, beta_b = 0.0f;
+  if (warp == 0) {
+    const int ta = 2 * lane, tb = 2 * lane + 1;
+    if (ta < n) {
+      alpha_a = __ldg(alpha + (size_t)(t0 + ta) * n_v + h);
+      beta_a = __ldg(beta + (size_t)(t0 + ta) * n_v + h);
     }
-    *reinterpret_cast<uint4*>(Kb + t * kLdH + ch * 8) = kv;
-    *reinterpret_cast<uint4*>(Qb + t * kLdH + ch * 8) = qv;
+    if (tb < n) {
+      alpha_b = __ldg(alpha + (size_t)(t0 + tb) * n_v + h);
+      beta_b = __ldg(beta + (size_t)(t0 + tb) * n_v + h);
+    }
   }
-  const int vch = dv / 8;
-  for (int idx = tid; idx < kCh * vch; idx += kThr) {
-    const int t = idx / vch, ch = idx % vch;
-    uint4 vv = z4;
-    if (t < n) vv = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(t0 + t) * n_v + h) * dv + ch * 8));
-    *reinterpret_cast<uint4*>(Vb + t * kLdH + ch * 8) = vv;
+  constexpr int kKQItems = 2 * kCh * (kDK / 8) / kThr;   // 8 chunks of [K; Q] per thread
+  constexpr int kVKItems = 2 * (kCh / 2) * 16 / kThr;    // 4 (pair, 8 columns) items
+  uint4 kq[kKQItems], ra[kVKItems], rb[kVKItems];
+#pragma unroll
+  for (int m = 0; m < kKQItems; ++m) {
+    const int idx = tid + m * kThr, r = idx >> 4, ch = idx & 15;  // r < 64: K; r >= 64: Q
+    const int t = r & (kCh - 1);
+    kq[m] = z4;
+    if (t < n)
+      kq[m] = __ldg(reinterpret_cast<const uint4*>((r < kCh ? k : q) +
+                                                   ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8));
+  }
+  // V^T (rows 0..127, zero past dv) and K^T (rows 128..255): item = (token
+  // pair p, 8 columns); two 16-byte row loads give 8 words of (t = 2p,
+  // 2p + 1) pairs. The lanes of a warp take the 32 token pairs, so each of
+  // its 4-byte stores fills one 128-byte row without bank conflict.
+#pragma unroll
+  for (int m = 0; m < kVKItems; ++m) {
+    const int idx = tid + m * kThr;
+    const int mat = idx >> 9, ch = (idx >> 5) & 15, p2 = idx & 31;
+    const int ta = 2 * p2, tb = ta + 1;
+    ra[m] = z4;
+    rb[m] = z4;
+    if (mat == 0) {
+      if (ch * 8 < dv) {
+        const uint16_t* vb = v + (size_t)h * dv + ch * 8;
+        if (ta < n) ra[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + ta) * n_v * dv));
+        if (tb < n) rb[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + tb) * n_v * dv));
+      }
+    } else {
+      const uint16_t* kb = k + (size_t)hk * kDK + ch * 8;
+      if (ta < n) ra[m] = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(t0 + ta) * n_k * kDK));
+      if (tb < n) rb[m] = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(t0 + tb) * n_k * kDK));
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kKQItems; ++m) {
+    const int idx = tid + m * kThr, r = idx >> 4, ch = idx & 15;
+    const int atom = ch >> 3, cc = ch & 7;
+    *reinterpret_cast<uint4*>(tKQ + atom * kPrepAtom + r * 128 + ((cc ^ (r & 7)) << 4)) = kq[m];
+  }
+#pragma unroll
+  for (int m = 0; m < kVKItems; ++m) {
+    const int idx = tid + m * kThr;
+    const int mat = idx >> 9, ch = (idx >> 5) & 15, p2 = idx & 31;
+    const int ta = 2 * p2;
+    const uint32_t wa[4] = {ra[m].x, ra[m].y, ra[m].z, ra[m].w};
+    const uint32_t wb[4] = {rb[m].x, rb[m].y, rb[m].z, rb[m].w};
+    const int cc = ta >> 3, within = (ta & 7) * 2;  // bytes of token ta inside its chunk
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int row = mat * 128 + ch * 8 + e;
+      const uint32_t lo = (e & 1) ? (wa[e >> 1] >> 16) : (wa[e >> 1] & 0xFFFFu);
+      const uint32_t hi = (e & 1) ? (wb[e >> 1] & 0xFFFF0000u) : (wb[e >> 1] << 16);
+      *reinterpret_cast<uint32_t*>(tVK + row * 128 + ((cc ^ (row & 7)) << 4) + within) = lo | hi;
+    }
   }
   float* blk = ws + ((size_t)c * n_v + h) * blk_floats(dv);
   float* gW1 = blk;
@@ -179,8 +258,8 @@ __global__ void __launch_bounds__(kThr, 2)
     // log alpha, bounded below so that a gate of exactly 0 still gives
     // finite differences (exp(-100) is 0 to fp32 precision in every product)
     const int ta = 2 * lane, tb = 2 * lane + 1;
-    const float la = ta < n ? fmaxf(logf(__ldg(alpha + (size_t)(t0 + ta) * n_v + h)), -100.0f) : 0.0f;
-    const float lb = tb < n ? fmaxf(logf(__ldg(alpha + (size_t)(t0 + tb) * n_v + h)), -100.0f) : 0.0f;
+    const float la = ta < n ? fmaxf(logf(alpha_a), -100.0f) : 0.0f;
+    const float lb = tb < n ? fmaxf(logf(alpha_b), -100.0f) : 0.0f;
     float incl = la + lb;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -191,63 +270,58 @@ __global__ void __launch_bounds__(kThr, 2)
     G[ta] = Ga;
     G[tb] = Gb;
     const float GC = __shfl_sync(0xffffffffu, incl, 31);
-    const float ba = ta < n ? __ldg(beta + (size_t)(t0 + ta) * n_v + h) : 0.0f;
-    const float bb = tb < n ? __ldg(beta + (size_t)(t0 + tb) * n_v + h) : 0.0f;
-    const float ga = expf(Ga), gb = expf(Gb);
+    const float ba = beta_a, bb = beta_b;
+    const float ga = expf(Ga), gbv = expf(Gb);
     bt[ta] = ba;
     bt[tb] = bb;
     bg[ta] = ba * ga;
-    bg[tb] = bb * gb;
-    *reinterpret_cast<float2*>(gG + ta) = make_float2(ga, gb);
+    bg[tb] = bb * gbv;
+    *reinterpret_cast<float2*>(gG + ta) = make_float2(ga, gbv);
     *reinterpret_cast<float2*>(gG + kCh + ta) = make_float2(expf(GC - Ga), expf(GC - Gb));
   }
+  fence_proxy_async_smem();  // the tiles are read by the tensor core
   __syncthreads();
-  {
-    // 2. warps 0-3: K K^T -> A, warps 4-7: Q K^T -> P; warp row tile mt,
-    // column tiles 0 .. 2mt+1 (the rest lies above the diagonal)
-    const int pq = warp >> 2, mt = warp & 3, ntn = 2 * mt + 2;
-    const uint16_t* L = pq ? Qb : Kb;
-    float acc[8][4];
+  // 2. [K; Q] K^T
+  bool ok = true;
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16(128, kCh);
+    const uint32_t a0 = smem_u32(tKQ);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
-    const int ra = 16 * mt + gq;
-#pragma unroll 2
-    for (int kb = 0; kb < kDK / 16; ++kb) {
-      const int j = 16 * kb + 2 * cq;
-      uint32_t af[4];
-      af[0] = *reinterpret_cast<const uint32_t*>(L + ra * kLdH + j);
-      af[1] = *reinterpret_cast<const uint32_t*>(L + (ra + 8) * kLdH + j);
-      af[2] = *reinterpret_cast<const uint32_t*>(L + ra * kLdH + j + 8);
-      af[3] = *reinterpret_cast<const uint32_t*>(L + (ra + 8) * kLdH + j + 8);
+    for (int atom = 0; atom < 2; ++atom)
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (u < ntn) {
-          const uint16_t* kr = Kb + (8 * u + gq) * kLdH + j;
-          mma_bf16(acc[u], af, *reinterpret_cast<const uint32_t*>(kr),
-                   *reinterpret_cast<const uint32_t*>(kr + 8));
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; e += 2) {
-        const int t = ra + 8 * (e >> 1), s = 8 * u + 2 * cq;
-        float2 val = make_float2(0.0f, 0.0f);
-        if (u < ntn) {
-          const float r0 = s <= t ? expf(G[t] - G[s]) : 0.0f;
-          const float r1 = s + 1 <= t ? expf(G[t] - G[s + 1]) : 0.0f;
-          if (pq)
-            val = make_float2(r0 * acc[u][e], r1 * acc[u][e + 1]);
-          else
-            val = make_float2(s < t ? bt[t] * r0 * acc[u][e] : 0.0f,
-                              s + 1 < t ? bt[t] * r1 * acc[u][e + 1] : 0.0f);
-        }
-        if (pq)
-          *reinterpret_cast<float2*>(gP + (size_t)t * kCh + s) = val;
-        else if (u < ntn)
-          *reinterpret_cast<float2*>(As + t * kLdA + s) = val;
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t d = smem_desc_sw128(a0 + atom * kPrepAtom + kk * 32);
+        mma_bf16_ss(tmem, d, d, idesc, (atom | kk) != 0);
       }
+    mma_commit(bar1);
   }
+  ok = mbar_wait(bar1, 0, &never);
+  if (!ok && lane == 0) set_error(ctrl, MOE_ERR_TIMEOUT, KID_GDN, 1);
+  tc_fence_after();
+  {
+    // warps q and q + 4 read TMEM lane quarter q, 32 columns each
+    const int qr = warp & 3, half = warp >> 2;
+    const int row = 32 * qr + lane, t = row & (kCh - 1);
+    const uint32_t taddr = tmem + ((uint32_t)(32 * qr) << 16) + 32 * half;
+    uint32_t va[16], vb2[16];
+    tmem_ld16r(taddr, va);
+    tmem_ld16r(taddr + 16, vb2);
+    tmem_wait_ld();
+    float out[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int s2 = 32 * half + i;
+      const float acc = __uint_as_float(i < 16 ? va[i] : vb2[i - 16]);
+      const float ratio = s2 <= t ? expf(G[t] - G[s2]) : 0.0f;
+      out[i] = row < kCh ? (s2 < t ? bt[t] * ratio * acc : 0.0f) : ratio * acc;
+    }
+    float* dst = row < kCh ? As + t * kLdA + 32 * half : gP + (size_t)t * kCh + 32 * half;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+      *reinterpret_cast<float4*>(dst + i) = make_float4(out[i], out[i + 1], out[i + 2], out[i + 3]);
+  }
+  tc_fence_before();
   __syncthreads();
   // 3. diagonal blocks of T: thread (b, cc) solves column cc of block b;
   // entries above the diagonal come out as 0
@@ -305,53 +379,91 @@ __global__ void __launch_bounds__(kThr, 2)
     }
     __syncthreads();
   }
-  {
-    // 4. warps 0-3: W1 (right factor V, column scale beta), warps 4-7: W2
-    // (right factor K, column scale beta g); each warp takes half of the
-    // column tiles and row tiles {0, 3} or {1, 2} (the same number of
-    // k-steps, T being lower triangular)
-    const int pw = warp >> 2, nh = (warp >> 1) & 1, mp = warp & 1;
-    const int ntot = pw ? kDK / 8 : dv / 8, nhalf = ntot / 2, nbase = nh * nhalf;
-    const uint16_t* R = pw ? Kb : Vb;
-    const float* sc = pw ? bg : bt;
-    float* dst = pw ? gW2 : gW1;
-    const int ld = pw ? kDK : dv;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int mt = pass == 0 ? mp : 3 - mp;
-      const int ra = 16 * mt + gq;
-      float acc[8][4];
+  // 4. the left factor [T diag(beta); T diag(beta g)] in three bf16 parts,
+  // over the dead [K; Q] tile and A; thread item = (row, 8 columns). T is
+  // lower triangular, so the blocks above the diagonal are written as 0.
+  for (int idx = tid; idx < 2 * kCh * 8; idx += kThr) {
+    const int r = idx >> 3, cc = idx & 7, t = r & (kCh - 1);
+    const float* sc = r < kCh ? bt : bg;
+    uint32_t pw[3][4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
-#pragma unroll 1
-      for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
-        const int s0 = 8 * kb + cq;
-        const float c0 = sc[s0], c1 = sc[s0 + 4];
-        uint32_t hi[4], lo[4];
-        split_tf32(Ts[ra * kLdT + s0] * c0, hi[0], lo[0]);
-        split_tf32(Ts[(ra + 8) * kLdT + s0] * c0, hi[1], lo[1]);
-        split_tf32(Ts[ra * kLdT + s0 + 4] * c1, hi[2], lo[2]);
-        split_tf32(Ts[(ra + 8) * kLdT + s0 + 4] * c1, hi[3], lo[3]);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (u < nhalf) {
-            const int col = 8 * (nbase + u) + gq;
-            const uint32_t b0 = (uint32_t)R[s0 * kLdH + col] << 16;
-            const uint32_t b1 = (uint32_t)R[(s0 + 4) * kLdH + col] << 16;
-            mma_tf32(acc[u], hi, b0, b1);
-            mma_tf32(acc[u], lo, b0, b1);
-          }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (u < nhalf)
-#pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int t = ra + 8 * (e >> 1), col = 8 * (nbase + u) + 2 * cq;
-            *reinterpret_cast<float2*>(dst + (size_t)t * ld + col) =
-                make_float2(acc[u][e], acc[u][e + 1]);
-          }
+    for (int e = 0; e < 8; e += 2) {
+      const int s0 = 8 * cc + e;
+      const bool lo_ok = (s0 >> 4) <= (t >> 4), hi_ok = ((s0 + 1) >> 4) <= (t >> 4);
+      const float x0 = lo_ok ? Ts[t * kLdT + s0] * sc[s0] : 0.0f;
+      const float x1 = hi_ok ? Ts[t * kLdT + s0 + 1] * sc[s0 + 1] : 0.0f;
+      const uint32_t h01 = pack_bf2(x0, x1);
+      const float r0 = x0 - bf_lo(h01), r1 = x1 - bf_hi(h01);
+      const uint32_t m01 = pack_bf2(r0, r1);
+      const uint32_t l01 = pack_bf2(r0 - bf_lo(m01), r1 - bf_hi(m01));
+      pw[0][e >> 1] = h01;
+      pw[1][e >> 1] = m01;
+      pw[2][e >> 1] = l01;
     }
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+      *reinterpret_cast<uint4*>(tTP + part * kPrepAtom + r * 128 + ((cc ^ (r & 7)) << 4)) =
+          make_uint4(pw[part][0], pw[part][1], pw[part][2], pw[part][3]);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && ok) {
+    tc_fence_after();
+    const uint32_t idesc = idesc_bf16(128, 256);
+    const uint32_t a0 = smem_u32(tTP), b0 = smem_u32(tVK);
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_bf16_ss(tmem, smem_desc_sw128(a0 + part * kPrepAtom + kk * 32),
+                    smem_desc_sw128(b0 + kk * 32), idesc, (part | kk) != 0);
+    mma_commit(bar2);
+  }
+  if (ok) {
+    ok = mbar_wait(bar2, 0, &never);
+    if (!ok && lane == 0) set_error(ctrl, MOE_ERR_TIMEOUT, KID_GDN, 2);
+  }
+  tc_fence_after();
+  if (ok) {
+    // rows 0..63: T diag(beta) [V | K], columns 0..dv-1 are W1; rows
+    // 64..127: T diag(beta g) [V | K], columns 128..255 are W2. Warps q and
+    // q + 4 take lane quarter q, 64 columns each.
+    const int qr = warp & 3, half = warp >> 2;
+    const int row = 32 * qr + lane, t = row & (kCh - 1);
+    const bool w1 = row < kCh;
+    const int cbase = (w1 ? 0 : 128) + 64 * half;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * qr) << 16) + cbase;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      uint32_t va[16];
+      tmem_ld16r(taddr + c0, va);
+      tmem_wait_ld();
+      const int col = 64 * half + c0;  // column of W1 or W2
+      if (w1) {
+        if (col < dv) {
+          float* dst = gW1 + (size_t)t * dv + col;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                make_float4(__uint_as_float(va[i]), __uint_as_float(va[i + 1]),
+                            __uint_as_float(va[i + 2]), __uint_as_float(va[i + 3]));
+        }
+      } else {
+        float* dst = gW2 + (size_t)t * kDK + col;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          *reinterpret_cast<float4*>(dst + i) =
+              make_float4(__uint_as_float(va[i]), __uint_as_float(va[i + 1]),
+                          __uint_as_float(va[i + 2]), __uint_as_float(va[i + 3]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPrepTmemCols);
   }
 }
 
@@ -748,9 +860,11 @@ __global__ void __launch_bounds__(kThr, 1)
   }
 }
 
+// The workspace: a 256-byte status header (Ctrl, zero-filled once by the
+// caller), then the per-(chunk, head) blocks.
 size_t gdn_chunk_ws_bytes(const moe_gdn_shape_t* s) {
   const size_t n_chunks = ((size_t)s->T + kCh - 1) / kCh;
-  return n_chunks * (size_t)s->n_v * blk_floats(s->dv) * sizeof(float);
+  return sizeof(Ctrl) + n_chunks * (size_t)s->n_v * blk_floats(s->dv) * sizeof(float);
 }
 
 cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, const uint16_t* k,
@@ -773,9 +887,11 @@ cudaError_t launch_gdn_chunked(const moe_gdn_shape_t* s, const uint16_t* q, cons
     attr_set = true;
   }
   const int n_chunks = (s->T + kCh - 1) / kCh;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
+  ws += sizeof(Ctrl) / sizeof(float);
   cudaError_t e = launch_pdl(gdn_chunk_prep_kernel, dim3(n_chunks, s->n_v), dim3(kThr),
                              (size_t)prep_smem, stream, q, k, v, alpha, beta, s->T, s->n_k, s->n_v,
-                             s->dv, ws);
+                             s->dv, ws, ctrl);
   if (e != cudaSuccess) return e;
   // the tensor-core scan (32 state rows per CTA) when dv allows, else the
   // CUDA-core one with 16 rows

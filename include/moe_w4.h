@@ -395,9 +395,12 @@ moe_status_t moe_gdn_scan(const moe_gdn_shape_t* shape, const void* q_dev, const
  * exact, fp32 operands split into two tf32 parts; decay ratios taken as
  * exp of differences of summed log alpha). ws_dev: device workspace of at
  * least moe_gdn_chunked_workspace_bytes(shape) bytes, 16-byte aligned,
- * caller owned (per chunk and value head the chunk's two solved right-hand
- * sides, its decay-masked q.k matrix and two decay vectors; the contents
- * need no initialisation). Errors: as moe_gdn_scan, plus
+ * caller owned: a 256-byte status header, zero-filled once before first
+ * use (moe_workspace_init), then per chunk and value head the chunk's two
+ * solved right-hand sides, its decay-masked q.k matrix and two decay
+ * vectors (no initialisation needed). A bounded wait inside the kernels
+ * that runs out is recorded in the header and surfaces through
+ * moe_query_device_status(ws_dev). Errors: as moe_gdn_scan, plus
  * MOE_ERR_WORKSPACE when ws_bytes is too small. */
 size_t moe_gdn_chunked_workspace_bytes(const moe_gdn_shape_t* shape);
 moe_status_t moe_gdn_chunked_scan(const moe_gdn_shape_t* shape, const void* q_dev,
