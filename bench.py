@@ -15,6 +15,9 @@ so no L2 flush is needed between steps; config says so.
   attn_decode  one token through the 10 full-attention layers: 16 query
                heads on 2 KV heads, D=128, a 32K block-paged cache each
                (moe_attn_decode; 336 MB of caches, more than L2)
+  gdn_prefill  a 2048-token prompt through the 30 Gated DeltaNet layers:
+               16 key and 32 value heads of 128, the chunked scan
+               (moe_gdn_chunked_scan), distinct inputs and states per layer
 Options: --block (decode: decoder blocks fed token ids, moe_decoder_blocks),
 --tile-rows N (the grouped GEMMs' most tokens per tile), --layers N.
 
@@ -873,13 +876,209 @@ def run_attn(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------- Gated DeltaNet prefill leg --
+# The model's 30 Gated DeltaNet layers over one 2048-token prompt: 16 key
+# heads and 32 value heads of 128, each layer's chunked scan from its own
+# state (inputs and states distinct per layer, about 1.6 GB, more than L2;
+# one workspace shared, the calls being in stream order).
+GDN_WORKLOADS = {"gdn_prefill": dict(T=2048, n_k=16, n_v=32, dk=128, dv=128, layers=30)}
+GDN_METRIC = "Gated DeltaNet chunked-scan prefill tokens/s (T=2048, 30 layers); % of HBM roofline"
+
+
+def gdn_bytes(c):
+    """Algorithmic bytes of one layer's call: q, k, v, alpha and beta read,
+    the state read and written, o written."""
+    T, n_k, n_v, dk, dv = c["T"], c["n_k"], c["n_v"], c["dk"], c["dv"]
+    return (2 * T * n_k * dk * 2 + T * n_v * dv * 2 + 2 * T * n_v * 4 + 2 * n_v * dv * dk * 4 +
+            T * n_v * dv * 2)
+
+
+def gdn_oracle(c, budget_s=12.0, steps=0):
+    """Seconds per call of the oracle's recurrence on one layer (at least
+    one call, more within budget)."""
+    import oracle
+    inp = synth.gen_gdn(c["T"], c["n_k"], c["n_v"], c["dk"], c["dv"], seed=1)
+    times = []
+    while not times or (sum(times) < budget_s and len(times) < max(3, steps)):
+        t0 = time.time()
+        oracle.gdn_scan(*inp)
+        times.append(time.time() - t0)
+    return times, oracle.num_threads()
+
+
+def run_gdn(args):
+    import torch
+    name = args.workload
+    c = GDN_WORKLOADS[name]
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times, thr = gdn_oracle(c, budget_s=60.0, steps=args.warmup + args.steps)
+        times = times[args.warmup:] or times
+        v = c["T"] / (statistics.mean(times) * c["layers"])
+        cb = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+              "sample": "one layer's scan per step, tokens/s divided by %d layers" % c["layers"]}
+        print(json.dumps({"impl": "reference", "metric": GDN_METRIC, "value": v,
+                          "unit": "tokens/s", "n_gpus": args.gpus, "steps": len(times),
+                          "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 3),
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "config": dict(workload=name, **c),
+                          "cpu_baseline": cb,
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_moe_expert_histogram_gb300 as m
+    m.load()
+    T = c["T"]
+    shape = m.make_gdn_shape(T, c["n_k"], c["n_v"], c["dk"], c["dv"])
+    d16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)  # noqa
+    layers = []
+    for l in range(c["layers"]):
+        q, k, v, a, b, s0 = synth.gen_gdn(T, c["n_k"], c["n_v"], c["dk"], c["dv"],
+                                          seed=1000 * rank + l)
+        layers.append((d16(q), d16(k), d16(v), f32(a), f32(b), f32(s0)))
+    ws = m.alloc_gdn_workspace(shape, dev)
+    o = torch.empty((T, c["n_v"], c["dv"]), dtype=torch.int16, device=dev)
+
+    def step():
+        for (q, k, v, a, b, s) in layers:
+            m.moe_gdn_chunked_scan(shape, q, k, v, a, b, s, s, o, ws)
+
+    # e2e: the first layer's inputs copied in from pinned host memory, every
+    # layer's scan, the last output read back
+    pins = [t.cpu().pin_memory() for t in layers[0][:5]]
+    devs = [torch.empty_like(t) for t in layers[0][:5]]
+    o_pin = torch.empty_like(o, device="cpu").pin_memory()
+
+    def step_e2e():
+        for dst, src in zip(devs, pins):
+            dst.copy_(src, non_blocking=True)
+        q, k, v, a, b = devs
+        m.moe_gdn_chunked_scan(shape, q, k, v, a, b, layers[0][5], layers[0][5], o, ws)
+        for (q2, k2, v2, a2, b2, s2) in layers[1:]:
+            m.moe_gdn_chunked_scan(shape, q2, k2, v2, a2, b2, s2, s2, o, ws)
+        o_pin.copy_(o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    if m.moe_query_device_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+        step_e2e()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g_step, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    with torch.cuda.graph(g_e2e):
+        step_e2e()
+    for _ in range(args.warmup):
+        g_step.replay()
+    stream = torch.cuda.current_stream()
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus) if rank == 0 else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    for e0, e1 in evs:
+        e0.record(stream)
+        g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(per)
+    if world > 1:
+        ms = max_over_ranks(ms, dist, dev)
+    if m.moe_query_device_status(ws) != 0:
+        raise RuntimeError("device status after the timed region")
+    e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        g_e2e.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if world > 1:
+        e_ms = max_over_ranks(e_ms, dist, dev)
+    hbm, _, _, src = peaks()
+    ms_step = ms / args.steps
+    per_launch_ms = ms_step / c["layers"]
+    ub = gdn_bytes(c)
+    gbs = ub / (per_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": GDN_METRIC, "value": round(job_throughput(T, world, ms_step), 2),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "step_ms": step_spread(per),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 q/k/v -> fp32 state and sums",
+        "data": "synthetic (seeded numpy: q, k unit rows, v N(0,1), alpha U[0.9,1), beta U[0,1),"
+                " state N(0,0.01))",
+        "config": dict(workload=name, l2="no flush: %d layers' inputs and states, %.0f MB > 129 MB L2"
+                       % (c["layers"], c["layers"] * ub / 1e6),
+                       parallelism="replicas x%d" % world, **c),
+        "roofline": {"kernel": "gdn_chunk_prep_kernel + gdn_chunk_scan_tc_kernel, one layer's call",
+                     "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "peak_source": src,
+                     "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "traffic": measured_traffic(name),
+                     "ms_per_launch": round(per_launch_ms, 5),
+                     "algorithmic_bytes_per_launch": ub},
+        "e2e": {"value": round(job_throughput(T, world, e_ms), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in pins)),
+                "d2h_bytes_per_step": int(o_pin.numel() * 2), "steps": e_steps,
+                "ms_per_step": round(e_ms, 5),
+                "mode": "CUDA graph of the first layer's input copies, the 30 moe_gdn_chunked_scan"
+                        " calls and the read-back"},
+        "gpu_launches": 2 * c["layers"] * args.steps,
+        "launch_mode": "CUDA graph replay (prep and scan kernels per layer)",
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, thr = gdn_oracle(c, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": T / (statistics.mean(times) * c["layers"]),
+                                "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": "%d call(s) of one layer's recurrence, scaled to %d layers"
+                                          % (len(times), c["layers"]),
+                                "seconds": round(sum(times), 3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="prefill",
-                    choices=sorted(synth.CONFIGS) + sorted(ATTN_WORKLOADS))
+                    choices=sorted(synth.CONFIGS) + sorted(ATTN_WORKLOADS) + sorted(GDN_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-legs", action="store_true",
@@ -897,6 +1096,9 @@ def main():
         args.warmup = 3
     if args.workload in ATTN_WORKLOADS:
         run_attn(args)
+        return
+    if args.workload in GDN_WORKLOADS:
+        run_gdn(args)
         return
     wl = synth.CONFIGS[args.workload]
     if args.layers > 0:
