@@ -909,7 +909,9 @@ def gdn_oracle(c, budget_s=12.0, steps=0):
 def run_gdn(args):
     import torch
     name = args.workload
-    c = GDN_WORKLOADS[name]
+    c = dict(GDN_WORKLOADS[name])
+    if args.layers > 0:
+        c["layers"] = args.layers
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank != 0:
