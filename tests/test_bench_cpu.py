@@ -58,6 +58,12 @@ def test_algorithmic_counts():
     assert flops == ffn_flops + 2 * S.E * S.H * 16
     c = bench.ATTN_WORKLOADS["attn_decode"]
     assert bench.attn_bytes(c) == c["L"] * 2 * 128 * 4 + 512 * 4 + 2 * 16 * 128 * 2
+    # one chunked DeltaNet call at T=2048: q and k (16 heads), v and o (32
+    # heads) in bf16, the two fp32 gates, the fp32 state read and written
+    g = bench.GDN_WORKLOADS["gdn_prefill"]
+    assert (g["T"], g["n_k"], g["n_v"], g["dk"], g["dv"]) == (2048, 16, 32, 128, 128)
+    assert bench.gdn_bytes(g) == (2 * 2048 * 16 * 128 * 2 + 2 * 2048 * 32 * 128 * 2 +
+                                  2 * 2048 * 32 * 4 + 2 * 32 * 128 * 128 * 4)
 
 
 def test_tensor_or_hbm_bound_by_the_ridge():

@@ -86,6 +86,7 @@ def run_chunked(T, n_k, n_v, dk, dv, inputs, state=None):
     m.moe_gdn_chunked_scan(shape, d16(q, "cuda"), d16(k, "cuda"), d16(v, "cuda"), dev_f32(alpha),
                            dev_f32(beta), sd, sd, o, ws)
     torch.cuda.synchronize()
+    assert m.moe_query_device_status(ws) == 0  # the workspace's status word stays clear
     return h16(o).copy(), sd.cpu().numpy()
 
 
