@@ -81,6 +81,36 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// acc (+)= sum over nk blocks b of L_b R_b, each a 16 x 16 fp32 block: L_b
+// at L + b * lstep (row stride ldL), R_b at R + b * rstep (row stride ldR);
+// both factors split into tf32 hi + lo (hi*hi + hi*lo + lo*hi). acc holds
+// the warp's D fragments of the two 8-column halves (m16n8k8 layout).
+__device__ __forceinline__ void blk16_mm(const float* L, int ldL, int lstep, const float* R,
+                                         int ldR, int rstep, int nk, float (&acc)[2][4], int lane) {
+  const int gq = lane >> 2, cq = lane & 3;
+  for (int b = 0; b < nk; ++b) {
+    const float* Lb = L + b * lstep;
+    const float* Rb = R + b * rstep;
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+      uint32_t ah[4], al[4];
+      split_tf32(Lb[gq * ldL + k0 + cq], ah[0], al[0]);
+      split_tf32(Lb[(gq + 8) * ldL + k0 + cq], ah[1], al[1]);
+      split_tf32(Lb[gq * ldL + k0 + cq + 4], ah[2], al[2]);
+      split_tf32(Lb[(gq + 8) * ldL + k0 + cq + 4], ah[3], al[3]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(Rb[(k0 + cq) * ldR + 8 * u + gq], bh0, bl0);
+        split_tf32(Rb[(k0 + cq + 4) * ldR + 8 * u + gq], bh1, bl1);
+        mma_tf32(acc[u], ah, bh0, bh1);
+        mma_tf32(acc[u], ah, bl0, bl1);
+        mma_tf32(acc[u], al, bh0, bh1);
+      }
+    }
+  }
+}
+
 // prep tiles: bf16 rows of 136 halves (68 words) and fp32 rows of 72 / 68
 // floats put the fragment loads and stores of the MMAs on 32 distinct banks
 constexpr int kLdH = 136;
@@ -126,7 +156,8 @@ constexpr int scan_smem_floats() {
 //     give A, rows 64..127 give P
 //  3. T = (I + A)^-1 by 16 x 16 blocks: the four diagonal blocks by forward
 //     substitution (one thread per column), then the blocks below them by
-//     distance from the diagonal, T_ij = -T_ii sum_k A_ik T_kj
+//     distance from the diagonal, T_ij = -T_ii sum_k A_ik T_kj (16 x 16
+//     products on mma.sync, tf32 with both factors split)
 //  4. [T diag(beta); T diag(beta g)] [V | K] on the tensor cores (M = 128,
 //     N = 256): the fp32 left factor is split into three bf16 parts (24
 //     significant bits) and the three products summed in TMEM; W1 and W2
@@ -194,6 +225,7 @@ __global__ void __launch_bounds__(kThr, 2)
   }
   constexpr int kKQItems = 2 * kCh * (kDK / 8) / kThr;   // 8 chunks of [K; Q] per thread
   constexpr int kVKItems = 2 * (kCh / 2) * 16 / kThr;    // 4 (pair, 8 columns) items
+  constexpr int kVItems = kVKItems / 2;                  // the V^T half comes from global
   uint4 kq[kKQItems], ra[kVKItems], rb[kVKItems];
 #pragma unroll
   for (int m = 0; m < kKQItems; ++m) {
@@ -205,26 +237,21 @@ __global__ void __launch_bounds__(kThr, 2)
                                                    ((size_t)(t0 + t) * n_k + hk) * kDK + ch * 8));
   }
   // V^T (rows 0..127, zero past dv) and K^T (rows 128..255): item = (token
-  // pair p, 8 columns); two 16-byte row loads give 8 words of (t = 2p,
+  // pair p, 8 columns); two 16-byte row chunks give 8 words of (t = 2p,
   // 2p + 1) pairs. The lanes of a warp take the 32 token pairs, so each of
-  // its 4-byte stores fills one 128-byte row without bank conflict.
+  // its 4-byte stores fills one 128-byte row without bank conflict. V's
+  // chunks come from global memory, K's from the [K; Q] tile once it is in.
 #pragma unroll
-  for (int m = 0; m < kVKItems; ++m) {
+  for (int m = 0; m < kVItems; ++m) {
     const int idx = tid + m * kThr;
-    const int mat = idx >> 9, ch = (idx >> 5) & 15, p2 = idx & 31;
+    const int ch = (idx >> 5) & 15, p2 = idx & 31;
     const int ta = 2 * p2, tb = ta + 1;
     ra[m] = z4;
     rb[m] = z4;
-    if (mat == 0) {
-      if (ch * 8 < dv) {
-        const uint16_t* vb = v + (size_t)h * dv + ch * 8;
-        if (ta < n) ra[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + ta) * n_v * dv));
-        if (tb < n) rb[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + tb) * n_v * dv));
-      }
-    } else {
-      const uint16_t* kb = k + (size_t)hk * kDK + ch * 8;
-      if (ta < n) ra[m] = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(t0 + ta) * n_k * kDK));
-      if (tb < n) rb[m] = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(t0 + tb) * n_k * kDK));
+    if (ch * 8 < dv) {
+      const uint16_t* vb = v + (size_t)h * dv + ch * 8;
+      if (ta < n) ra[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + ta) * n_v * dv));
+      if (tb < n) rb[m] = __ldg(reinterpret_cast<const uint4*>(vb + (size_t)(t0 + tb) * n_v * dv));
     }
   }
 #pragma unroll
@@ -232,6 +259,15 @@ __global__ void __launch_bounds__(kThr, 2)
     const int idx = tid + m * kThr, r = idx >> 4, ch = idx & 15;
     const int atom = ch >> 3, cc = ch & 7;
     *reinterpret_cast<uint4*>(tKQ + atom * kPrepAtom + r * 128 + ((cc ^ (r & 7)) << 4)) = kq[m];
+  }
+  __syncthreads();  // the [K; Q] tile is in: K^T's chunks come from it
+#pragma unroll
+  for (int m = kVItems; m < kVKItems; ++m) {
+    const int idx = tid + m * kThr;
+    const int ch = (idx >> 5) & 15, p2 = idx & 31;
+    const int ta = 2 * p2, tb = ta + 1, atom = ch >> 3, kc = ch & 7;
+    ra[m] = *reinterpret_cast<const uint4*>(tKQ + atom * kPrepAtom + ta * 128 + ((kc ^ (ta & 7)) << 4));
+    rb[m] = *reinterpret_cast<const uint4*>(tKQ + atom * kPrepAtom + tb * 128 + ((kc ^ (tb & 7)) << 4));
   }
 #pragma unroll
   for (int m = 0; m < kVKItems; ++m) {
@@ -313,7 +349,9 @@ __global__ void __launch_bounds__(kThr, 2)
     for (int i = 0; i < 32; ++i) {
       const int s2 = 32 * half + i;
       const float acc = __uint_as_float(i < 16 ? va[i] : vb2[i - 16]);
-      const float ratio = s2 <= t ? expf(G[t] - G[s2]) : 0.0f;
+      // exp2 of a scaled argument (relative error ~1e-6 for the arguments
+      // here, which are <= 0 and above -6400)
+      const float ratio = s2 <= t ? __expf(G[t] - G[s2]) : 0.0f;
       out[i] = row < kCh ? (s2 < t ? bt[t] * ratio * acc : 0.0f) : ratio * acc;
     }
     float* dst = row < kCh ? As + t * kLdA + 32 * half : gP + (size_t)t * kCh + 32 * half;
@@ -345,37 +383,35 @@ __global__ void __launch_bounds__(kThr, 2)
     for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdT + 16 * b + cc] = x[r];
   }
   __syncthreads();
+  // the blocks below the diagonal by distance d: warp j takes block
+  // (i = j + d, j); X_ij = sum_{k=j}^{i-1} A_ik T_kj, then T_ij = -T_ii X_ij,
+  // both 16 x 16 products on the tensor cores
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
-    // X_ij = sum_{k=j}^{i-1} A_ik T_kj for the blocks (i, j = i - d)
-    for (int e = tid; e < nb * 256; e += kThr) {
-      const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
-      float a0 = 0.0f, a1 = 0.0f;
-      for (int kk = j; kk < i; ++kk) {
-        const float* ar = As + (16 * i + r) * kLdA + 16 * kk;
-        const float* tc = Ts + (16 * kk) * kLdT + 16 * j + cc;
+    const int gq = lane >> 2, cq = lane & 3;
+    if (warp < nb) {
+      const int j = warp, i = j + d;
+      float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+      blk16_mm(As + (16 * i) * kLdA + 16 * j, kLdA, 16, Ts + (16 * j) * kLdT + 16 * j, kLdT,
+               16 * kLdT, i - j, acc, lane);
+      float* X = Xs + (j << 8);
 #pragma unroll
-        for (int s2 = 0; s2 < 16; s2 += 2) {
-          a0 = __fmaf_rn(ar[s2], tc[s2 * kLdT], a0);
-          a1 = __fmaf_rn(ar[s2 + 1], tc[(s2 + 1) * kLdT], a1);
-        }
+      for (int u = 0; u < 2; ++u) {
+        *reinterpret_cast<float2*>(X + gq * 16 + 8 * u + 2 * cq) = make_float2(acc[u][0], acc[u][1]);
+        *reinterpret_cast<float2*>(X + (gq + 8) * 16 + 8 * u + 2 * cq) =
+            make_float2(acc[u][2], acc[u][3]);
       }
-      Xs[e] = a0 + a1;
-    }
-    __syncthreads();
-    // T_ij = -T_ii X_ij (T_ii lower triangular)
-    for (int e = tid; e < nb * 256; e += kThr) {
-      const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
-      const float* tr = Ts + (16 * i + r) * kLdT + 16 * i;
-      const float* xc = Xs + (j << 8) + cc;
-      float a0 = 0.0f, a1 = 0.0f;
-      for (int s2 = 0; s2 <= r; ++s2) {
-        if (s2 & 1)
-          a1 = __fmaf_rn(tr[s2], xc[s2 * 16], a1);
-        else
-          a0 = __fmaf_rn(tr[s2], xc[s2 * 16], a0);
+      __syncwarp();
+      float tacc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+      blk16_mm(Ts + (16 * i) * kLdT + 16 * i, kLdT, 0, X, 16, 0, 1, tacc, lane);
+      float* To = Ts + (16 * i) * kLdT + 16 * j;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        *reinterpret_cast<float2*>(To + gq * kLdT + 8 * u + 2 * cq) =
+            make_float2(-tacc[u][0], -tacc[u][1]);
+        *reinterpret_cast<float2*>(To + (gq + 8) * kLdT + 8 * u + 2 * cq) =
+            make_float2(-tacc[u][2], -tacc[u][3]);
       }
-      Ts[(16 * i + r) * kLdT + 16 * j + cc] = -(a0 + a1);
     }
     __syncthreads();
   }
