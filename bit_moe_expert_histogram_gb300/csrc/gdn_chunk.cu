@@ -45,8 +45,10 @@ constexpr int kDK = 128;   // key head size
 constexpr int kCh = 64;    // tokens per chunk
 constexpr int kThr = 256;
 
-// per (chunk, head) block of the workspace: W1 [C][dv], W2 [C][dk],
-// P [C][C], g [C] (g_t), gr [C] (g_C / g_t)
+// per (chunk, head) block of the workspace, the matrices transposed (token
+// index fastest, so the prep's one-row-per-lane stores are coalesced):
+// W1^T [dv][C], W2^T [dk][C], P^T [C][C] (P^T[s][t] = P[t][s]), g [C] (g_t),
+// gr [C] (g_C / g_t)
 __host__ __device__ __forceinline__ size_t blk_floats(int dv) {
   return (size_t)kCh * dv + (size_t)kCh * kDK + (size_t)kCh * kCh + 2 * kCh;
 }
@@ -114,7 +116,7 @@ __device__ __forceinline__ void blk16_mm(const float* L, int ldL, int lstep, con
 // prep tiles: bf16 rows of 136 halves (68 words) and fp32 rows of 72 / 68
 // floats put the fragment loads and stores of the MMAs on 32 distinct banks
 constexpr int kLdH = 136;
-constexpr int kLdA = 72;
+constexpr int kLdA = 68;  // consecutive rows 4 banks apart: row-per-lane float4 stores conflict-free
 constexpr int kLdT = 68;
 // tensor-core prep: 128-byte-swizzled bf16 tiles of 128 rows x 64 elements
 // (16 KB atoms); region 0 holds the [K; Q] tile (two atoms) and A, later the
@@ -133,11 +135,11 @@ constexpr int kLdP = kCh + 1;
 // tensor-core scan tiles (32 state rows): padded so that every fragment
 // load of the MMAs touches 32 distinct banks
 constexpr int kTcLdS = 40;    // ST [dk][40]
-constexpr int kTcLd = 132;    // W2, Q [C][132] (A operands)
-constexpr int kTcLdP = 68;    // P [C][68]
-constexpr int kTcLdU = 40;    // W1 rows, U, Ug [C][40]
-// one stage: W2, P, W1 rows, g and g_C / g in fp32, Q and K in bf16
-constexpr int kTcStageFloats = kCh * kTcLd + kCh * kTcLdP + kCh * kTcLdU + 2 * kCh + kCh * kLdH;
+constexpr int kTcLdT = 72;    // W2^T [dk][72], P^T [C][72] (A operands read transposed)
+constexpr int kTcLdW1 = 68;   // W1^T rows r0 .. r0+31 [32][68]
+constexpr int kTcLdU = 40;    // U [C][40]
+// one stage: W2^T, P^T, W1^T rows, g and g_C / g in fp32, Q and K in bf16
+constexpr int kTcStageFloats = kDK * kTcLdT + kCh * kTcLdT + 32 * kTcLdW1 + 2 * kCh + kCh * kLdH;
 constexpr int kTcSmemFloats = kDK * kTcLdS + kCh * kTcLdU + 2 * kTcStageFloats;
 template <int R>
 constexpr int scan_smem_floats() {
@@ -354,10 +356,15 @@ __global__ void __launch_bounds__(kThr, 2)
       const float ratio = s2 <= t ? __expf(G[t] - G[s2]) : 0.0f;
       out[i] = row < kCh ? (s2 < t ? bt[t] * ratio * acc : 0.0f) : ratio * acc;
     }
-    float* dst = row < kCh ? As + t * kLdA + 32 * half : gP + (size_t)t * kCh + 32 * half;
+    if (row < kCh) {
+      float* dst = As + t * kLdA + 32 * half;
 #pragma unroll
-    for (int i = 0; i < 32; i += 4)
-      *reinterpret_cast<float4*>(dst + i) = make_float4(out[i], out[i + 1], out[i + 2], out[i + 3]);
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(out[i], out[i + 1], out[i + 2], out[i + 3]);
+    } else {  // P^T: lanes are consecutive tokens, one 128-byte line per store
+#pragma unroll
+      for (int i = 0; i < 32; ++i) gP[(size_t)(32 * half + i) * kCh + t] = out[i];
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -476,22 +483,15 @@ __global__ void __launch_bounds__(kThr, 2)
       tmem_ld16r(taddr + c0, va);
       tmem_wait_ld();
       const int col = 64 * half + c0;  // column of W1 or W2
+      // transposed: lanes are consecutive tokens, one 128-byte line per store
       if (w1) {
         if (col < dv) {
-          float* dst = gW1 + (size_t)t * dv + col;
 #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + i) =
-                make_float4(__uint_as_float(va[i]), __uint_as_float(va[i + 1]),
-                            __uint_as_float(va[i + 2]), __uint_as_float(va[i + 3]));
+          for (int i = 0; i < 16; ++i) gW1[(size_t)(col + i) * kCh + t] = __uint_as_float(va[i]);
         }
       } else {
-        float* dst = gW2 + (size_t)t * kDK + col;
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          *reinterpret_cast<float4*>(dst + i) =
-              make_float4(__uint_as_float(va[i]), __uint_as_float(va[i + 1]),
-                          __uint_as_float(va[i + 2]), __uint_as_float(va[i + 3]));
+        for (int i = 0; i < 16; ++i) gW2[(size_t)(col + i) * kCh + t] = __uint_as_float(va[i]);
       }
     }
   }
@@ -551,21 +551,21 @@ __global__ void __launch_bounds__(kThr, 1)
     const float* gP = gW2 + (size_t)kCh * kDK;
     const float* gG = gP + (size_t)kCh * kCh;
     __syncthreads();  // the previous chunk's reads of the tiles are done
-    for (int idx = tid; idx < kCh * kDK / 4; idx += kThr) {  // coalesced, 16 bytes a thread
-      const int t = idx / (kDK / 4), j = (idx % (kDK / 4)) * 4;
-      const float4 w = __ldcg(reinterpret_cast<const float4*>(gW2 + (size_t)t * kDK + j));
-      float* d = W2 + t * kLd + j;
-      d[0] = w.x; d[1] = w.y; d[2] = w.z; d[3] = w.w;
+    for (int idx = tid; idx < kCh * kDK / 4; idx += kThr) {  // W2^T rows, 16 bytes a thread
+      const int j = idx / (kCh / 4), t = (idx % (kCh / 4)) * 4;
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(gW2 + (size_t)j * kCh + t));
+      W2[(t + 0) * kLd + j] = w.x; W2[(t + 1) * kLd + j] = w.y;
+      W2[(t + 2) * kLd + j] = w.z; W2[(t + 3) * kLd + j] = w.w;
     }
-    for (int idx = tid; idx < kCh * kCh / 4; idx += kThr) {
-      const int t = idx / (kCh / 4), sc = (idx % (kCh / 4)) * 4;
-      const float4 w = __ldcg(reinterpret_cast<const float4*>(gP + (size_t)t * kCh + sc));
-      float* d = P + t * kLdP + sc;
-      d[0] = w.x; d[1] = w.y; d[2] = w.z; d[3] = w.w;
+    for (int idx = tid; idx < kCh * kCh / 4; idx += kThr) {  // P^T rows
+      const int sc = idx / (kCh / 4), t = (idx % (kCh / 4)) * 4;
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(gP + (size_t)sc * kCh + t));
+      P[(t + 0) * kLdP + sc] = w.x; P[(t + 1) * kLdP + sc] = w.y;
+      P[(t + 2) * kLdP + sc] = w.z; P[(t + 3) * kLdP + sc] = w.w;
     }
-    for (int idx = tid; idx < kCh * R; idx += kThr) {
-      const int t = idx / R, i = idx % R;
-      W1r[idx] = __ldcg(gW1 + (size_t)t * dv + r0 + i);
+    for (int idx = tid; idx < kCh * R; idx += kThr) {  // W1^T rows r0 ..
+      const int i = idx / kCh, t = idx % kCh;
+      W1r[t * R + i] = __ldcg(gW1 + (size_t)(r0 + i) * kCh + t);
     }
     if (tid < 2 * kCh) g[tid] = __ldcg(gG + tid);
     for (int idx = tid; idx < kCh * (kDK / 8); idx += kThr) {
@@ -667,9 +667,9 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // One chunk's tiles for the tensor-core scan, in shared memory
 struct ScanStage {
-  float* W2;     // [C][kTcLd]
-  float* P;      // [C][kTcLdP]
-  float* W1r;    // [C][kTcLdU]: W1 columns r0 .. r0+31
+  float* W2;     // [dk][kTcLdT]: W2^T
+  float* P;      // [C][kTcLdT]: P^T
+  float* W1r;    // [32][kTcLdW1]: W1^T rows r0 .. r0+31
   float* g;      // [C] g_t, then [C] g_C / g_t
   uint16_t* Qb;  // [C][kLdH] bf16
   uint16_t* Kb;  // [C][kLdH] bf16
@@ -677,9 +677,9 @@ struct ScanStage {
 __device__ __forceinline__ ScanStage scan_stage(float* base) {
   ScanStage st;
   st.W2 = base;
-  st.P = st.W2 + kCh * kTcLd;
-  st.W1r = st.P + kCh * kTcLdP;
-  st.g = st.W1r + kCh * kTcLdU;
+  st.P = st.W2 + kDK * kTcLdT;
+  st.W1r = st.P + kCh * kTcLdT;
+  st.g = st.W1r + 32 * kTcLdW1;
   st.Qb = reinterpret_cast<uint16_t*>(st.g + 2 * kCh);
   st.Kb = st.Qb + kCh * kLdH;
   return st;
@@ -697,19 +697,19 @@ __device__ __forceinline__ void scan_issue(const ScanStage& st, const uint16_t* 
   const float* gP = gW2 + (size_t)kCh * kDK;
   const float* gG = gP + (size_t)kCh * kCh;
 #pragma unroll
-  for (int m = 0; m < kCh * kDK / 4 / kThr; ++m) {
-    const int idx = tid + m * kThr, t = idx >> 5, j = (idx & 31) * 4;
-    cp_async16(st.W2 + t * kTcLd + j, gW2 + (size_t)t * kDK + j, 16);
+  for (int m = 0; m < kCh * kDK / 4 / kThr; ++m) {  // W2^T: 128 rows of 64
+    const int idx = tid + m * kThr, j = idx >> 4, t = (idx & 15) * 4;
+    cp_async16(st.W2 + j * kTcLdT + t, gW2 + (size_t)j * kCh + t, 16);
   }
 #pragma unroll
-  for (int m = 0; m < kCh * kCh / 4 / kThr; ++m) {
-    const int idx = tid + m * kThr, t = idx >> 4, sc = (idx & 15) * 4;
-    cp_async16(st.P + t * kTcLdP + sc, gP + (size_t)t * kCh + sc, 16);
+  for (int m = 0; m < kCh * kCh / 4 / kThr; ++m) {  // P^T: 64 rows of 64
+    const int idx = tid + m * kThr, sc = idx >> 4, t = (idx & 15) * 4;
+    cp_async16(st.P + sc * kTcLdT + t, gP + (size_t)sc * kCh + t, 16);
   }
 #pragma unroll
-  for (int m = 0; m < kCh * 32 / 4 / kThr; ++m) {
-    const int idx = tid + m * kThr, t = idx >> 3, i = (idx & 7) * 4;
-    cp_async16(st.W1r + t * kTcLdU + i, gW1 + (size_t)t * dv + r0 + i, 16);
+  for (int m = 0; m < kCh * 32 / 4 / kThr; ++m) {  // W1^T rows r0 .. r0+31
+    const int idx = tid + m * kThr, i = idx >> 4, t = (idx & 15) * 4;
+    cp_async16(st.W1r + i * kTcLdW1 + t, gW1 + (size_t)(r0 + i) * kCh + t, 16);
   }
   if (tid < 2 * kCh / 4) cp_async16(st.g + 4 * tid, gG + 4 * tid, 16);
 #pragma unroll
@@ -786,10 +786,10 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int kb = 0; kb < kDK / 8; ++kb) {
       const int j = 8 * kb + cq;
       uint32_t wh[4], wl[4], qa[4];
-      split_tf32(W2[ra * kTcLd + j], wh[0], wl[0]);
-      split_tf32(W2[(ra + 8) * kTcLd + j], wh[1], wl[1]);
-      split_tf32(W2[ra * kTcLd + j + 4], wh[2], wl[2]);
-      split_tf32(W2[(ra + 8) * kTcLd + j + 4], wh[3], wl[3]);
+      split_tf32(W2[j * kTcLdT + ra], wh[0], wl[0]);
+      split_tf32(W2[j * kTcLdT + ra + 8], wh[1], wl[1]);
+      split_tf32(W2[(j + 4) * kTcLdT + ra], wh[2], wl[2]);
+      split_tf32(W2[(j + 4) * kTcLdT + ra + 8], wh[3], wl[3]);
       qa[0] = (uint32_t)Qb[ra * kLdH + j] << 16;
       qa[1] = (uint32_t)Qb[(ra + 8) * kLdH + j] << 16;
       qa[2] = (uint32_t)Qb[ra * kLdH + j + 4] << 16;
@@ -812,9 +812,8 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int e = 0; e < 4; e += 2) {
         const int t = ra + 8 * (e >> 1), i = 8 * (nt0 + u) + 2 * cq;
-        const float2 w = *reinterpret_cast<const float2*>(sg.W1r + t * kTcLdU + i);
-        *reinterpret_cast<float2*>(U + t * kTcLdU + i) =
-            make_float2(w.x - au[u][e], w.y - au[u][e + 1]);
+        const float w0 = sg.W1r[i * kTcLdW1 + t], w1 = sg.W1r[(i + 1) * kTcLdW1 + t];
+        *reinterpret_cast<float2*>(U + t * kTcLdU + i) = make_float2(w0 - au[u][e], w1 - au[u][e + 1]);
       }
     __syncthreads();
     // (3) O = g Q S0^T + P U; P is zero above the diagonal
@@ -822,10 +821,10 @@ __global__ void __launch_bounds__(kThr, 1)
     for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
       const int sc = 8 * kb + cq;
       uint32_t ph[4], pl[4];
-      split_tf32(P[ra * kTcLdP + sc], ph[0], pl[0]);
-      split_tf32(P[(ra + 8) * kTcLdP + sc], ph[1], pl[1]);
-      split_tf32(P[ra * kTcLdP + sc + 4], ph[2], pl[2]);
-      split_tf32(P[(ra + 8) * kTcLdP + sc + 4], ph[3], pl[3]);
+      split_tf32(P[sc * kTcLdT + ra], ph[0], pl[0]);
+      split_tf32(P[sc * kTcLdT + ra + 8], ph[1], pl[1]);
+      split_tf32(P[(sc + 4) * kTcLdT + ra], ph[2], pl[2]);
+      split_tf32(P[(sc + 4) * kTcLdT + ra + 8], ph[3], pl[3]);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int col = 8 * (nt0 + u) + gq;
