@@ -236,8 +236,9 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
   cudaError_t ge = launch_gather_x(static_cast<const uint16_t*>(x), plan->sorted_rows_dev, K, R, S,
                                    T, H, xs, ctrl, nsm, stream);
   if (ge != cudaSuccess) return cuda_fail(ge, "activation gather launch");
-  // operand rows: boxes of 16 rows x 64 elements
-  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, S, 64, 16,
+  // operand rows: boxes of ffn_b_box_rows() rows x 64 elements
+  const uint32_t bbox = (uint32_t)ffn_b_box_rows();
+  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xs, H, S, 64, bbox,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   FfnArgs a{};
   a.block_map = plan->block_map_dev;
@@ -270,7 +271,7 @@ moe_status_t run_ffn(const moe_shape_t* s, const void* x, const moe_w4_weights_t
                  wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
   MOE_TRY(map_2d(&twsh, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, shw->q_down_dev, I / 8,
                  (uint64_t)(s->n_shared ? 1 : E) * H, wbox, 128, CU_TENSOR_MAP_SWIZZLE_128B));
-  MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, 16,
+  MOE_TRY(map_2d(&th, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, S, 64, bbox,
                  CU_TENSOR_MAP_SWIZZLE_128B));
   a.sorted_rows = nullptr;
   a.rows_per_expert = H;

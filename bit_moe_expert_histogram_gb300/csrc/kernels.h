@@ -176,5 +176,6 @@ void set_last_cuda_error(cudaError_t e, const char* where);
 int ffn_tile_m();
 int ffn_max_tile_n();
 int ffn_stage_k();
+int ffn_b_box_rows();
 
 }  // namespace moe
