@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t acol = tmem + kABase + s * kACols;
           const uint64_t bd = bdesc0 + (uint64_t)((s * kBStage) >> 4);
           mma_bf16_ts(dacc, acol, bd, idesc, st != 0 ? 1u : 0u);
-          if (st + 1 < bstages || ksteps_last == kKS / 16) {
+          // gate_up's reduction (H) is a multiple of kKS: every slot is full
+          if (GATED || st + 1 < bstages || ksteps_last == kKS / 16) {
 #pragma unroll
             for (int kk = 1; kk < kKS / 16; ++kk)
               mma_bf16_ts_acc(dacc, acol + kk * 8,
