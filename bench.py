@@ -768,6 +768,41 @@ ATTN_WORKLOADS = {"attn_decode": dict(T=1, n_q=16, n_kv=2, D=128, L=32768, layer
 ATTN_METRIC = "GQA decode attention tokens/s over a 32K block-paged KV cache; % of HBM roofline"
 
 
+def pipelined_graph_e2e(torch, copy_in, graphs, copy_out, n):
+    """n steps of a serving loop: step i's input copy (copy_in(b)) and
+    read-back (copy_out(b)) on a copy stream, its compute (graphs[b].replay())
+    on the current stream, b = i % 2; step i+1's input copy and step i-1's
+    read-back overlap step i's compute. Returns the milliseconds per step."""
+    comp = torch.cuda.current_stream()
+    cp = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_done = [torch.cuda.Event() for _ in range(n)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    cp.wait_stream(comp)
+
+    def cin(i):
+        with torch.cuda.stream(cp):
+            copy_in(i % 2)  # after step i-2's read-back on this stream
+            ev_in[i].record(cp)
+
+    cin(0)
+    for i in range(n):
+        if i + 1 < n:
+            cin(i + 1)
+        comp.wait_event(ev_in[i])
+        graphs[i % 2].replay()
+        ev_done[i].record(comp)
+        with torch.cuda.stream(cp):
+            cp.wait_event(ev_done[i])
+            copy_out(i % 2)
+    comp.wait_stream(cp)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
 def attn_bytes(c):
     """Algorithmic bytes of one layer's call: the visible keys and values,
     the block table, q read and o written."""
@@ -834,15 +869,19 @@ def run_attn(args):
         for (q, k, v, tab) in layers:
             m.moe_attn_decode(shape, q, k, v, tab, o, ws)
 
-    q_pin = layers[0][0].cpu().pin_memory()
-    o_pin = torch.empty_like(o, device="cpu").pin_memory()
-    q_dev = torch.empty_like(layers[0][0])
+    q_pin = [layers[0][0].cpu().pin_memory() for _ in range(2)]
+    o_pin = [torch.empty_like(o, device="cpu").pin_memory() for _ in range(2)]
+    q_dev = [torch.empty_like(layers[0][0]) for _ in range(2)]
+    o_dev = [torch.empty_like(o) for _ in range(2)]
+
+    def compute_e2e(bf):
+        for (_, k, v, tab) in layers:
+            m.moe_attn_decode(shape, q_dev[bf], k, v, tab, o_dev[bf], ws)
 
     def step_e2e():
-        q_dev.copy_(q_pin, non_blocking=True)
-        for (_, k, v, tab) in layers:
-            m.moe_attn_decode(shape, q_dev, k, v, tab, o, ws)
-        o_pin.copy_(o, non_blocking=True)
+        q_dev[0].copy_(q_pin[0], non_blocking=True)
+        compute_e2e(0)
+        o_pin[0].copy_(o_dev[0], non_blocking=True)
 
     for _ in range(args.warmup):
         step()
@@ -855,11 +894,13 @@ def run_attn(args):
         step_e2e()
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    g_step, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         step()
-    with torch.cuda.graph(g_e2e):
-        step_e2e()
+    g_comp = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+    for bf in range(2):
+        with torch.cuda.graph(g_comp[bf]):
+            compute_e2e(bf)
     for _ in range(args.warmup):
         g_step.replay()
     stream = torch.cuda.current_stream()
@@ -889,17 +930,10 @@ def run_attn(args):
     if m.moe_query_device_status(ws) != 0:
         raise RuntimeError("device status after the timed region")
     e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
-        g_e2e.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        g_e2e.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
+    a_in = lambda bf: q_dev[bf].copy_(q_pin[bf], non_blocking=True)  # noqa
+    a_out = lambda bf: o_pin[bf].copy_(o_dev[bf], non_blocking=True)  # noqa
+    pipelined_graph_e2e(torch, a_in, g_comp, a_out, 4)
+    e_ms = pipelined_graph_e2e(torch, a_in, g_comp, a_out, e_steps)
     if world > 1:
         e_ms = max_over_ranks(e_ms, dist, dev)
     hbm, _, _, src = peaks()
@@ -916,7 +950,7 @@ def run_attn(args):
         "data": "synthetic (seeded numpy: q, k, v N(0,1); block table a random permutation)",
         "config": dict(workload=name, l2="no flush: %d layers' caches, %.0f MB > 129 MB L2" % (
             c["layers"], c["layers"] * ub / 1e6), parallelism="replicas x%d" % world, **c),
-        "roofline": {"kernel": "attn_split_kernel<%d> + attn_merge_kernel, one layer's call"
+        "roofline": {"kernel": "attn_split_kernel<%d> (the merge inside), one layer's call"
                                % c["D"],
                      "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "peak_source": src,
                      "unit": "GB/s", "frac": round(gbs / hbm, 4),
@@ -924,12 +958,14 @@ def run_attn(args):
                      "ms_per_launch": round(per_launch_ms, 5),
                      "algorithmic_bytes_per_launch": ub},
         "e2e": {"value": round(job_throughput(c["T"], world, e_ms), 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(q_pin.numel() * 2),
-                "d2h_bytes_per_step": int(o_pin.numel() * 2), "steps": e_steps,
+                "h2d_bytes_per_step": int(q_pin[0].numel() * 2),
+                "d2h_bytes_per_step": int(o_pin[0].numel() * 2), "steps": e_steps,
                 "ms_per_step": round(e_ms, 5),
-                "mode": "CUDA graph of the q copy, the 10 moe_attn_decode calls and the read-back"},
-        "gpu_launches": 2 * c["layers"] * args.steps,
-        "launch_mode": "CUDA graph replay (split and merge kernels per layer)",
+                "mode": "CUDA graph of the %d moe_attn_decode calls on the compute stream; "
+                        "each step's q copy and read-back on a copy stream, double-buffered so "
+                        "that they overlap the neighbouring steps" % c["layers"]},
+        "gpu_launches": c["layers"] * args.steps,
+        "launch_mode": "CUDA graph replay (one cooperative launch per layer, merge inside)",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1027,18 +1063,28 @@ def run_gdn(args):
 
     # e2e: the first layer's inputs copied in from pinned host memory, every
     # layer's scan, the last output read back
-    pins = [t.cpu().pin_memory() for t in layers[0][:5]]
-    devs = [torch.empty_like(t) for t in layers[0][:5]]
-    o_pin = torch.empty_like(o, device="cpu").pin_memory()
+    pins = [[t.cpu().pin_memory() for t in layers[0][:5]] for _ in range(2)]
+    devs = [[torch.empty_like(t) for t in layers[0][:5]] for _ in range(2)]
+    o_pin = [torch.empty_like(o, device="cpu").pin_memory() for _ in range(2)]
+    o_dev = [torch.empty_like(o) for _ in range(2)]
+
+    def compute_e2e(bf):
+        q, k, v, a, b = devs[bf]
+        m.moe_gdn_chunked_scan(shape, q, k, v, a, b, layers[0][5], layers[0][5], o_dev[bf], ws)
+        for (q2, k2, v2, a2, b2, s2) in layers[1:]:
+            m.moe_gdn_chunked_scan(shape, q2, k2, v2, a2, b2, s2, s2, o_dev[bf], ws)
+
+    def g_in(bf):
+        for dst, src in zip(devs[bf], pins[bf]):
+            dst.copy_(src, non_blocking=True)
+
+    def g_out(bf):
+        o_pin[bf].copy_(o_dev[bf], non_blocking=True)
 
     def step_e2e():
-        for dst, src in zip(devs, pins):
-            dst.copy_(src, non_blocking=True)
-        q, k, v, a, b = devs
-        m.moe_gdn_chunked_scan(shape, q, k, v, a, b, layers[0][5], layers[0][5], o, ws)
-        for (q2, k2, v2, a2, b2, s2) in layers[1:]:
-            m.moe_gdn_chunked_scan(shape, q2, k2, v2, a2, b2, s2, s2, o, ws)
-        o_pin.copy_(o, non_blocking=True)
+        g_in(0)
+        compute_e2e(0)
+        g_out(0)
 
     for _ in range(args.warmup):
         step()
@@ -1051,11 +1097,13 @@ def run_gdn(args):
         step_e2e()
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    g_step, g_e2e = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         step()
-    with torch.cuda.graph(g_e2e):
-        step_e2e()
+    g_comp = [torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()]
+    for bf in range(2):
+        with torch.cuda.graph(g_comp[bf]):
+            compute_e2e(bf)
     for _ in range(args.warmup):
         g_step.replay()
     stream = torch.cuda.current_stream()
@@ -1085,17 +1133,8 @@ def run_gdn(args):
     if m.moe_query_device_status(ws) != 0:
         raise RuntimeError("device status after the timed region")
     e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        g_e2e.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        g_e2e.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1) / e_steps
+    pipelined_graph_e2e(torch, g_in, g_comp, g_out, 3)
+    e_ms = pipelined_graph_e2e(torch, g_in, g_comp, g_out, e_steps)
     if world > 1:
         e_ms = max_over_ranks(e_ms, dist, dev)
     hbm, _, _, src = peaks()
@@ -1121,11 +1160,13 @@ def run_gdn(args):
                      "ms_per_launch": round(per_launch_ms, 5),
                      "algorithmic_bytes_per_launch": ub},
         "e2e": {"value": round(job_throughput(T, world, e_ms), 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in pins)),
-                "d2h_bytes_per_step": int(o_pin.numel() * 2), "steps": e_steps,
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in pins[0])),
+                "d2h_bytes_per_step": int(o_pin[0].numel() * 2), "steps": e_steps,
                 "ms_per_step": round(e_ms, 5),
-                "mode": "CUDA graph of the first layer's input copies, the 30 moe_gdn_chunked_scan"
-                        " calls and the read-back"},
+                "mode": "CUDA graph of the %d moe_gdn_chunked_scan calls on the compute "
+                        "stream; each step's first-layer input copies and read-back on a copy "
+                        "stream, double-buffered so that they overlap the neighbouring steps"
+                        % c["layers"]},
         "gpu_launches": 2 * c["layers"] * args.steps,
         "launch_mode": "CUDA graph replay (prep and scan kernels per layer)",
         "clocks": clocks,
