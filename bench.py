@@ -551,25 +551,34 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    step_ev[0].record(stream)
-    for i in range(args.steps):
-        if G.fused:
+    if G.fused:
+        step_ev[0].record(stream)
+        for i in range(args.steps):
             G.g_step.replay()
-        else:
+            step_ev[i + 1].record(stream)
+    else:
+        # An event between two kernels ends their programmatic dependent
+        # launch, so the K steps that give the value carry events only at
+        # their two ends; a second pass of the same steps with an event
+        # between steps gives the per-step spread, and a third with events
+        # around the FFN call that call's own duration (its roofline).
+        t_a = torch.cuda.Event(enable_timing=True)
+        t_b = torch.cuda.Event(enable_timing=True)
+        t_a.record(stream)
+        for i in range(args.steps):
             G.step()
-        step_ev[i + 1].record(stream)
-    if not G.fused:
-        # the FFN call's own duration, for its roofline: a second pass of the
-        # same steps with events around the call (an event between two
-        # kernels ends their programmatic dependent launch, so the steps of
-        # the first pass carry none)
+        t_b.record(stream)
+        step_ev[0].record(stream)
+        for i in range(args.steps):
+            G.step()
+            step_ev[i + 1].record(stream)
         for i in range(args.steps):
             G.step(ffn_ev[i])
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     if world > 1:
         dist.barrier()
-    ms = step_ev[0].elapsed_time(step_ev[-1])
+    ms = step_ev[0].elapsed_time(step_ev[-1]) if G.fused else t_a.elapsed_time(t_b)
     per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     if G.persistent:  # the unit is one launch of the persistent kernel (all layers)
         ffn_ms = ms / args.steps / G.launches_per_step()
@@ -671,8 +680,9 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
         "gpu_launches": G.launches_per_step() * args.steps,
         "launch_mode": ("CUDA graph replay of one cooperative launch per step" if G.persistent
                         else "CUDA graph replay, programmatic dependent launch" if G.fused
-                        else "eager stream launches (the FFN call's duration from a second "
-                             "pass of the same steps with events around it)"),
+                        else "eager stream launches; value from K steps with events at their "
+                             "ends only, step_ms from a second pass with an event per step, the "
+                             "FFN call's duration from a third with events around it"),
         "clocks": clocks,
     }
     unit_bytes = (algo_bytes * len(G.layers) // G.launches_per_step() if G.persistent
