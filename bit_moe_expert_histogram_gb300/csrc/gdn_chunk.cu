@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kThr, 1)
     // (1) W2 S0^T and (2) Q S0^T over j = 0..127
     float au[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, aq[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
     const int ra = 16 * mt + gq;
-#pragma unroll 2
+#pragma unroll
     for (int kb = 0; kb < kDK / 8; ++kb) {
       const int j = 8 * kb + cq;
       uint32_t wh[4], wl[4], qa[4];
@@ -818,7 +818,9 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncthreads();
     // (3) O = g Q S0^T + P U; P is zero above the diagonal
     float ao[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-    for (int kb = 0; kb <= 2 * mt + 1; ++kb) {
+#pragma unroll
+    for (int kb = 0; kb < kCh / 8; ++kb) {
+      if (kb > 2 * mt + 1) break;  // P is zero above the diagonal
       const int sc = 8 * kb + cq;
       uint32_t ph[4], pl[4];
       split_tf32(P[sc * kTcLdT + ra], ph[0], pl[0]);
@@ -858,7 +860,7 @@ __global__ void __launch_bounds__(kThr, 1)
         const int i = 16 * ms + gq + 8 * (e >> 1), j = 8 * (ns0 + u) + 2 * cq + (e & 1);
         as[u][e] = gC * ST[j * kTcLdS + i];
       }
-#pragma unroll 2
+#pragma unroll
     for (int kb = 0; kb < kCh / 8; ++kb) {
       const int t = 8 * kb + cq;
       const int ia = 16 * ms + gq;
