@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kAThreads)
     const int gg = pr / rows, r = pr - gg * rows, d = dsl * 32 + lane;
     const float* pg = part + (size_t)gg * n_chunks * stride;
     float M = -INFINITY, Ls = 0.0f, Os = 0.0f;
-#pragma unroll 8
+#pragma unroll 16  // 16 chunks' loads in flight (8: 2.4% slower at 32K, 24: 26%)
     for (int cc = warp; cc < n_chunks; cc += kAWarps) {
       const float* pc = pg + cc * stride;
       const float mc = __ldcg(pc + r), lc = __ldcg(pc + kARows + r);

@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
     float* out = P + (size_t)s * T * E;
     const int c_begin = half * (kRtTile / 2), c_end = c_begin + kRtTile / 2;
-#pragma unroll 1
+#pragma unroll
     for (int c0 = c_begin; c0 < c_end; c0 += 32) {
       uint32_t v[16], u[16];
       tmem_ld16r(taddr + c0, v);
