@@ -361,12 +361,13 @@ class GpuWorkload:
     def launches_per_step(self):
         """Kernel launches of one step: the persistent decode kernel runs up
         to 48 layers per launch; the per-layer decode path launches route,
-        gate_up, down per layer; otherwise route 2, plan 2, activation
-        gather 1, ffn 2, combine 1."""
+        gate_up, down per layer; otherwise route 2, plan 1 (the router's
+        screen counts the plan's histogram from 64 tokens on, else 2),
+        activation gather 1, ffn 2, combine 1."""
         calls = self.n_chunks * len(self.layers)
         if self.persistent:
             return -(-len(self.layers) // 48)
-        return (3 if self.fused else 8) * calls
+        return (3 if self.fused else 7 if self.T >= 64 else 8) * calls
 
     def capture(self):
         """CUDA graphs of the device step and of the host-buffer step (the
@@ -392,7 +393,9 @@ class GpuWorkload:
         torch.cuda.synchronize()
 
     def step(self, ev_pairs=None):
-        """One pass of the hot path over the step's tokens (device-resident)."""
+        """One pass of the hot path over the step's tokens (device-resident):
+        each layer one moe_layer_w4 call; with ev_pairs, each layer as the
+        four calls with events around the first layer's moe_expert_ffn_w4."""
         m, S, T = self.m, self.S, self.T
         nl = len(self.layers)
         if self.block:  # every decoder block in one call, h_0 from the token ids
@@ -406,6 +409,13 @@ class GpuWorkload:
             x = self.x_all[c * T:(c + 1) * T]
             for l, (wr, bias, ex, sh) in enumerate(self.layers):
                 last = l == nl - 1
+                if ev_pairs is None:
+                    y = self.y_out[c * T:(c + 1) * T] if last else self.y
+                    xn = None if last else (self.xa if l % 2 == 0 else self.xb)
+                    m.moe_layer_w4(self.shape, x, wr, bias, ex, sh, y, self.ws, x_next=xn,
+                                   topk_ids=self.ids, topk_w=self.w)
+                    x = xn
+                    continue
                 m.moe_route(self.shape, x, wr, bias, self.ids, self.w, self.ws)
                 m.moe_plan(self.shape, self.ids, self.plan, self.ws)
                 if ev_pairs is not None:
@@ -680,9 +690,11 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
         "gpu_launches": G.launches_per_step() * args.steps,
         "launch_mode": ("CUDA graph replay of one cooperative launch per step" if G.persistent
                         else "CUDA graph replay, programmatic dependent launch" if G.fused
-                        else "eager stream launches; value from K steps with events at their "
-                             "ends only, step_ms from a second pass with an event per step, the "
-                             "FFN call's duration from a third with events around it"),
+                        else "eager stream launches, one moe_layer_w4 call per layer (programmatic "
+                             "dependent launch between its kernels); value from K steps with "
+                             "events at their ends only, step_ms from a second pass with an event "
+                             "per step, the FFN call's duration from a third pass of the four "
+                             "calls with events around moe_expert_ffn_w4"),
         "clocks": clocks,
     }
     unit_bytes = (algo_bytes * len(G.layers) // G.launches_per_step() if G.persistent

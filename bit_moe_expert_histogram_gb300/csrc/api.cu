@@ -433,6 +433,25 @@ moe_status_t moe_workspace_init(void* ws_dev, size_t ws_bytes, moe_stream_t stre
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_workspace_init");
 }
 
+// The tensor-core router (route_tc_supported shapes); hist != nullptr also
+// has its screen count the plan's chunk histogram into hist.
+static moe_status_t route_tc(const moe_shape_t* shape, const void* x_dev,
+                             const void* w_router_dev, const float* router_bias_dev,
+                             int32_t* ids, float* w, uint8_t* ws, const Layout& L,
+                             cudaStream_t st, int32_t* hist) {
+  CUtensorMap tw, tx;
+  MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_router_dev, shape->H, shape->E, 64,
+                 128, CU_TENSOR_MAP_SWIZZLE_128B));
+  MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_dev, shape->H, shape->T, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B));
+  cudaError_t e = launch_route_tc(
+      tw, tx, static_cast<const uint16_t*>(x_dev), static_cast<const uint16_t*>(w_router_dev),
+      router_bias_dev, shape->T, shape->H, shape->E, shape->K,
+      reinterpret_cast<float*>(ws + L.rpart), ids, w, reinterpret_cast<Ctrl*>(ws + L.ctrl), st,
+      hist, kPlanChunk);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
+}
+
 moe_status_t moe_route(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
                        const float* router_bias_dev, int32_t* topk_ids_dev, float* topk_w_dev,
                        void* ws_dev, size_t ws_bytes, moe_stream_t stream) {
@@ -442,19 +461,9 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x_dev, const void* 
   MOE_TRY(check_ws(shape, ws_dev, ws_bytes));
   uint8_t* ws = static_cast<uint8_t*>(ws_dev);
   const Layout L = layout_of(shape);
-  if (route_tc_supported(shape->T, shape->H, shape->E, shape->K)) {
-    CUtensorMap tw, tx;
-    MOE_TRY(map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_router_dev, shape->H, shape->E, 64,
-                   128, CU_TENSOR_MAP_SWIZZLE_128B));
-    MOE_TRY(map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_dev, shape->H, shape->T, 64, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B));
-    cudaError_t e = launch_route_tc(
-        tw, tx, static_cast<const uint16_t*>(x_dev), static_cast<const uint16_t*>(w_router_dev),
-        router_bias_dev, shape->T, shape->H, shape->E, shape->K,
-        reinterpret_cast<float*>(ws + L.rpart), topk_ids_dev, topk_w_dev,
-        reinterpret_cast<Ctrl*>(ws + L.ctrl), (cudaStream_t)stream);
-    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
-  }
+  if (route_tc_supported(shape->T, shape->H, shape->E, shape->K))
+    return route_tc(shape, x_dev, w_router_dev, router_bias_dev, topk_ids_dev, topk_w_dev, ws, L,
+                    (cudaStream_t)stream, nullptr);
   cudaError_t e = launch_route(static_cast<const uint16_t*>(x_dev),
                                static_cast<const uint16_t*>(w_router_dev), router_bias_dev,
                                shape->T, shape->H, shape->E, shape->K,
@@ -552,8 +561,20 @@ moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const voi
     cudaError_t e = launch_decode_layer(d, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
   }
-  MOE_TRY(moe_route(shape, x_dev, w_router_dev, router_bias_dev, ids, w, ws_dev, ws_bytes, stream));
-  MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
+  if (route_tc_supported(shape->T, shape->H, shape->E, shape->K)) {
+    // moe_route + moe_plan with the plan's histogram counted by the router's
+    // screen: one launch fewer, the same ids, weights and plan
+    int32_t* hist = reinterpret_cast<int32_t*>(ws + L.hist);
+    MOE_TRY(route_tc(shape, x_dev, w_router_dev, router_bias_dev, ids, w, ws, L, st, hist));
+    cudaError_t e = launch_plan(ids, shape->T, shape->K, shape->E, shape->n_shared,
+                                shape->tile_rows, plan, hist, reinterpret_cast<Ctrl*>(ws + L.ctrl),
+                                kPlanChunk, st, true);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_plan launch");
+  } else {
+    MOE_TRY(moe_route(shape, x_dev, w_router_dev, router_bias_dev, ids, w, ws_dev, ws_bytes,
+                      stream));
+    MOE_TRY(moe_plan(shape, ids, &plan, ws_dev, ws_bytes, stream));
+  }
   MOE_TRY(run_ffn(shape, x_dev, experts, shared, &plan, y_slots, ws, st));
   return moe_combine(shape, y_slots, plan.row_pos_dev, w, y_dev, x_next_dev, stream);
 }

@@ -117,14 +117,15 @@ bool route_tc_supported(int T, int H, int E, int K);
 size_t route_tc_partial_floats(int T, int H, int E);
 cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const uint16_t* x,
                             const uint16_t* wr, const float* bias, int T, int H, int E, int K,
-                            float* part, int32_t* ids, float* w, Ctrl* ctrl, cudaStream_t stream);
+                            float* part, int32_t* ids, float* w, Ctrl* ctrl, cudaStream_t stream,
+                            int32_t* hist = nullptr, int chunk = 0);
 
 cudaError_t launch_route(const uint16_t* x, const uint16_t* wr, const float* bias, int T, int H,
                          int E, int K, float* logits, int32_t* ids, float* w,
                          cudaStream_t stream);
 cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, int BM,
                         const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, int chunk,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool hist_ready = false);
 cudaError_t launch_ffn_gate_up(const CUtensorMap& tw, const CUtensorMap& twsh,
                                const CUtensorMap& tx, const FfnArgs& a, int grid,
                                cudaStream_t stream);

@@ -8,7 +8,8 @@
 // and deterministic.
 //
 // Two launches. plan_hist: block c counts the experts of items
-// [c*CH, (c+1)*CH) into hist[c][E]. plan_scatter: block c derives the
+// [c*CH, (c+1)*CH) into hist[c][E] (the layer call has the router's screen
+// count them instead and launches plan_scatter alone). plan_scatter: block c derives the
 // global offsets and its own starting position per expert from all blocks'
 // histograms, then scatters its items in ascending order, 256 per round,
 // ranking equal experts inside a warp with match.any and across warps with
@@ -200,12 +201,14 @@ __global__ void __launch_bounds__(kPlanThreads)
 
 cudaError_t launch_plan(const int32_t* ids, int T, int K, int E, int n_shared, int BM,
                         const moe_plan_t& plan, int32_t* hist, Ctrl* ctrl, int chunk,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool hist_ready) {
   const int R = T * K;
   const int nchunks = (R + chunk - 1) / chunk;
-  cudaError_t err = launch_pdl(plan_hist_kernel, dim3(nchunks), dim3(kPlanThreads), 0, stream, ids,
-                               R, E, chunk, hist, ctrl);
-  if (err != cudaSuccess) return err;
+  if (!hist_ready) {  // else the router's screen counted the chunks already
+    cudaError_t err = launch_pdl(plan_hist_kernel, dim3(nchunks), dim3(kPlanThreads), 0, stream,
+                                 ids, R, E, chunk, hist, ctrl);
+    if (err != cudaSuccess) return err;
+  }
   return launch_pdl(plan_scatter_kernel, dim3(nchunks), dim3(kPlanThreads), 0, stream, ids, T, K,
                     E, n_shared, BM, hist, nchunks, chunk, plan);
 }

@@ -20,6 +20,10 @@
 //                       top K is taken among them exactly as topk_warp does.
 // The selected ids and weights are therefore bit-identical to the CUDA-core
 // path; only the work to find them changes.
+// Inside the layer call the screen also counts its selections into the
+// plan's per-chunk expert histogram (hist[f / chunk][e] for item f = t*K + k,
+// zeroed by route_mma_kernel), which replaces the plan's histogram launch;
+// the counts are integers, so the order of the atomic adds does not matter.
 #include "common.cuh"
 #include "kernels.h"
 #include "topk.cuh"
@@ -45,7 +49,8 @@ constexpr int kScreenMaxJ = 8;          // H / 256 at most (the row in registers
 // columns 128..255).
 __global__ void __launch_bounds__(kRtThreads, 1)
     route_mma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                     int T, int E, float* __restrict__ P, float* __restrict__ Wn, Ctrl* ctrl) {
+                     int T, int E, float* __restrict__ P, float* __restrict__ Wn, Ctrl* ctrl,
+                     int32_t* __restrict__ hist, int hist_n) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -72,6 +77,11 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // everything above reads no global memory
   pdl_trigger();
+  if (hist) {  // the plan histogram that the screen fills
+    const int nblk = gridDim.x * gridDim.y * gridDim.z;
+    const int bid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    for (int i = bid * kRtThreads + threadIdx.x; i < hist_n; i += nblk * kRtThreads) hist[i] = 0;
+  }
   volatile int never = 0;
   bool ok = true;
   if (threadIdx.x == 0) {
@@ -168,7 +178,8 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
     route_screen_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                         const float* __restrict__ bias, const float* __restrict__ P,
                         const float* __restrict__ Wn, int T, int H, int E, int K, int S,
-                        int32_t* __restrict__ ids, float* __restrict__ w) {
+                        int32_t* __restrict__ ids, float* __restrict__ w,
+                        int32_t* __restrict__ hist, int chunk) {
   __shared__ float wn[kScreenMaxE];
   __shared__ float cval[kScreenWarps][kScreenMaxE];
   __shared__ int cid[kScreenWarps][kScreenMaxE];
@@ -360,8 +371,10 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, d);
   if (lane < K) {
-    ids[(size_t)t * K + lane] = (int)(0xFFFFFFFFu - (uint32_t)mine);
+    const int id = (int)(0xFFFFFFFFu - (uint32_t)mine);
+    ids[(size_t)t * K + lane] = id;
     w[(size_t)t * K + lane] = ex / z;
+    if (hist) atomicAdd(hist + (size_t)((t * K + lane) / chunk) * E + id, 1);
   }
 }
 
@@ -376,7 +389,8 @@ size_t route_tc_partial_floats(int T, int H, int E) {
 
 cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, const uint16_t* x,
                             const uint16_t* wr, const float* bias, int T, int H, int E, int K,
-                            float* part, int32_t* ids, float* w, Ctrl* ctrl, cudaStream_t stream) {
+                            float* part, int32_t* ids, float* w, Ctrl* ctrl, cudaStream_t stream,
+                            int32_t* hist, int chunk) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(route_mma_kernel,
@@ -388,12 +402,13 @@ cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, co
   float* P = part;
   float* Wn = part + (size_t)S * T * E;
   dim3 grid((T + kRtTile - 1) / kRtTile, (E + kRtTile - 1) / kRtTile, S);
+  const int hist_n = hist ? (T * K + chunk - 1) / chunk * E : 0;
   cudaError_t err = launch_pdl(route_mma_kernel, grid, dim3(kRtThreads), kRtSmem, stream, tm_w,
-                               tm_x, T, E, P, Wn, ctrl);
+                               tm_x, T, E, P, Wn, ctrl, hist, hist_n);
   if (err != cudaSuccess) return err;
   return launch_pdl(route_screen_kernel, dim3((T + kScreenWarps - 1) / kScreenWarps),
                     dim3(kScreenWarps * 32), 0, stream, x, wr, bias, (const float*)P,
-                    (const float*)Wn, T, H, E, K, S, ids, w);
+                    (const float*)Wn, T, H, E, K, S, ids, w, hist, chunk);
 }
 
 }  // namespace moe

@@ -177,7 +177,10 @@ moe_status_t moe_combine(const moe_shape_t* shape, const void* y_slots_dev,
  * intermediate in the workspace. Small T takes fused decode kernels that
  * stream only the selected experts' packed bytes ([Lily] "Decode").
  * Results equal the four calls above within the FFN's fp32 tolerance;
- * routing is bit-identical. topk_ids_dev / topk_w_dev may be NULL. */
+ * routing and the plan are bit-identical. Where moe_route takes its
+ * tensor-core screen (T >= 64), the screen also counts the plan's per-chunk
+ * expert histogram (integer atomic adds), so the plan's histogram launch is
+ * skipped. topk_ids_dev / topk_w_dev may be NULL. */
 moe_status_t moe_layer_w4(const moe_shape_t* shape, const void* x_dev, const void* w_router_dev,
                           const float* router_bias_dev, const moe_w4_weights_t* experts,
                           const moe_w4_weights_t* shared, void* y_dev, void* x_next_dev,

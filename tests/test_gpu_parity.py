@@ -295,6 +295,27 @@ def test_layer_call_equals_four_calls_and_oracle():
     close(f64(xn4), f64(oracle.rmsnorm_rows(y4)), "x_next")
 
 
+@pytest.mark.parametrize("T,zipf", [(64, 0.0), (77, 0.0), (2048, 1.1)])
+def test_layer_call_plan_counted_by_router_screen(T, zipf):
+    """From 64 tokens the layer call has the router's screen count the plan's
+    per-chunk histogram (no histogram launch): the same ids, weights and y as
+    the four calls, at the threshold, with a ragged last chunk and with
+    skewed routing; a second call on the same workspace (the histogram zeroed
+    again) gives the same bits."""
+    L = layer(T, FULL, 3, zipf)
+    c = Case(L, T, FULL)
+    c.run_calls()
+    ids4, w4, y4 = c.ids.cpu().numpy().copy(), c.w.cpu().numpy().copy(), h16(c.y).copy()
+    for _ in range(2):
+        c.ids.fill_(-7)
+        c.w.zero_()
+        c.y.zero_()
+        c.run_layer()
+        assert np.array_equal(c.ids.cpu().numpy(), ids4)
+        assert np.array_equal(c.w.cpu().numpy(), w4)
+        assert np.array_equal(h16(c.y), y4)
+
+
 def test_determinism_two_runs():
     L = layer(512, FULL, 0)
     c = Case(L, 512, FULL)
