@@ -686,6 +686,18 @@ __global__ void __launch_bounds__(kPsThreads, 1)
           st_tag(a.h_tag + (size_t)tau * kLine + col * 4 + row, ep, hb | (hi << 16));
         }
       }
+      // the next layer's rows of this shared tile go to L2 now, so that its
+      // shared tiles do not share the HBM with the routed rows after its top-K
+      if (!routed && l + 1 < a.n_layers && lane == 0) {
+        const moe_w4_weights_t& nw = a.layer[l + 1].shared;
+        if (qs < 2) {
+          bulk_prefetch_l2(nw.q_gate_up_dev + (size_t)(qs * I + j0) * wpr, 8u * wpr * 4u);
+        } else {
+          const uint16_t* sb = qs == 2 ? nw.s_gate_up_dev : nw.b_gate_up_dev;
+          bulk_prefetch_l2(sb + (size_t)j0 * gpr, 8u * gpr * 2u);
+          bulk_prefetch_l2(sb + (size_t)(I + j0) * gpr, 8u * gpr * 2u);
+        }
+      }
     }
     if (!pref) prefetch_down();
     // ------------------------------------------------------------ down --
