@@ -26,7 +26,9 @@
 // the chunks (at most one CTA per SM over all groups, every CTA resident:
 // a cooperative launch) write partials, meet at a grid barrier, and merge
 // them: each CTA takes 32 output elements of one query row, its four warps
-// a quarter of the chunks each.
+// a quarter of the chunks each. The launch allows programmatic dependent
+// launch, so consecutive calls overlap their launch with the previous
+// call's tail.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -92,6 +94,11 @@ __global__ void __launch_bounds__(kAThreads)
   const int group = n_q / n_kv, rows = group * T;
   const int nblk = (L + kAB - 1) / kAB;
   const int b0 = c * cb, b1 = min(b0 + cb, nblk);
+  // programmatic dependent launch: the next call's CTAs may be placed while
+  // this call runs, but nothing before this wait reads or writes global
+  // memory (q, the cache and the workspace all come from earlier work)
+  pdl_wait();
+  pdl_trigger();
   // Q fragments (rows r = t * group + head in group; rows >= rows are zero)
   uint32_t qa[kKS][4];
   {
@@ -400,16 +407,18 @@ cudaError_t launch_attn_decode(const moe_attn_shape_t* s, const CUtensorMap& tm_
   const int cb = (nblk + per_group - 1) / per_group;
   const int n_chunks = (nblk + cb - 1) / cb;
   const size_t smem = attn_smem(s->D);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_chunks, s->n_kv);
   cfg.blockDim = dim3(kAThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = n_chunks > 1 ? 1 : 0;  // the grid barrier needs every CTA resident
+  cfg.numAttrs = n_chunks > 1 ? 2 : 1;  // the grid barrier needs every CTA resident
   cudaError_t e;
   if (s->D == 64) {
     e = cudaFuncSetAttribute(attn_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
