@@ -561,7 +561,17 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
     if sampler:
         sampler.start()
         time.sleep(0.3)
+    t_a = torch.cuda.Event(enable_timing=True)
+    t_b = torch.cuda.Event(enable_timing=True)
     if G.fused:
+        # the value from K graph replays with events at their two ends (an
+        # event between two launches ends their programmatic dependent
+        # launch), the per-step spread from a second pass with an event
+        # between replays
+        t_a.record(stream)
+        for i in range(args.steps):
+            G.g_step.replay()
+        t_b.record(stream)
         step_ev[0].record(stream)
         for i in range(args.steps):
             G.g_step.replay()
@@ -572,8 +582,6 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
         # their two ends; a second pass of the same steps with an event
         # between steps gives the per-step spread, and a third with events
         # around the FFN call that call's own duration (its roofline).
-        t_a = torch.cuda.Event(enable_timing=True)
-        t_b = torch.cuda.Event(enable_timing=True)
         t_a.record(stream)
         for i in range(args.steps):
             G.step()
@@ -588,7 +596,7 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
     clocks = sampler.stop() if sampler else None
     if world > 1:
         dist.barrier()
-    ms = step_ev[0].elapsed_time(step_ev[-1]) if G.fused else t_a.elapsed_time(t_b)
+    ms = t_a.elapsed_time(t_b)
     per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     if G.persistent:  # the unit is one launch of the persistent kernel (all layers)
         ffn_ms = ms / args.steps / G.launches_per_step()
@@ -688,8 +696,13 @@ def measure_workload(args, wl, dev, m, rank, world, dist, cpu_budget):
                               "they overlap the neighbouring chunks' layers"),
                 "eager_value": round(job_throughput(G.tokens_per_step, world, e_eager_ms), 2)},
         "gpu_launches": G.launches_per_step() * args.steps,
-        "launch_mode": ("CUDA graph replay of one cooperative launch per step" if G.persistent
-                        else "CUDA graph replay, programmatic dependent launch" if G.fused
+        "launch_mode": ("CUDA graph replay of one cooperative launch per step (programmatic "
+                        "dependent launch between steps); value from K replays with events at "
+                        "their ends only, step_ms from a second pass with an event per replay"
+                        if G.persistent
+                        else "CUDA graph replay, programmatic dependent launch; value from K "
+                             "replays with events at their ends only, step_ms from a second pass "
+                             "with an event per replay" if G.fused
                         else "eager stream launches, one moe_layer_w4 call per layer (programmatic "
                              "dependent launch between its kernels); value from K steps with "
                              "events at their ends only, step_ms from a second pass with an event "
@@ -987,7 +1000,9 @@ def run_attn(args):
                         "each step's q copy and read-back on a copy stream, double-buffered so "
                         "that they overlap the neighbouring steps" % c["layers"]},
         "gpu_launches": c["layers"] * args.steps,
-        "launch_mode": "CUDA graph replay (one cooperative launch per layer, merge inside)",
+        "launch_mode": "CUDA graph replay (one cooperative launch per layer, merge inside, "
+                       "programmatic dependent launch between layers); events at the ends of "
+                       "the K steps only",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1149,7 +1164,7 @@ def run_gdn(args):
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     per = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(per)
+    ms = evs[0][0].elapsed_time(evs[-1][1])  # the gaps between steps included
     if world > 1:
         ms = max_over_ranks(ms, dist, dev)
     if m.moe_query_device_status(ws) != 0:
@@ -1190,7 +1205,9 @@ def run_gdn(args):
                         "stream, double-buffered so that they overlap the neighbouring steps"
                         % c["layers"]},
         "gpu_launches": 2 * c["layers"] * args.steps,
-        "launch_mode": "CUDA graph replay (prep and scan kernels per layer)",
+        "launch_mode": "CUDA graph replay (prep and scan kernels per layer); value from the "
+                       "first step's start to the last one's end, step_ms from the event pair "
+                       "around each replay",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

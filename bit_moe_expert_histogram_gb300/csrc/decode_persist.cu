@@ -401,6 +401,10 @@ __global__ void __launch_bounds__(kPsThreads, 1)
   // decoder blocks: the residual stream h of this layer, pair layout [T][H/8]
   uint4* rp = reinterpret_cast<uint4*>(
       (reinterpret_cast<uintptr_t>(yv + (size_t)nud * kPsGroup) + 15) & ~(uintptr_t)15);
+  // programmatic dependent launch: the blocks may be placed while the
+  // previous launch runs; nothing before this wait touches global memory
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) S.seq = *reinterpret_cast<volatile unsigned*>(&ctrl->ps_seq);
   __syncthreads();
   const uint32_t base = S.seq * kPsEpochStride + 1u;
@@ -892,16 +896,18 @@ bool persist_config(int T, int H, int E, int K, int I, int ns, int* grid, size_t
 
 cudaError_t launch_decode_persist(const PersistArgs& a, int grid, size_t smem,
                                   cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kPsThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (a.block) {
     switch (a.I) {
       case 128: return cudaLaunchKernelEx(&cfg, dec_persist_kernel<128, true>, a);
