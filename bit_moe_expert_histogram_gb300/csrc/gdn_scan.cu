@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kGThreads)
   const size_t srow0 = ((size_t)h * dv + r0) * DK + 4 * lane;
   const size_t srow1 = srow0 + DK;
   float s0[4], s1[4];
+  pdl_wait();  // programmatic dependent launch: global memory only after this
+  pdl_trigger();
   {
     const float4 a = *reinterpret_cast<const float4*>(s_in + srow0);
     const float4 b = *reinterpret_cast<const float4*>(s_in + srow1);
@@ -130,9 +132,8 @@ cudaError_t launch_gdn_scan(const moe_gdn_shape_t* s, const uint16_t* q, const u
                             const uint16_t* v, const float* alpha, const float* beta,
                             const float* s_in, float* s_out, uint16_t* o, cudaStream_t stream) {
   dim3 grid(s->n_v, s->dv / kGRows);
-  gdn_scan_kernel<<<grid, kGThreads, 0, stream>>>(q, k, v, alpha, beta, s_in, s_out, o, s->T,
-                                                  s->n_k, s->n_v, s->dv);
-  return cudaGetLastError();
+  return launch_pdl(gdn_scan_kernel, grid, dim3(kGThreads), 0, stream, q, k, v, alpha, beta, s_in,
+                    s_out, o, s->T, s->n_k, s->n_v, s->dv);
 }
 
 }  // namespace moe
