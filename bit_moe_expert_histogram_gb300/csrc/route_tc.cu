@@ -37,7 +37,7 @@ constexpr int kRtKB = 4;                // 64-element K blocks per CTA (a 256-wi
 constexpr int kRtThreads = 256;
 constexpr int kRtBlock = kRtTile * 128; // bytes of one 128-row x 64-element bf16 tile
 constexpr int kRtSmem = 2 * kRtKB * kRtBlock + 1024 + 64;
-constexpr int kScreenWarps = 4;        // tokens per screen block (one warp each)
+constexpr int kScreenWarps = 4;        // warps per screen block (one or two per token)
 constexpr int kScreenMaxE = 256;        // 8 experts per lane in the screen
 constexpr int kScreenMaxJ = 8;          // H / 256 at most (the row in registers; K slices)
 
@@ -170,10 +170,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
 }
 
-// One warp per token, kScreenWarps tokens per block, no barrier after the
-// expert norms: the warp forms the candidate set, computes the candidates'
-// fixed-order logits four at a time (four independent chains per lane) and
-// selects the top K among them. See the file comment.
+// SPLIT warps per token, kScreenWarps / SPLIT tokens per block, no barrier
+// after the expert norms: each warp of a token forms the token's candidate
+// set (the same set in each), computes every SPLIT-th batch of four
+// candidates' fixed-order logits (four independent chains per lane), and the
+// token's first warp selects the top K among them. Two warps per token halve
+// the rounds of candidate loads while every token's warps are resident at
+// once; past that, one warp per token. See the file comment.
+template <int SPLIT>
 __global__ void __launch_bounds__(kScreenWarps * 32)
     route_screen_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                         const float* __restrict__ bias, const float* __restrict__ P,
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
   __shared__ unsigned long long ckey[kScreenWarps][kScreenMaxE];
   __shared__ unsigned long long csel[kScreenWarps][32];
   const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kScreenWarps + g;
+  const int t = blockIdx.x * (kScreenWarps / SPLIT) + g / SPLIT, sub = g % SPLIT, gk = g - sub;
   const bool active = t < T;
   const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)(active ? t : 0) * H);
   const int nj = H >> 8;  // at most kScreenMaxJ
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
   // order), four candidates at a time with every chunk of the four rows in
   // flight at once (one round trip per round); a missing fourth repeats the
   // first
-  for (int c0 = 0; c0 < nc; c0 += 4) {
+  for (int c0 = 4 * sub; c0 < nc; c0 += 4 * SPLIT) {
     int e4[4];
     const uint4* wq[4];
 #pragma unroll
@@ -352,14 +356,19 @@ __global__ void __launch_bounds__(kScreenWarps * 32)
       for (int d = 16; d >= 1; d >>= 1)
         acc[m] = __fadd_rn(acc[m], __shfl_xor_sync(0xFFFFFFFFu, acc[m], d));
       if (lane == 0 && c0 + m < nc)
-        ckey[g][c0 + m] = topk_ckey(bias ? __fadd_rn(acc[m], bias[e4[m]]) : acc[m], e4[m]);
+        ckey[gk][c0 + m] = topk_ckey(bias ? __fadd_rn(acc[m], bias[e4[m]]) : acc[m], e4[m]);
     }
   }
-  __syncwarp();
+  if constexpr (SPLIT == 2) {  // the token's two warps: named barrier 1 + token slot
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + g / 2) : "memory");
+    if (sub) return;
+  } else {
+    __syncwarp();
+  }
   for (int i = lane; i < nc; i += 32) {
-    const unsigned long long ci = ckey[g][i];
+    const unsigned long long ci = ckey[gk][i];
     int rk = 0;
-    for (int j = 0; j < nc; ++j) rk += ckey[g][j] > ci;
+    for (int j = 0; j < nc; ++j) rk += ckey[gk][j] > ci;
     if (rk < K) csel[g][rk] = ci;
   }
   __syncwarp();
@@ -406,7 +415,23 @@ cudaError_t launch_route_tc(const CUtensorMap& tm_w, const CUtensorMap& tm_x, co
   cudaError_t err = launch_pdl(route_mma_kernel, grid, dim3(kRtThreads), kRtSmem, stream, tm_w,
                                tm_x, T, E, P, Wn, ctrl, hist, hist_n);
   if (err != cudaSuccess) return err;
-  return launch_pdl(route_screen_kernel, dim3((T + kScreenWarps - 1) / kScreenWarps),
+  // two warps per token while every token's warps fit on the device at once
+  static int warps_resident = 0;
+  if (warps_resident == 0) {
+    int dev = 0, nsm = 0, blocks = 0;
+    err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+      err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, route_screen_kernel<2>,
+                                                          kScreenWarps * 32, 0);
+    if (err != cudaSuccess) return err;
+    warps_resident = nsm * blocks * kScreenWarps;
+  }
+  if (2 * T <= warps_resident)
+    return launch_pdl(route_screen_kernel<2>, dim3((T + kScreenWarps / 2 - 1) / (kScreenWarps / 2)),
+                      dim3(kScreenWarps * 32), 0, stream, x, wr, bias, (const float*)P,
+                      (const float*)Wn, T, H, E, K, S, ids, w, hist, chunk);
+  return launch_pdl(route_screen_kernel<1>, dim3((T + kScreenWarps - 1) / kScreenWarps),
                     dim3(kScreenWarps * 32), 0, stream, x, wr, bias, (const float*)P,
                     (const float*)Wn, T, H, E, K, S, ids, w, hist, chunk);
 }
