@@ -21,6 +21,11 @@
  *    default stream) and never synchronise it, so they can be captured in a
  *    CUDA graph. The device that is current when a call is made must own all
  *    device pointers of that call.
+ *  - Kernels are launched with programmatic stream serialisation (the
+ *    cooperative ones too): a kernel may be placed on the device while the
+ *    work before it in the stream finishes, but it reads and writes no
+ *    global memory before that work has completed and its writes are
+ *    visible. To the caller the stream order is unchanged.
  *  - Argument and shape errors are returned before anything is enqueued.
  *    A failed launch returns MOE_ERR_CUDA (text in moe_last_error()).
  *    Errors found on the device (an expert id out of range, a bounded wait
