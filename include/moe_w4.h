@@ -21,8 +21,9 @@
  *    default stream) and never synchronise it, so they can be captured in a
  *    CUDA graph. The device that is current when a call is made must own all
  *    device pointers of that call.
- *  - Kernels are launched with programmatic stream serialisation (the
- *    cooperative ones too): a kernel may be placed on the device while the
+ *  - Kernels (all but those of the moe_debug_* calls) are launched with
+ *    programmatic stream serialisation, the cooperative ones included: a
+ *    kernel may be placed on the device while the
  *    work before it in the stream finishes, but it reads and writes no
  *    global memory before that work has completed and its writes are
  *    visible. To the caller the stream order is unchanged.
