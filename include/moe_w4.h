@@ -23,10 +23,10 @@
  *    device pointers of that call.
  *  - Kernels (all but those of the moe_debug_* calls) are launched with
  *    programmatic stream serialisation, the cooperative ones included: a
- *    kernel may be placed on the device while the
- *    work before it in the stream finishes, but it reads and writes no
- *    global memory before that work has completed and its writes are
- *    visible. To the caller the stream order is unchanged.
+ *    kernel may be placed on the device while the work before it in the
+ *    stream finishes, but it reads no data before the work that wrote it
+ *    has completed and writes nothing before the work before it has
+ *    completed. To the caller the stream order is unchanged.
  *  - Argument and shape errors are returned before anything is enqueued.
  *    A failed launch returns MOE_ERR_CUDA (text in moe_last_error()).
  *    Errors found on the device (an expert id out of range, a bounded wait
